@@ -1,0 +1,559 @@
+"""Throughput of one DDTree round on GB300: top-K -> heap build -> tree
+attention (one target layer) -> acceptance walk, through libddtree.so.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gb300|reference]
+
+Prints ONE JSON line (rank 0).  `value` is sequence-rounds per second with all
+inputs resident in HBM; a "step" is one round over one batch.  The round's four
+C-ABI calls are captured in CUDA graphs; to keep the 129 MB L2 from serving a
+step's inputs, steps rotate over R copies of every per-step input (R copies
+> 2x L2).  `e2e` repeats the measurement through the public API from pinned
+host buffers (inputs copied in and results copied out every step).
+`--impl reference` times the CPU oracle on the host cores instead (a reported
+baseline; it runs a bounded sample of the same workload per step).
+Multi-GPU runs are independent replicas (sequences are independent units).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from diffusion_draft_tree_gb300 import workloads as wl  # noqa: E402
+
+L2_BYTES = 129 * 2**20
+X36 = 36  # layers of the 8B-class target (Qwen3-8B)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="8b_single", choices=sorted(wl.CONFIGS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-x36", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work per launch (bytes that must move, flops that must run)
+# ---------------------------------------------------------------------------
+
+def work_model(w, tree_anc_total: int) -> dict:
+    R = w.N + 1
+    es = w.esize
+    topk_bytes = w.B * w.L * (w.V * es + w.K * 8 + 4)
+    kv_prefix = 4 * w.Hkv * w.D * sum(w.P)               # K + V, bf16
+    kv_tree = 4 * w.Hkv * w.D * R * w.B
+    qo = 4 * w.Hq * w.D * R * w.B                         # Q read + O written, bf16
+    attn_bytes = kv_prefix + kv_tree + qo
+    attn_flops = 4 * w.Hq * w.D * (R * sum(w.P)) + 4 * w.Hq * w.D * tree_anc_total
+    accept_bytes = w.B * R * w.V * es
+    build_bytes = w.B * (w.L * w.K * 8 + R * (7 * 4 + ((R + 31) // 32) * 4))
+    return {"topk": {"bytes": topk_bytes}, "build": {"bytes": build_bytes},
+            "tree_attn": {"bytes": attn_bytes, "flops": attn_flops},
+            "accept": {"bytes": accept_bytes}}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def to_dev_logits(a, dtype, dev):
+    import torch
+    if dtype == wl.BF16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+
+
+class Round:
+    """Device buffers and calls for one round over one copy of the inputs."""
+
+    def __init__(self, ops, w, inputs, dev, ws, layers=1):
+        import torch
+        self.ops, self.w = ops, w
+        self.inp = inputs
+        B, L, K, N = w.B, w.L, w.K, w.N
+        self.topk_idx = torch.empty((B * L, K), dtype=torch.int32, device=dev)
+        self.topk_lp = torch.empty((B * L, K), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((B * L,), dtype=torch.float32, device=dev)
+        self.tree = ops.tree_buffers(B, N, dev)
+        self.out = [torch.empty_like(inputs["q"][0]) for _ in range(layers)]
+        self.acc = ops.accept_buffers(B, L, N, dev)
+        self.ws = ws
+
+    def run(self, layers=1):
+        ops, w, x = self.ops, self.w, self.inp
+        ops.ddtree_topk(x["draft"], w.K, self.topk_idx, self.topk_lp, self.lse, self.ws["topk"])
+        ops.ddtree_build(self.topk_lp.view(w.B, w.L, w.K), self.topk_idx.view(w.B, w.L, w.K),
+                         x["bonus"], x["prefix_len"], w.N, self.tree)
+        for l in range(layers):
+            ops.ddtree_tree_attn(x["q"][l], x["k_cache"][l], x["v_cache"][l], x["k_tree"][l],
+                                 x["v_tree"][l], x["prefix_len"], self.tree["n_nodes"],
+                                 self.tree["anc_mask"], self.out[l], None, None,
+                                 self.ws["attn"])
+        ops.ddtree_accept(x["target"], self.tree["parent"], self.tree["token"],
+                          self.tree["n_nodes"], w.L, self.acc, w.T, wl.philox_seed(w), 0,
+                          self.ws["accept"])
+
+    def stages(self):
+        """The four calls as separate closures (for per-kernel event timing)."""
+        ops, w, x = self.ops, self.w, self.inp
+        return [
+            lambda: ops.ddtree_topk(x["draft"], w.K, self.topk_idx, self.topk_lp, self.lse,
+                                    self.ws["topk"]),
+            lambda: ops.ddtree_build(self.topk_lp.view(w.B, w.L, w.K),
+                                     self.topk_idx.view(w.B, w.L, w.K), x["bonus"],
+                                     x["prefix_len"], w.N, self.tree),
+            lambda: ops.ddtree_tree_attn(x["q"][0], x["k_cache"][0], x["v_cache"][0],
+                                         x["k_tree"][0], x["v_tree"][0], x["prefix_len"],
+                                         self.tree["n_nodes"], self.tree["anc_mask"],
+                                         self.out[0], None, None, self.ws["attn"]),
+            lambda: ops.ddtree_accept(x["target"], self.tree["parent"], self.tree["token"],
+                                      self.tree["n_nodes"], w.L, self.acc, w.T,
+                                      wl.philox_seed(w), 0, self.ws["accept"]),
+        ]
+
+
+def host_inputs(w):
+    return {"draft": wl.draft_logits(w).reshape(w.B * w.L, w.V), "bonus": wl.bonus_tokens(w),
+            "prefix_len": wl.prefix_lengths(w), "q": wl.queries(w), "k_cache": wl.kv_cache(w, 0),
+            "v_cache": wl.kv_cache(w, 1), "k_tree": wl.kv_tree(w, 0), "v_tree": wl.kv_tree(w, 1)}
+
+
+def gpu_arm(args, rank, world, dev):
+    import torch
+    from diffusion_draft_tree_gb300 import ops
+
+    w = wl.CONFIGS[args.workload]
+    torch.cuda.set_device(dev)
+    h = host_inputs(w)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(
+        torch.bfloat16)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+    ws = {"topk": ops.alloc_workspace(ops.workspace_size(ops.OP_TOPK, B=w.B, L=w.L, V=w.V,
+                                                         dtype=w.dtype), dev),
+          "attn": ops.alloc_workspace(ops.workspace_size(ops.OP_TREE_ATTN, B=w.B, N=w.N,
+                                                         Hq=w.Hq, Hkv=w.Hkv, D=w.D,
+                                                         cache_cap=w.P_cap), dev),
+          "accept": ops.alloc_workspace(ops.workspace_size(ops.OP_ACCEPT, B=w.B, N=w.N, V=w.V,
+                                                           dtype=w.dtype), dev)}
+    base = {"draft": to_dev_logits(h["draft"], w.dtype, dev), "bonus": i32(h["bonus"]),
+            "prefix_len": i32(h["prefix_len"]), "q": [bf(h["q"])], "k_cache": [bf(h["k_cache"])],
+            "v_cache": [bf(h["v_cache"])], "k_tree": [bf(h["k_tree"])],
+            "v_tree": [bf(h["v_tree"])]}
+    # target logits come from the tree the GPU builds for these draft logits
+    probe = Round(ops, w, dict(base, target=None), dev, ws)
+    probe.stages()[0]()
+    probe.stages()[1]()
+    depth = probe.tree["depth"].cpu().numpy()
+    h["target"] = wl.target_logits(w, wl.draft_logits(w), depth)
+    base["target"] = to_dev_logits(h["target"], w.dtype, dev)
+    torch.cuda.synchronize()
+
+    per_copy = sum(t.numel() * t.element_size() for k, t in base.items()
+                   if k in ("draft", "target")) + sum(
+        t[0].numel() * t[0].element_size() for k, t in base.items()
+        if k in ("q", "k_cache", "v_cache", "k_tree", "v_tree"))
+    R = max(2, min(64, int(np.ceil(3 * L2_BYTES / per_copy))))
+
+    def clone(src):
+        return {k: ([t.clone() for t in v] if isinstance(v, list) else v.clone())
+                for k, v in src.items()}
+
+    copies = [base] + [clone(base) for _ in range(R - 1)]
+    rounds = [Round(ops, w, c, dev, ws) for c in copies]
+    for r in rounds:  # eager warm-up outside capture (sets function attributes)
+        r.run()
+    torch.cuda.synchronize()
+    ops.ddtree_device_check()
+
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    g_all = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_all, stream=stream):
+        for r in rounds:
+            r.run()
+    g_one = []
+    for r in rounds:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            r.run()
+        g_one.append(g)
+
+    def replay(n):
+        for _ in range(n // R):
+            g_all.replay()
+        for c in range(n % R):
+            g_one[c].replay()
+
+    replay(max(args.warmup, 3) * 1)
+    torch.cuda.synchronize()
+    # sustained pre-run so that the clock samples see the GPU under this load
+    sampler = ClockSampler(torch.cuda.current_device() if dev.index is None else dev.index)
+    with sampler:
+        t_end = time.time() + 1.5
+        while time.time() < t_end:
+            replay(R * 16)
+            torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        replay(args.steps)
+        e1.record()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    ms_total = e0.elapsed_time(e1)
+    clocks = sampler.summary()
+
+    # per-kernel durations: external event nodes inside a captured graph
+    kern = {}
+    try:
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
+               for _ in range(R)]
+        g_ev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_ev, stream=stream):
+            for r, ev in zip(rounds, evs):
+                st = r.stages()
+                for i in range(4):
+                    ev[i].record()
+                    st[i]()
+                ev[4].record()
+        acc = np.zeros(4)
+        reps = max(4, min(200, args.steps // R))
+        for _ in range(reps):
+            g_ev.replay()
+            torch.cuda.synchronize()
+            for ev in evs:
+                acc += [ev[i].elapsed_time(ev[i + 1]) for i in range(4)]
+        kern_ms = acc / (reps * R)
+        kern_method = "external CUDA events between the four kernels inside the graph"
+    except Exception as e:  # noqa: BLE001
+        kern_ms = np.full(4, np.nan)
+        kern_method = f"unavailable: {e!r}"
+
+    # 36-layer round: 36 tree-attention launches, each on its own KV cache
+    x36 = None
+    if not args.no_x36:
+        layers = X36
+        cache_bytes = 2 * base["k_cache"][0].numel() * 2
+        if cache_bytes * layers < 40 * 2**30:
+            lay = dict(base)
+            for k in ("q", "k_cache", "v_cache", "k_tree", "v_tree"):
+                lay[k] = [base[k][0]] + [base[k][0].clone() for _ in range(layers - 1)]
+            r36 = Round(ops, w, lay, dev, ws, layers=layers)
+            r36.run(layers)
+            torch.cuda.synchronize()
+            g36 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g36, stream=stream):
+                r36.run(layers)
+            for _ in range(3):
+                g36.replay()
+            torch.cuda.synchronize()
+            n36 = max(10, min(200, args.steps // 10))
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record()
+            for _ in range(n36):
+                g36.replay()
+            a1.record()
+            torch.cuda.synchronize()
+            ms36 = a0.elapsed_time(a1) / n36
+            x36 = {"rounds_per_s": w.B * 1000.0 / ms36, "ms_per_round": ms36, "steps": n36,
+                   "layers": layers}
+            del r36, lay
+
+    # end to end through the public API, inputs from pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        def host_t(a):
+            a = np.ascontiguousarray(a)
+            return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
+
+        pin = {k: host_t(h[k]) for k in ("draft", "target", "q", "k_tree", "v_tree", "bonus",
+                                         "prefix_len")}
+        dst = copies[0]
+        out_pin = {k: torch.empty(rounds[0].acc[k].shape, dtype=torch.int32).pin_memory()
+                   for k in ("accept_len", "out_tokens", "next_bonus")}
+
+        def h2d(dst_t, src):
+            d = dst_t.view(torch.int16) if dst_t.dtype == torch.bfloat16 else dst_t
+            d.copy_(src.view(d.shape), non_blocking=True)
+
+        h2d_bytes = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h_bytes = sum(t.numel() * t.element_size() for t in out_pin.values())
+
+        def e2e_step():
+            for k in ("draft", "target", "bonus", "prefix_len"):
+                h2d(dst[k], pin[k])
+            for k in ("q", "k_tree", "v_tree"):
+                h2d(dst[k][0], pin[k])
+            rounds[0].run()
+            for k, t in out_pin.items():
+                t.copy_(rounds[0].acc[k], non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for _ in range(max(3, args.warmup // 4)):
+            e2e_step()
+        n_e2e = max(20, min(500, args.steps // 4))
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        t1 = time.perf_counter()
+        e2e = {"value": w.B * n_e2e / (t1 - t0), "unit": "rounds/s",
+               "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes),
+               "steps": n_e2e,
+               "note": "public Python API (ops.*) over the C ABI; pinned host inputs copied "
+                       "in and accept outputs copied out every step; the KV cache is "
+                       "device-resident state"}
+
+    ops.ddtree_device_check()
+    tree_anc = int(np.sum([bin(int(x)).count("1") for x in
+                           rounds[0].tree["anc_mask"].cpu().numpy().view(np.uint32).ravel()]))
+    return {"w": w, "ms_total": ms_total, "R": R, "per_copy": per_copy, "clocks": clocks,
+            "kern_ms": kern_ms, "kern_method": kern_method, "x36": x36, "e2e": e2e,
+            "tree_anc": tree_anc}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (reported baseline; also the `--impl reference` arm)
+# ---------------------------------------------------------------------------
+
+def oracle_step(o, w, h, attn_units):
+    t0 = time.perf_counter()
+    idx, _, lp32, _ = o.topk(h["draft"].reshape(w.B, w.L, w.V), w.dtype, w.K)
+    t1 = time.perf_counter()
+    tree = o.build_tree(lp32, idx, h["bonus"], h["prefix_len"], w.N)
+    t2 = time.perf_counter()
+    o.tree_attn(h["q"], h["k_cache"], h["v_cache"], h["k_tree"], h["v_tree"], h["prefix_len"],
+                tree["n_nodes"], tree["anc_mask"], units=attn_units)
+    t3 = time.perf_counter()
+    o.accept(h["target"], w.dtype, tree, w.L, temperature=w.T, seed=wl.philox_seed(w))
+    t4 = time.perf_counter()
+    scale_attn = (w.B * w.Hkv) / len(attn_units)
+    return (t1 - t0) + (t2 - t1) + (t3 - t2) * scale_attn + (t4 - t3)
+
+
+def oracle_setup(w):
+    import oracle
+    h = host_inputs(w)
+    draft = wl.draft_logits(w)
+    idx, _, lp32, _ = oracle.topk(draft, w.dtype, w.K)
+    tree = oracle.build_tree(lp32, idx, h["bonus"], h["prefix_len"], w.N)
+    h["target"] = wl.target_logits(w, draft, tree["depth"])
+    return oracle, h
+
+
+def cpu_baseline(w, seconds, steps=None):
+    o, h = oracle_setup(w)
+    units = [(0, 0)]  # one (sequence, KV head) unit of tree attention per step, scaled up
+    times = []
+    t_start = time.perf_counter()
+    while True:
+        times.append(oracle_step(o, w, h, units))
+        if steps is not None and len(times) >= steps:
+            break
+        if steps is None and (time.perf_counter() - t_start > seconds or len(times) >= 50):
+            break
+    per_step = float(np.mean(times))
+    sample = (f"{len(times)} rounds of '{w.name}': top-K, heap and walk in full; tree attention "
+              f"on 1 of {w.B * w.Hkv} (sequence, KV head) units, time scaled x{w.B * w.Hkv}")
+    return {"value": w.B / per_step, "unit": "rounds/s", "cores": 1, "kind": "oracle",
+            "sample": sample, "seconds_per_round": per_step}
+
+
+def reference_arm(args, rank, world):
+    w = wl.CONFIGS[args.workload]
+    if rank != 0:
+        return
+    o, h = oracle_setup(w)
+    units = [(0, 0)]
+    for _ in range(args.warmup):
+        oracle_step(o, w, h, units)
+    t = [oracle_step(o, w, h, units) for _ in range(args.steps)]
+    per_step = float(np.mean(t))
+    value = w.B / per_step
+    sample = (f"each step: one round of '{w.name}' with tree attention on 1 of "
+              f"{w.B * w.Hkv} (sequence, KV head) units, time scaled x{w.B * w.Hkv}")
+    line = {"impl": "reference", "metric": "draft-tree rounds/sec (topK+build+tree-attn+accept)",
+            "value": value, "unit": "rounds/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, None),
+            "cpu_baseline": {"value": value, "unit": "rounds/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "rounds/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, R):
+    c = {"workload": w.name, "B": w.B, "L": w.L, "V": w.V, "K": w.K, "N": w.N,
+         "P": list(w.P) if len(set(w.P)) > 1 else w.P[0], "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+         "temperature": w.T, "layers": 1}
+    if R is not None:
+        c["l2"] = f"inputs rotated over {R} copies per step (> 2x the 129 MB L2)"
+    return c
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
+    if world > 1 and "RANK" not in os.environ:
+        world = 1
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        local = int(os.environ.get("LOCAL_RANK", rank))
+        dev = torch.device("cuda", local)
+    else:
+        dev = torch.device("cuda", 0)
+    res = gpu_arm(args, rank, world, dev)
+    w = res["w"]
+    ms_total = res["ms_total"]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = world * w.B * args.steps / (ms_total / 1e3)
+    peaks = load_peaks()
+    model = work_model(w, res["tree_anc"])
+    names = ["topk", "build", "tree_attn", "accept"]
+    kernels = {}
+    for n, ms in zip(names, res["kern_ms"]):
+        k = {"ms": float(ms)}
+        if "bytes" in model[n]:
+            k["GBps"] = model[n]["bytes"] / (ms * 1e-3) / 1e9
+            k["hbm_frac"] = k["GBps"] / peaks["hbm_gbs"]
+        if "flops" in model[n]:
+            k["TFLOPps"] = model[n]["flops"] / (ms * 1e-3) / 1e12
+            k["tensor_frac"] = k["TFLOPps"] / peaks["bf16_tflops"]
+        kernels[n] = k
+    a = model["tree_attn"]
+    t_hbm = a["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = a["flops"] / (peaks["bf16_tflops"] * 1e12)
+    ams = float(res["kern_ms"][2])
+    if t_tc >= t_hbm:
+        roof = {"kernel": "tree_attn", "bound": "tensor", "achieved": a["flops"] / (ams * 1e-3) / 1e12,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        roof = {"kernel": "tree_attn", "bound": "hbm", "achieved": a["bytes"] / (ams * 1e-3) / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json burst figure)"
+    roof["algorithmic_bytes"] = a["bytes"]
+    roof["algorithmic_flops"] = a["flops"]
+    line = {"metric": "draft-tree rounds/sec (topK+build+tree-attn+accept); tree-attn % roofline",
+            "value": value, "unit": "rounds/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_of(w, res["R"]), "roofline": roof, "kernels": kernels,
+            "kernel_timing": res["kern_method"], "gpu_launches": 4 * args.steps,
+            "clocks": res["clocks"], "e2e": res["e2e"]}
+    if res["x36"]:
+        line["rounds_per_s_x36_layers"] = res["x36"]["rounds_per_s"] * world
+        line["x36"] = res["x36"]
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,344 @@
+// accept.cu -- step 4 of a DDTree round: the target's decoding rule at every
+// tree node, then the acceptance walk ("Accelerating Speculative Decoding with
+// Block Diffusion Draft Trees", §4.1: walk the tree with the target's decoding
+// rule, accept the matched path, the first unmatched target token becomes the
+// next bonus; §5 / App. B: temperatures 0 and 1).
+//
+// Grid = (vocabulary chunk, node, sequence): every live node row is streamed
+// once from HBM, split over enough CTAs to fill the GPU.
+//   T = 0: each CTA finds its chunk's (max, lowest index);
+//   T > 0: each CTA finds its chunk's max m_c and s_c = sum 2^((x - m_c) c),
+//          c = log2(e) / T.
+// The last CTA of a row (atomic ticket, no spinning) resolves the row's token:
+// the argmax over chunks, or the inverse-CDF sample -- it locates the chunk in
+// which the running sum crosses U * Z and rescans only that chunk (from L2).
+// The last row of a sequence to resolve runs the walk.
+#include "chunk.cuh"
+#include "internal.h"
+
+#include "../../include/ddtree.h"
+
+namespace ddt {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kItems = 8;
+
+struct AcceptWs {
+    unsigned int* row_tickets;  // [B][N+1]
+    unsigned int* seq_tickets;  // [B]
+    float2* parts;              // [B][N+1][nchunks]: (max, idx-as-bits) or (m_c, s_c)
+    int32_t* tok;               // [B][N+1] resolved target tokens
+};
+
+// Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two 64x64
+// multiplies with the Weyl key schedule.
+DDT_DEV void philox4x64_10(uint64_t c[4], uint64_t k0, uint64_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t lo0 = 0xD2E7470EE14C6C93ull * c[0], hi0 = __umul64hi(0xD2E7470EE14C6C93ull, c[0]);
+        const uint64_t lo1 = 0xCA5A826395121157ull * c[2], hi1 = __umul64hi(0xCA5A826395121157ull, c[2]);
+        const uint64_t x0 = hi1 ^ c[1] ^ k0, x2 = hi0 ^ c[3] ^ k1;
+        c[0] = x0; c[1] = lo1; c[2] = x2; c[3] = lo0;
+        k0 += 0x9E3779B97F4A7C15ull;
+        k1 += 0xBB67AE8584CAA73Bull;
+    }
+}
+
+DDT_DEV float node_uniform(uint64_t seed, uint64_t step, uint64_t seq, uint64_t node) {
+    uint64_t c[4] = {seq, node, 0ull, 0ull};
+    philox4x64_10(c, seed, step);
+    return (float)(c[0] >> 40) * (1.0f / 16777216.0f);
+}
+
+// Block-wide exclusive scan of one float per thread (256 threads); also returns
+// the block total.  Fixed shuffle/shared-memory tree: deterministic.
+DDT_DEV float block_exclusive_scan(float v, float* s_warp, float& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    float before = 0.f, tot = 0.f;
+#pragma unroll
+    for (int i = 0; i < kThreads / 32; ++i) {
+        const float wv = s_warp[i];
+        if (i < warp) before += wv;
+        tot += wv;
+    }
+    total = tot;
+    __syncthreads();
+    return before + incl - v;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads)
+accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nchunks,
+              bool aligned, const int32_t* __restrict__ parent, const int32_t* __restrict__ token,
+              const int32_t* __restrict__ n_nodes, int L, int N, float temperature, float c_exp,
+              uint64_t seed, uint64_t step, int32_t* __restrict__ target_token,
+              int32_t* __restrict__ accept_len, int32_t* __restrict__ accepted_nodes,
+              int32_t* __restrict__ out_tokens, int32_t* __restrict__ next_bonus, AcceptWs ws,
+              uint32_t* err) {
+    using Chunk = RowChunk<BF16, kItems>;
+    __shared__ float s_red[2 * (kThreads / 32)];
+    __shared__ int s_ired[kThreads / 32];
+    __shared__ bool s_flag;
+    __shared__ int s_pick;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int chunk = blockIdx.x, u = blockIdx.y, b = blockIdx.z;
+    const int R = N + 1;
+    const int n = n_nodes[b];
+    if (n < 0 || n > N) {
+        if (tid == 0 && chunk == 0 && u == 0) record_error(err, ERR_ACCEPT | ERR_BAD_N_NODES);
+        return;
+    }
+    if (u > n) return;
+
+    const size_t row = (size_t)b * R + u;
+    const char* rowp = (const char*)logits + row * (size_t)row_stride * Chunk::ES;
+    const int c0 = chunk * Chunk::SIZE;
+    Chunk x;
+    x.load(rowp, c0, V, aligned);
+
+    // ---- per-chunk partial ----------------------------------------------------
+    float vmax;
+    int vidx;
+    x.thread_max(c0, V, vmax, vidx);
+    // warp argmax: larger value, then lower index (vidx < 0 = empty)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, vmax, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, vidx, o);
+        const bool take = (oi >= 0) && (vidx < 0 || ov > vmax || (ov == vmax && oi < vidx));
+        vmax = take ? ov : vmax;
+        vidx = take ? oi : vidx;
+    }
+    if (lane == 0) { s_red[warp] = vmax; s_ired[warp] = vidx; }
+    __syncthreads();
+    float cmax = s_red[0];
+    int cidx = s_ired[0];
+#pragma unroll
+    for (int i = 1; i < kThreads / 32; ++i) {
+        const float ov = s_red[i];
+        const int oi = s_ired[i];
+        const bool take = (oi >= 0) && (cidx < 0 || ov > cmax || (ov == cmax && oi < cidx));
+        cmax = take ? ov : cmax;
+        cidx = take ? oi : cidx;
+    }
+    const bool sample = temperature > 0.f;
+    float csum = 0.f;
+    if (sample) {
+        const float ref = (cmax == -INFINITY) ? 0.f : cmax;
+        const float w = warp_sum(x.thread_exp_sum(ref, c_exp));
+        __syncthreads();
+        if (lane == 0) s_red[kThreads / 32 + warp] = w;
+        __syncthreads();
+        for (int i = 0; i < kThreads / 32; ++i) csum += s_red[kThreads / 32 + i];
+    }
+
+    float2* rparts = ws.parts + row * nchunks;
+    if (tid == 0) {
+        rparts[chunk] = sample ? make_float2(cmax, csum) : make_float2(cmax, __int_as_float(cidx));
+        s_flag = ticket_is_last(&ws.row_tickets[row], (unsigned)nchunks);
+    }
+    __syncthreads();
+    if (!s_flag) return;
+
+    // ---- last CTA of this row: resolve the row's token ---------------------------
+    int pick = -1;
+    if (!sample) {
+        if (tid == 0) {
+            float bv = 0.f;
+            for (int c = 0; c < nchunks; ++c) {
+                const float2 p = __ldcg(&rparts[c]);
+                const int pi = __float_as_int(p.y);
+                if (pi >= 0 && (pick < 0 || p.x > bv)) { bv = p.x; pick = pi; }
+            }
+            s_pick = pick;
+        }
+        __syncthreads();
+        pick = s_pick;
+    } else {
+        // Z = sum_c s_c 2^((m_c - M) c); target = U * Z; find the crossing chunk.
+        __shared__ int s_cstar;
+        __shared__ float s_tloc;
+        if (tid == 0) {
+            float M = -INFINITY;
+            for (int c = 0; c < nchunks; ++c) M = fmaxf(M, __ldcg(&rparts[c].x));
+            float Z = 0.f;
+            for (int c = 0; c < nchunks; ++c) {
+                const float2 p = __ldcg(&rparts[c]);
+                Z += p.y * fast_exp2((p.x - M) * c_exp);
+            }
+            const float target = node_uniform(seed, step, (uint64_t)b, (uint64_t)u) * Z;
+            float cum = 0.f;
+            int cs = nchunks - 1;
+            float tloc = 0.f;
+            for (int c = 0; c < nchunks; ++c) {
+                const float2 p = __ldcg(&rparts[c]);
+                const float scale = fast_exp2((p.x - M) * c_exp);
+                const float contrib = p.y * scale;
+                if (cum + contrib > target || c == nchunks - 1) {
+                    cs = c;
+                    tloc = (scale > 0.f) ? (target - cum) / scale : 0.f;
+                    break;
+                }
+                cum += contrib;
+            }
+            s_cstar = cs;
+            s_tloc = tloc;
+        }
+        __syncthreads();
+        const int cs = s_cstar;
+        const float tloc = s_tloc;
+        const float mref = fmaxf(__ldcg(&rparts[cs].x), -3.0e38f);
+        // Rescan chunk cs with a contiguous segment per thread, in token order.
+        constexpr int SEG = Chunk::SIZE / kThreads;
+        const int e0 = cs * Chunk::SIZE + tid * SEG;
+        float seg[SEG];
+        float tsum = 0.f;
+#pragma unroll
+        for (int i = 0; i < SEG; ++i) {
+            const int e = e0 + i;
+            float v = -INFINITY;
+            if (e < V) {
+                if (BF16) v = bf16lo((uint32_t)__ldcg((const unsigned short*)rowp + e));
+                else v = __ldcg((const float*)rowp + e);
+            }
+            seg[i] = fast_exp2((v - mref) * c_exp);
+            tsum += seg[i];
+        }
+        float total;
+        const float before = block_exclusive_scan(tsum, s_red, total);
+        // The owner is the first thread whose running sum passes tloc; if
+        // rounding leaves none (tloc at the chunk's very end), the last thread
+        // with nonzero weight.
+        __shared__ int s_first, s_lastnz;
+        if (tid == 0) { s_first = 0x7fffffff; s_lastnz = -1; }
+        __syncthreads();
+        if (tsum > 0.f) {
+            if (tloc < before + tsum) atomicMin(&s_first, tid);
+            atomicMax(&s_lastnz, tid);
+        }
+        __syncthreads();
+        const int owner = (s_first != 0x7fffffff) ? s_first : s_lastnz;
+        if (tid == owner) {
+            float acc = before;
+            int p = -1, lastnz = -1;
+#pragma unroll
+            for (int i = 0; i < SEG; ++i) {
+                acc += seg[i];
+                if (p < 0 && acc > tloc) p = e0 + i;
+                if (seg[i] > 0.f) lastnz = e0 + i;
+            }
+            s_pick = (p >= 0) ? p : lastnz;
+        }
+        if (owner < 0 && tid == 0) s_pick = cs * Chunk::SIZE;
+        __syncthreads();
+        pick = s_pick;
+    }
+    if (tid == 0) {
+        ws.tok[row] = pick;
+        if (target_token) target_token[row] = pick;
+        s_flag = ticket_is_last(&ws.seq_tickets[b], (unsigned)(n + 1));
+    }
+    __syncthreads();
+    if (!s_flag) return;
+
+    // ---- last row of the sequence: the walk ---------------------------------------
+    // chosen[p] = the child c of p whose token equals the target's token at p.
+    __shared__ int s_chosen[DDTREE_MAX_N + 1];
+    for (int i = tid; i <= n; i += kThreads) s_chosen[i] = -1;
+    __syncthreads();
+    const int32_t* par = parent + (size_t)b * R;
+    const int32_t* tk = token + (size_t)b * R;
+    const int32_t* tt = ws.tok + (size_t)b * R;
+    for (int c = 1 + tid; c <= n; c += kThreads) {
+        const int p = par[c];
+        if (p < 0 || p >= c) {
+            record_error(err, ERR_ACCEPT | ERR_BAD_TREE);
+            continue;
+        }
+        if (tk[c] == __ldcg(&tt[p])) s_chosen[p] = c;  // children have distinct tokens
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int cur = 0, len = 0;
+        int32_t* acc = accepted_nodes + (size_t)b * L;
+        int32_t* ot = out_tokens + (size_t)b * (L + 1);
+        while (len < L && s_chosen[cur] >= 0) {
+            cur = s_chosen[cur];
+            acc[len] = cur;
+            ot[len] = tk[cur];
+            ++len;
+        }
+        for (int i = len; i < L; ++i) acc[i] = -1;
+        const int bonus = __ldcg(&tt[cur]);
+        ot[len] = bonus;
+        for (int i = len + 1; i <= L; ++i) ot[i] = -1;
+        accept_len[b] = len;
+        next_bonus[b] = bonus;
+    }
+    if (target_token) {
+        for (int i = n + 1 + tid; i < R; i += kThreads) target_token[(size_t)b * R + i] = -1;
+    }
+}
+
+struct WsLayout {
+    size_t row_tickets, seq_tickets, parts, tok, total;
+};
+
+WsLayout accept_layout(int B, int N, int nch) {
+    WsLayout l;
+    const size_t R = (size_t)N + 1;
+    l.row_tickets = 0;
+    l.seq_tickets = align_up(l.row_tickets + (size_t)B * R * 4, 256);
+    l.parts = align_up(l.seq_tickets + (size_t)B * 4, 256);
+    l.tok = align_up(l.parts + (size_t)B * R * nch * sizeof(float2), 256);
+    l.total = align_up(l.tok + (size_t)B * R * 4, 256);
+    return l;
+}
+
+int accept_chunks(int V, int dtype) {
+    const int size = dtype == DDTREE_BF16 ? RowChunk<true, kItems>::SIZE
+                                          : RowChunk<false, kItems>::SIZE;
+    return (V + size - 1) / size;
+}
+
+}  // namespace
+
+size_t accept_workspace_bytes(int B, int N, int V, int dtype) {
+    return accept_layout(B, N, accept_chunks(V, dtype)).total;
+}
+
+cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s) {
+    const int nch = accept_chunks(a.V, a.dtype);
+    const WsLayout l = accept_layout(a.B, a.N, nch);
+    char* base = (char*)a.ws;
+    AcceptWs ws{(unsigned int*)(base + l.row_tickets), (unsigned int*)(base + l.seq_tickets),
+                (float2*)(base + l.parts), (int32_t*)(base + l.tok)};
+    const int es = a.dtype == DDTREE_BF16 ? 2 : 4;
+    const bool aligned = ((uintptr_t)a.logits % 16 == 0) && ((a.row_stride * es) % 16 == 0);
+    const float c_exp = a.temperature > 0.f ? kLog2e / a.temperature : 0.f;
+    dim3 grid(nch, a.N + 1, a.B);
+    if (a.dtype == DDTREE_BF16)
+        accept_kernel<true><<<grid, kThreads, 0, s>>>(
+            a.logits, a.V, a.row_stride, nch, aligned, a.parent, a.token, a.n_nodes, a.L, a.N,
+            a.temperature, c_exp, a.seed, a.step, a.target_token, a.accept_len, a.accepted_nodes,
+            a.out_tokens, a.next_bonus, ws, a.err);
+    else
+        accept_kernel<false><<<grid, kThreads, 0, s>>>(
+            a.logits, a.V, a.row_stride, nch, aligned, a.parent, a.token, a.n_nodes, a.L, a.N,
+            a.temperature, c_exp, a.seed, a.step, a.target_token, a.accept_len, a.accepted_nodes,
+            a.out_tokens, a.next_bonus, ws, a.err);
+    return cudaGetLastError();
+}
+
+}  // namespace ddt

@@ -1,0 +1,167 @@
+// api.cu -- the C ABI (include/ddtree.h): host-side validation, the per-device
+// error word, and dispatch to the kernel launchers.  No allocation, no
+// synchronisation except in ddtree_device_check().
+#include <mutex>
+
+#include "internal.h"
+
+#include "../../include/ddtree.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+uint32_t* g_err_ptr[kMaxDevices];
+std::mutex g_err_mu;
+
+}  // namespace
+
+// One error word per device; kernels record the first inconsistency they meet.
+static __device__ uint32_t g_ddtree_error_word;
+
+namespace {
+
+// Device address of this device's error word (looked up once per device).
+uint32_t* error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> g(g_err_mu);
+    if (!g_err_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_ddtree_error_word) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = (uint32_t*)p;
+    }
+    return g_err_ptr[dev];
+}
+
+inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+ddtree_status launched(cudaError_t e) { return e == cudaSuccess ? DDTREE_OK : DDTREE_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* ddtree_status_str(ddtree_status s) {
+    switch (s) {
+        case DDTREE_OK: return "ok";
+        case DDTREE_ERR_INVALID_ARG: return "invalid argument";
+        case DDTREE_ERR_UNSUPPORTED: return "unsupported shape";
+        case DDTREE_ERR_CUDA: return "CUDA error";
+        case DDTREE_ERR_DEVICE: return "kernel recorded bad device data or a timeout";
+    }
+    return "unknown status";
+}
+
+size_t ddtree_workspace_size(ddtree_op op, int B, int L, int N, int V, int K, int dtype, int Hq,
+                             int Hkv, int D, int64_t cache_cap) {
+    (void)K;
+    switch (op) {
+        case DDTREE_OP_TOPK:
+            if (B <= 0 || V <= 0 || (dtype != DDTREE_BF16 && dtype != DDTREE_FP32)) return 0;
+            return ddt::topk_workspace_bytes(B * (L > 0 ? L : 1), V, dtype);
+        case DDTREE_OP_TREE_ATTN:
+            if (B <= 0 || N < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || cache_cap < 0) return 0;
+            return ddt::attn_workspace_bytes(B, N, Hq, Hkv, D, cache_cap);
+        case DDTREE_OP_ACCEPT:
+            if (B <= 0 || N < 0 || V <= 0 || (dtype != DDTREE_BF16 && dtype != DDTREE_FP32))
+                return 0;
+            return ddt::accept_workspace_bytes(B, N, V, dtype);
+    }
+    return 0;
+}
+
+ddtree_status ddtree_topk(const void* draft_logits, int dtype, int rows, int V,
+                          int64_t row_stride, int K, int32_t* topk_idx, float* topk_logp,
+                          float* lse, void* workspace, size_t ws_bytes, void* stream) {
+    if (!draft_logits || !topk_idx || !topk_logp) return DDTREE_ERR_INVALID_ARG;
+    if (dtype != DDTREE_BF16 && dtype != DDTREE_FP32) return DDTREE_ERR_INVALID_ARG;
+    if (rows <= 0 || rows > 65535 || V <= 0 || row_stride < V || K < 1 || K > V)
+        return DDTREE_ERR_INVALID_ARG;
+    if (K > DDTREE_MAX_K) return DDTREE_ERR_UNSUPPORTED;
+    if (!aligned(draft_logits, dtype == DDTREE_BF16 ? 2 : 4)) return DDTREE_ERR_INVALID_ARG;
+    const size_t need = ddt::topk_workspace_bytes(rows, V, dtype);
+    if (need && (!workspace || ws_bytes < need || !aligned(workspace, 256)))
+        return DDTREE_ERR_INVALID_ARG;
+    ddt::TopkArgs a{draft_logits, dtype, rows, V, row_stride, K, topk_idx, topk_logp, lse,
+                    workspace, error_word()};
+    return launched(ddt::launch_topk(a, (cudaStream_t)stream));
+}
+
+ddtree_status ddtree_build(const float* topk_logp, const int32_t* topk_idx, const int32_t* bonus,
+                           const int32_t* prefix_len, int B, int L, int K, int N,
+                           int32_t* parent, int32_t* depth, int32_t* rank, int32_t* token,
+                           int32_t* pos_id, float* score, int32_t* child_count,
+                           uint32_t* anc_mask, int32_t* n_nodes, void* stream) {
+    if (!topk_logp || !topk_idx || !bonus || !prefix_len || !parent || !depth || !rank ||
+        !token || !pos_id || !score || !child_count || !anc_mask || !n_nodes)
+        return DDTREE_ERR_INVALID_ARG;
+    if (B <= 0 || L <= 0 || K <= 0 || N < 0) return DDTREE_ERR_INVALID_ARG;
+    if (L > DDTREE_MAX_L || K > DDTREE_MAX_K || N > DDTREE_MAX_N) return DDTREE_ERR_UNSUPPORTED;
+    ddt::BuildArgs a{topk_logp, topk_idx, bonus, prefix_len, B, L, K, N, parent, depth, rank,
+                     token, pos_id, score, child_count, anc_mask, n_nodes, error_word()};
+    return launched(ddt::launch_build(a, (cudaStream_t)stream));
+}
+
+ddtree_status ddtree_tree_attn(const void* q, const void* k_cache, const void* v_cache,
+                               int64_t cache_cap, const void* k_tree, const void* v_tree,
+                               const int32_t* prefix_len, const int32_t* n_nodes,
+                               const uint32_t* anc_mask, int B, int N, int Hq, int Hkv, int D,
+                               float scale, void* out, float* lse, void* workspace,
+                               size_t ws_bytes, void* stream) {
+    if (!q || !k_cache || !v_cache || !k_tree || !v_tree || !prefix_len || !n_nodes ||
+        !anc_mask || !out)
+        return DDTREE_ERR_INVALID_ARG;
+    if (B <= 0 || N < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || cache_cap < 0 || !(scale > 0.f))
+        return DDTREE_ERR_INVALID_ARG;
+    const int G = Hq / Hkv;
+    if (N > DDTREE_MAX_N || (D != 64 && D != 128) || (G & (G - 1)) || G > 128)
+        return DDTREE_ERR_UNSUPPORTED;
+    for (const void* p : {q, k_cache, v_cache, k_tree, v_tree, (const void*)out})
+        if (!aligned(p, 16)) return DDTREE_ERR_INVALID_ARG;
+    if (lse && !aligned(lse, 4)) return DDTREE_ERR_INVALID_ARG;
+    const size_t need = ddt::attn_workspace_bytes(B, N, Hq, Hkv, D, cache_cap);
+    if (need && (!workspace || ws_bytes < need || !aligned(workspace, 256)))
+        return DDTREE_ERR_INVALID_ARG;
+    ddt::AttnArgs a{q, k_cache, v_cache, cache_cap, k_tree, v_tree, prefix_len, n_nodes, anc_mask,
+                    B, N, Hq, Hkv, D, scale, out, lse, workspace, error_word()};
+    return launched(ddt::launch_tree_attn(a, (cudaStream_t)stream));
+}
+
+ddtree_status ddtree_accept(const void* target_logits, int dtype, int64_t row_stride,
+                            const int32_t* parent, const int32_t* token, const int32_t* n_nodes,
+                            int B, int L, int N, int V, float temperature, uint64_t seed,
+                            uint64_t step, int32_t* target_token, int32_t* accept_len,
+                            int32_t* accepted_nodes, int32_t* out_tokens, int32_t* next_bonus,
+                            void* workspace, size_t ws_bytes, void* stream) {
+    if (!target_logits || !parent || !token || !n_nodes || !accept_len || !accepted_nodes ||
+        !out_tokens || !next_bonus)
+        return DDTREE_ERR_INVALID_ARG;
+    if (dtype != DDTREE_BF16 && dtype != DDTREE_FP32) return DDTREE_ERR_INVALID_ARG;
+    if (B <= 0 || B > 65535 || L <= 0 || N < 0 || V <= 0 || row_stride < V ||
+        !(temperature >= 0.f) || temperature > 1e30f)
+        return DDTREE_ERR_INVALID_ARG;
+    if (N > DDTREE_MAX_N || L > DDTREE_MAX_L) return DDTREE_ERR_UNSUPPORTED;
+    if (!aligned(target_logits, dtype == DDTREE_BF16 ? 2 : 4)) return DDTREE_ERR_INVALID_ARG;
+    const size_t need = ddt::accept_workspace_bytes(B, N, V, dtype);
+    if (!workspace || ws_bytes < need || !aligned(workspace, 256)) return DDTREE_ERR_INVALID_ARG;
+    ddt::AcceptArgs a{target_logits, dtype, row_stride, parent, token, n_nodes, B, L, N, V,
+                      temperature, seed, step, target_token, accept_len, accepted_nodes,
+                      out_tokens, next_bonus, workspace, error_word()};
+    return launched(ddt::launch_accept(a, (cudaStream_t)stream));
+}
+
+ddtree_status ddtree_device_check(void* stream, uint32_t* detail) {
+    uint32_t* p = error_word();
+    if (!p) return DDTREE_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t v = 0, zero = 0;
+    if (cudaMemcpyAsync(&v, p, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return DDTREE_ERR_CUDA;
+    if (cudaMemcpyAsync(p, &zero, sizeof zero, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return DDTREE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return DDTREE_ERR_CUDA;
+    if (detail) *detail = v;
+    return v ? DDTREE_ERR_DEVICE : DDTREE_OK;
+}
+
+}  // extern "C"

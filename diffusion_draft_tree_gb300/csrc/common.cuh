@@ -1,0 +1,128 @@
+// common.cuh -- small device helpers shared by the DDTree kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define DDT_DEV __device__ __forceinline__
+
+namespace ddt {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Error word codes: high byte = kernel, low bytes = reason.  A kernel that
+// meets inconsistent device-side data records a code with atomicCAS (first
+// error wins) and skips the offending work; it never dereferences it.
+enum : uint32_t {
+    ERR_TOPK = 0x01000000u,
+    ERR_BUILD = 0x02000000u,
+    ERR_ATTN = 0x03000000u,
+    ERR_ACCEPT = 0x04000000u,
+    ERR_BAD_PREFIX_LEN = 0x1,
+    ERR_BAD_N_NODES = 0x2,
+    ERR_BAD_TREE = 0x3,
+    ERR_WAIT_TIMEOUT = 0x4,
+    ERR_BAD_INPUT = 0x5,
+};
+
+DDT_DEV void record_error(uint32_t* err, uint32_t code) {
+    if (err) atomicCAS(err, 0u, code);
+}
+
+// ---------------------------------------------------------------------------
+// Orderable keys: a float maps to a uint32 whose unsigned order is the float
+// order (-0.0 is folded onto +0.0 first).  A (value, index) pair maps to a
+// uint64 whose maximum is the largest value with the lowest index.
+// ---------------------------------------------------------------------------
+DDT_DEV uint32_t ord_from_bits(uint32_t b) {
+    b = (b == 0x80000000u) ? 0u : b;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+DDT_DEV uint32_t ord_from_float(float f) { return ord_from_bits(__float_as_uint(f)); }
+DDT_DEV float float_from_ord(uint32_t o) {
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+DDT_DEV uint64_t value_index_key(float v, uint32_t idx) {
+    return ((uint64_t)ord_from_float(v) << 32) | (uint64_t)(0xffffffffu - idx);
+}
+DDT_DEV float key_value(uint64_t k) { return float_from_ord((uint32_t)(k >> 32)); }
+DDT_DEV uint32_t key_index(uint64_t k) { return 0xffffffffu - (uint32_t)k; }
+
+// bf16 bits -> fp32 (exact)
+DDT_DEV float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+DDT_DEV float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+DDT_DEV float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+DDT_DEV uint64_t shfl_xor_u64(uint64_t v, int m) {
+    uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, m);
+    uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), m);
+    return ((uint64_t)hi << 32) | lo;
+}
+DDT_DEV uint64_t shfl_u64(uint64_t v, int src) {
+    uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)v, src);
+    uint32_t hi = __shfl_sync(0xffffffffu, (uint32_t)(v >> 32), src);
+    return ((uint64_t)hi << 32) | lo;
+}
+DDT_DEV uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
+DDT_DEV uint64_t umin64(uint64_t a, uint64_t b) { return a < b ? a : b; }
+
+// Warp-wide bitonic sort of one uint64 per lane, descending (lane 0 = max).
+DDT_DEV uint64_t warp_sort_desc(uint64_t v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            uint64_t o = shfl_xor_u64(v, j);
+            bool keep_max = (((lane & k) == 0) == ((lane & j) == 0));
+            v = keep_max ? umax64(v, o) : umin64(v, o);
+        }
+    }
+    return v;
+}
+
+// Both a and b sorted descending across the warp; returns the 32 largest of
+// their union, sorted descending.
+DDT_DEV uint64_t warp_merge_desc(uint64_t a, uint64_t b) {
+    const int lane = threadIdx.x & 31;
+    uint64_t rb = shfl_u64(b, 31 - lane);
+    uint64_t v = umax64(a, rb);  // bitonic
+#pragma unroll
+    for (int j = 16; j > 0; j >>= 1) {
+        uint64_t o = shfl_xor_u64(v, j);
+        v = ((lane & j) == 0) ? umax64(v, o) : umin64(v, o);
+    }
+    return v;
+}
+
+// 128-bit streaming global load that does not allocate in L1.
+DDT_DEV uint4 ld_stream_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// Counter ticket for "last CTA finishes the reduction".  Call from one thread
+// after the CTA's partial results are stored; returns true in exactly one CTA
+// of the `expected` that share the counter, and that CTA resets it to zero.
+// The release fence before and the acquire fence after make every other CTA's
+// partials visible to the last one.
+DDT_DEV bool ticket_is_last(unsigned int* counter, unsigned int expected) {
+    __threadfence();
+    unsigned int prev = atomicAdd(counter, 1u);
+    bool last = (prev + 1u == expected);
+    if (last) {
+        __threadfence();
+        *counter = 0u;
+    }
+    return last;
+}
+
+}  // namespace ddt

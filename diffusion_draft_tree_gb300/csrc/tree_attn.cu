@@ -1,0 +1,567 @@
+// tree_attn.cu -- step 3 of a DDTree round: one target layer's attention over
+// the draft tree ("Accelerating Speculative Decoding with Block Diffusion Draft
+// Trees", abstract and §4.1: every drafted node is verified in one target pass
+// with an ancestor-only attention mask; App. B: the pages' runs used a dense
+// masked attention because FlashAttention-2 cannot express the pattern).
+//
+// Work unit = (sequence b, KV head g, M tile, KV split).  An M tile holds 128
+// query rows: 128/G tree nodes x the G query heads that share KV head g, so the
+// GQA group turns the tree's (N+1) rows into a real dense contraction.  The
+// unit streams its KV range in 128-key tiles: prefix tiles from the cache, then
+// (last split only) the tree tiles, where the ancestor bitmask is applied.
+//
+// Per CTA: warp 0 issues TMA loads (K and V tiles, 128-byte swizzled) into a
+// 2-3 stage ring; warp 1 owns TMEM and issues tcgen05.mma: S = Q K^T into one
+// of two TMEM S buffers while the softmax warps read the other, then O += P V
+// into a TMEM accumulator; warps 2-5 (one thread per query row) run the online
+// softmax in the log2 domain (row max with lazy rescaling: O is rescaled only
+// when the max grows by more than 2^8), write P as bf16 into shared memory in
+// the swizzled K-major layout the MMA reads, and finally normalise O.  When a
+// unit's prefix is split, each split writes (O, m, l) partials and the last
+// split's CTA (atomic ticket) merges them.  Every mbarrier wait is bounded in
+// wall time; a timeout records an error and the CTA unwinds.
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+#include "sm100.cuh"
+
+#include "../../include/ddtree.h"
+
+namespace ddt {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int BM = 128;  // query rows per tile
+constexpr int BN = 128;  // keys per KV tile
+constexpr int kThreads = 192;
+constexpr int kHalfBytes = 128 * 128;  // [128 rows][64 bf16], one 128B-swizzled slab
+constexpr float kRescaleLog2 = 8.f;
+constexpr uint32_t kTmemCols = 512;
+
+template <int D>
+struct Cfg {
+    static constexpr int NH = D / 64;
+    static constexpr int Q_BYTES = NH * kHalfBytes;
+    static constexpr int KV_BYTES = NH * kHalfBytes;  // one K (or V) tile
+    static constexpr int P_BYTES = 2 * kHalfBytes;
+    static constexpr int NS = (D == 128) ? 2 : 3;
+    static constexpr int SMEM = 1024 + Q_BYTES + NS * 2 * KV_BYTES + P_BYTES;
+};
+
+struct Params {
+    const int32_t* prefix_len;
+    const int32_t* n_nodes;
+    const uint32_t* anc_mask;
+    uint16_t* out;
+    float* lse;
+    float* part_o;   // [unit][smax][D][128]
+    float* part_ml;  // [unit][smax][2][128]
+    unsigned int* tickets;
+    int B, N, Hq, Hkv, G, W, mtiles, tps, smax;
+    int64_t cache_cap;
+    float scale_log2;
+    uint32_t* err;
+};
+
+DDT_DEV uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+DDT_DEV void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Named barrier over the 128 softmax threads that also ANDs a flag.
+DDT_DEV bool softmax_bar_and(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
+                 const __grid_constant__ CUtensorMap tm_vc,
+                 const __grid_constant__ CUtensorMap tm_kt,
+                 const __grid_constant__ CUtensorMap tm_vt, const Params p) {
+    using C = Cfg<D>;
+    constexpr int NS = C::NS;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_q, bar_full[NS], bar_empty[NS], bar_sfull[2],
+        bar_sfree[2], bar_pfull, bar_odone;
+    __shared__ uint32_t s_tmem;
+    __shared__ volatile int s_abort;
+    __shared__ bool s_last;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // ---- decode the unit --------------------------------------------------------
+    int idx = blockIdx.x;
+    const int mtile = idx % p.mtiles;
+    idx /= p.mtiles;
+    const int split = idx % p.smax;
+    idx /= p.smax;
+    const int g = idx % p.Hkv;
+    const int b = idx / p.Hkv;
+    const int unit = (b * p.Hkv + g) * p.mtiles + mtile;
+    const int R = p.N + 1, G = p.G;
+    const int P = p.prefix_len[b];
+    const int n = p.n_nodes[b];
+    if (P < 0 || P > p.cache_cap || n < 0 || n > p.N) {
+        if (tid == 0 && split == 0 && mtile == 0 && g == 0)
+            record_error(p.err, ERR_ATTN | (n < 0 || n > p.N ? ERR_BAD_N_NODES : ERR_BAD_PREFIX_LEN));
+        return;
+    }
+    const int npt = (P + BN - 1) / BN;
+    const int splits = npt > 0 ? (npt + p.tps - 1) / p.tps : 1;
+    if (split >= splits) return;
+    const int rows_per_node = G;  // query rows of one node
+    const int u0 = mtile * (BM / G);
+    if (u0 > n) {  // every query row of this tile is padding: zeros, once
+        if (split != 0) return;
+        for (int r = tid; r < BM; r += kThreads) {
+            const int u = u0 + r / rows_per_node, h = g * G + r % rows_per_node;
+            if (u >= R) continue;
+            uint4* o = (uint4*)(p.out + (((size_t)b * R + u) * p.Hq + h) * D);
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+            if (p.lse) p.lse[((size_t)b * R + u) * p.Hq + h] = -INFINITY;
+        }
+        return;
+    }
+    const int t_begin = split * p.tps;
+    const int t_end = min(npt, t_begin + p.tps);
+    const int nprefix = max(0, t_end - t_begin);
+    const bool last_split = (split == splits - 1);
+    const int ntree = last_split ? (n + 1 + BN - 1) / BN : 0;
+    const int nt = nprefix + ntree;
+
+    // ---- shared memory carve-up (1024-byte aligned for the 128B swizzle) ----------
+    const uint32_t base_u32 = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t* base = smem_raw + (base_u32 - smem_u32(smem_raw));
+    uint8_t* sq = base;
+    uint8_t* sk = sq + C::Q_BYTES;           // NS stages of K
+    uint8_t* sv = sk + NS * C::KV_BYTES;     // NS stages of V
+    uint8_t* sp = sv + NS * C::KV_BYTES;     // P tile
+
+    if (tid == 0) {
+        mbar_init(&bar_q, 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&bar_full[s], 1);
+            mbar_init(&bar_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bar_sfull[s], 1);
+            mbar_init(&bar_sfree[s], 128);
+        }
+        mbar_init(&bar_pfull, 128);
+        mbar_init(&bar_odone, 1);
+        s_abort = 0;
+        mbar_init_fence();
+    }
+    if (warp == 1) tmem_alloc(&s_tmem, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    const uint32_t tm_s = tmem, tm_o = tmem + 256;
+
+    auto fail = [&]() {
+        record_error(p.err, ERR_ATTN | ERR_WAIT_TIMEOUT);
+        s_abort = 1;
+    };
+
+    if (warp == 0) {
+        // =========================== TMA producer ===========================
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_kc);
+            tma_prefetch_desc(&tm_vc);
+            tma_prefetch_desc(&tm_kt);
+            tma_prefetch_desc(&tm_vt);
+            mbar_arrive_expect_tx(&bar_q, C::Q_BYTES);
+            for (int h = 0; h < C::NH; ++h)
+                tma_load_3d(sq + h * kHalfBytes, &tm_q, &bar_q, 64 * h, g * G, b * R + u0);
+            for (int j = 0; j < nt; ++j) {
+                const int s = j % NS;
+                if (!mbar_wait(&bar_empty[s], ((j / NS) & 1) ^ 1, &s_abort)) { fail(); break; }
+                mbar_arrive_expect_tx(&bar_full[s], 2 * C::KV_BYTES);
+                uint8_t* dk = sk + s * C::KV_BYTES;
+                uint8_t* dv = sv + s * C::KV_BYTES;
+                if (j < nprefix) {
+                    const int p0 = (t_begin + j) * BN;
+                    for (int h = 0; h < C::NH; ++h) {
+                        tma_load_3d(dk + h * kHalfBytes, &tm_kc, &bar_full[s], 64 * h, p0, b * p.Hkv + g);
+                        tma_load_3d(dv + h * kHalfBytes, &tm_vc, &bar_full[s], 64 * h, p0, b * p.Hkv + g);
+                    }
+                } else {
+                    const int a0 = (j - nprefix) * BN;
+                    for (int h = 0; h < C::NH; ++h) {
+                        tma_load_3d(dk + h * kHalfBytes, &tm_kt, &bar_full[s], 64 * h, g, b * R + a0);
+                        tma_load_3d(dv + h * kHalfBytes, &tm_vt, &bar_full[s], 64 * h, g, b * R + a0);
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // =========================== MMA issuer =============================
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0, 0);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, 0, 1);
+            const uint32_t q_addr = smem_u32(sq), p_addr = smem_u32(sp);
+            bool ok = mbar_wait(&bar_q, 0, &s_abort);
+            if (!ok) fail();
+            for (int j = 0; ok && j <= nt; ++j) {
+                if (j < nt) {
+                    const int s = j % NS, sb = j & 1, use = j >> 1;
+                    if (!mbar_wait(&bar_full[s], (j / NS) & 1, &s_abort)) { fail(); break; }
+                    if (use >= 1 && !mbar_wait(&bar_sfree[sb], (use - 1) & 1, &s_abort)) { fail(); break; }
+                    tc_fence_after();
+                    const uint32_t k_addr = smem_u32(sk + s * C::KV_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                        mma_bf16_ss(tm_s + sb * BN, smem_desc_sw128(q_addr + off, 16, 1024),
+                                    smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0);
+                    }
+                    mma_commit(&bar_sfull[sb]);
+                }
+                if (j >= 1) {
+                    const int jj = j - 1, s2 = jj % NS;
+                    if (!mbar_wait(&bar_pfull, jj & 1, &s_abort)) { fail(); break; }
+                    tc_fence_after();
+                    const uint32_t v_addr = smem_u32(sv + s2 * C::KV_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        const uint32_t aoff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                        mma_bf16_ss(tm_o, smem_desc_sw128(p_addr + aoff, 16, 1024),
+                                    smem_desc_sw128(v_addr + kk * 2048, kHalfBytes, 1024), idesc_pv,
+                                    (jj > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&bar_odone);
+                    mma_commit(&bar_empty[s2]);
+                }
+            }
+        }
+    } else {
+        // ====================== softmax / epilogue (128 threads) ======================
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;  // query row == TMEM lane
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const int u = u0 + r / rows_per_node;
+        const int hh = g * G + r % rows_per_node;
+        const bool row_valid = (u <= n);
+        float m_run = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nt; ++j) {
+            const int sb = j & 1, use = j >> 1, s = j % NS;
+            if (!mbar_wait(&bar_sfull[sb], use & 1, &s_abort)) { fail(); ok = false; break; }
+            tc_fence_after();
+            float sc[BN];
+            {
+                uint32_t t[32];
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    tmem_ld32(tm_s + lane_off + sb * BN + c * 32, t);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) sc[c * 32 + i] = __uint_as_float(t[i]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bar_sfree[sb]);
+
+            // ---- mask + scale (log2 domain) ----
+            const bool is_tree = (j >= nprefix);
+            bool key_r_valid;
+            float mt = -INFINITY;
+            if (!is_tree) {
+                const int lim = P - (t_begin + j) * BN;  // keys c < lim are real
+                key_r_valid = r < lim;
+#pragma unroll
+                for (int c = 0; c < BN; ++c) {
+                    const float v = (c < lim) ? sc[c] * p.scale_log2 : -INFINITY;
+                    sc[c] = v;
+                    mt = fmaxf(mt, v);
+                }
+            } else {
+                const int a0 = (j - nprefix) * BN;
+                key_r_valid = (a0 + r) <= n;
+                uint32_t wd[4];
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const int wi = (a0 >> 5) + w;
+                    wd[w] = (row_valid && wi < p.W)
+                                ? __ldg(&p.anc_mask[((size_t)b * R + u) * p.W + wi])
+                                : 0u;
+                }
+                const int lim = n + 1 - a0;  // tree keys c < lim exist
+#pragma unroll
+                for (int c = 0; c < BN; ++c) {
+                    const bool on = ((wd[c >> 5] >> (c & 31)) & 1u) && (c < lim);
+                    const float v = on ? sc[c] * p.scale_log2 : -INFINITY;
+                    sc[c] = v;
+                    mt = fmaxf(mt, v);
+                }
+            }
+            const float m_new = fmaxf(m_run, mt);
+            const bool resc = m_new > m_run + kRescaleLog2;
+            const float m_use = resc ? m_new : m_run;
+            const float factor = resc ? fast_exp2(m_run - m_new) : 1.f;
+
+            // PV of the previous tile must be done before O or P is touched.
+            if (j >= 1) {
+                if (!mbar_wait(&bar_odone, (j - 1) & 1, &s_abort)) { fail(); ok = false; break; }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, factor != 1.f)) {
+                    uint32_t t[32];
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        tmem_ld32(tm_o + lane_off + c * 32, t);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            t[i] = __float_as_uint(__uint_as_float(t[i]) * factor);
+                        tmem_st32(tm_o + lane_off + c * 32, t);
+                    }
+                    tmem_st_wait();
+                }
+            }
+            l *= factor;
+            m_run = m_use;
+
+            // ---- P = 2^(s - m) as bf16, row r of the swizzled K-major P tile ----
+            const float mref = (m_use == -INFINITY) ? 0.f : m_use;
+            float sum = 0.f;
+#pragma unroll
+            for (int c16 = 0; c16 < BN / 8; ++c16) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = fast_exp2(sc[c16 * 8 + 2 * e] - mref);
+                    const float p1 = fast_exp2(sc[c16 * 8 + 2 * e + 1] - mref);
+                    w4[e] = pack_bf16x2(p0, p1);
+                    sum += __uint_as_float(w4[e] << 16) + __uint_as_float(w4[e] & 0xffff0000u);
+                }
+                const int half = c16 >> 3, chunk = c16 & 7;
+                uint8_t* dst = sp + half * kHalfBytes + r * 128 + ((chunk ^ (r & 7)) << 4);
+                *(uint4*)dst = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+            l += sum;
+            if (!key_r_valid) {
+                // key r of this tile is past the sequence: zero its V row so that
+                // uninitialised cache memory (possibly NaN) cannot reach O.
+                if (!mbar_wait(&bar_full[s], (j / NS) & 1, &s_abort)) { fail(); ok = false; break; }
+                uint8_t* vrow = sv + s * C::KV_BYTES + r * 128;
+#pragma unroll
+                for (int h = 0; h < C::NH; ++h)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        *(uint4*)(vrow + h * kHalfBytes + i * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bar_pfull);
+        }
+
+        // ---- epilogue (every softmax thread runs the same barrier sequence) ----
+        if (ok && !mbar_wait(&bar_odone, (nt - 1) & 1, &s_abort)) { fail(); ok = false; }
+        const bool all_ok = softmax_bar_and(ok);
+        float o[D];
+        if (all_ok) {
+            tc_fence_after();
+            uint32_t t[32];
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                tmem_ld32(tm_o + lane_off + c * 32, t);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[c * 32 + i] = __uint_as_float(t[i]);
+            }
+        }
+        tc_fence_before();
+        float M = m_run, Lsum = l;
+        bool write = all_ok;
+        if (splits > 1) {
+            const size_t slot = (size_t)unit * p.smax + split;
+            if (all_ok) {
+                float* po = p.part_o + slot * D * BM;
+#pragma unroll
+                for (int d = 0; d < D; ++d) po[d * BM + r] = o[d];
+                p.part_ml[slot * 2 * BM + r] = m_run;
+                p.part_ml[slot * 2 * BM + BM + r] = l;
+                __threadfence();
+            }
+            softmax_bar();
+            if (tid == 64) s_last = all_ok && ticket_is_last(&p.tickets[unit], (unsigned)splits);
+            softmax_bar();
+            write = s_last;
+            if (write) {
+                M = -INFINITY;
+                for (int s2 = 0; s2 < splits; ++s2)
+                    M = fmaxf(M, __ldcg(&p.part_ml[((size_t)unit * p.smax + s2) * 2 * BM + r]));
+                const float mref = (M == -INFINITY) ? 0.f : M;
+                Lsum = 0.f;
+#pragma unroll
+                for (int d = 0; d < D; ++d) o[d] = 0.f;
+                for (int s2 = 0; s2 < splits; ++s2) {
+                    const size_t sl = (size_t)unit * p.smax + s2;
+                    const float w = fast_exp2(__ldcg(&p.part_ml[sl * 2 * BM + r]) - mref);
+                    Lsum += __ldcg(&p.part_ml[sl * 2 * BM + BM + r]) * w;
+                    const float* q = p.part_o + sl * D * BM;
+#pragma unroll
+                    for (int d = 0; d < D; ++d) o[d] += __ldcg(&q[d * BM + r]) * w;
+                }
+            }
+        }
+        if (write && u < R) {
+            const bool live = row_valid && Lsum > 0.f;
+            const float inv = live ? 1.f / Lsum : 0.f;
+            uint4* dst = (uint4*)(p.out + (((size_t)b * R + u) * p.Hq + hh) * D);
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i)
+                dst[i] = make_uint4(pack_bf16x2(o[8 * i] * inv, o[8 * i + 1] * inv),
+                                    pack_bf16x2(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
+                                    pack_bf16x2(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
+                                    pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
+            if (p.lse)
+                p.lse[((size_t)b * R + u) * p.Hq + hh] =
+                    live ? (M + __log2f(Lsum)) * 0.6931471805599453f : -INFINITY;
+        }
+    }
+
+    // ---- teardown: every thread arrives here (all waits are bounded) -------------
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------- host side ---------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+    });
+    return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+              uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {d0, d1 ? d1 : 1, d2 ? d2 : 1};
+    cuuint64_t strides[2] = {s1_bytes, s2_bytes};
+    cuuint32_t box[3] = {b0, b1, b2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Plan {
+    int mtiles, tps, smax;
+};
+
+Plan make_plan(int B, int N, int Hq, int Hkv, int64_t cache_cap) {
+    Plan pl;
+    const int G = Hq / Hkv;
+    pl.mtiles = ((N + 1) * G + BM - 1) / BM;
+    const int max_tiles = (int)((cache_cap + BN - 1) / BN);
+    const long units = (long)B * Hkv * pl.mtiles;
+    const long target = 2 * 148;  // CTAs for about two waves on one GPU
+    int splits = (int)((target + units - 1) / units);
+    splits = std::max(1, std::min(splits, std::max(1, max_tiles)));
+    pl.tps = max_tiles > 0 ? (max_tiles + splits - 1) / splits : 1;
+    pl.smax = max_tiles > 0 ? (max_tiles + pl.tps - 1) / pl.tps : 1;
+    return pl;
+}
+
+struct WsLayout {
+    size_t tickets, part_o, part_ml, total;
+};
+
+WsLayout attn_layout(int B, int N, int Hq, int Hkv, int D, int64_t cache_cap) {
+    const Plan pl = make_plan(B, N, Hq, Hkv, cache_cap);
+    WsLayout w{};
+    const size_t units = (size_t)B * Hkv * pl.mtiles;
+    if (pl.smax <= 1) return w;
+    w.tickets = 0;
+    w.part_o = align_up(units * 4, 256);
+    w.part_ml = align_up(w.part_o + units * pl.smax * (size_t)D * BM * 4, 256);
+    w.total = align_up(w.part_ml + units * pl.smax * 2 * BM * 4, 256);
+    return w;
+}
+
+template <int D>
+cudaError_t launch_d(const AttnArgs& a, const Plan& pl, const WsLayout& wl, cudaStream_t s) {
+    static std::once_flag once[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaError_t attr_err = cudaSuccess;
+    std::call_once(once[dev & 63], [&] {
+        attr_err = cudaFuncSetAttribute(tree_attn_kernel<D>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int G = a.Hq / a.Hkv, R = a.N + 1;
+    CUtensorMap mq, mkc, mvc, mkt, mvt;
+    const uint64_t rowb = (uint64_t)D * 2;
+    bool ok = make_map(&mq, a.q, D, a.Hq, (uint64_t)a.B * R, rowb, rowb * a.Hq, 64, G, BM / G);
+    ok = ok && make_map(&mkc, a.k_cache, D, a.cache_cap, (uint64_t)a.B * a.Hkv, rowb,
+                        rowb * (a.cache_cap ? a.cache_cap : 1), 64, BN, 1);
+    ok = ok && make_map(&mvc, a.v_cache, D, a.cache_cap, (uint64_t)a.B * a.Hkv, rowb,
+                        rowb * (a.cache_cap ? a.cache_cap : 1), 64, BN, 1);
+    ok = ok && make_map(&mkt, a.k_tree, D, a.Hkv, (uint64_t)a.B * R, rowb, rowb * a.Hkv, 64, 1, BN);
+    ok = ok && make_map(&mvt, a.v_tree, D, a.Hkv, (uint64_t)a.B * R, rowb, rowb * a.Hkv, 64, 1, BN);
+    if (!ok) return cudaErrorInvalidValue;
+    Params p;
+    p.prefix_len = a.prefix_len;
+    p.n_nodes = a.n_nodes;
+    p.anc_mask = a.anc_mask;
+    p.out = (uint16_t*)a.out;
+    p.lse = a.lse;
+    char* ws = (char*)a.ws;
+    p.tickets = pl.smax > 1 ? (unsigned int*)(ws + wl.tickets) : nullptr;
+    p.part_o = pl.smax > 1 ? (float*)(ws + wl.part_o) : nullptr;
+    p.part_ml = pl.smax > 1 ? (float*)(ws + wl.part_ml) : nullptr;
+    p.B = a.B; p.N = a.N; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.W = (a.N + 1 + 31) / 32;
+    p.mtiles = pl.mtiles; p.tps = pl.tps; p.smax = pl.smax;
+    p.cache_cap = a.cache_cap;
+    p.scale_log2 = a.scale * kLog2e;
+    p.err = a.err;
+    const long grid = (long)a.B * a.Hkv * pl.mtiles * pl.smax;
+    tree_attn_kernel<D><<<(unsigned)grid, kThreads, Cfg<D>::SMEM, s>>>(mq, mkc, mvc, mkt, mvt, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t attn_workspace_bytes(int B, int N, int Hq, int Hkv, int D, int64_t cache_cap) {
+    return attn_layout(B, N, Hq, Hkv, D, cache_cap).total;
+}
+
+cudaError_t launch_tree_attn(const AttnArgs& a, cudaStream_t s) {
+    const Plan pl = make_plan(a.B, a.N, a.Hq, a.Hkv, a.cache_cap);
+    const WsLayout wl = attn_layout(a.B, a.N, a.Hq, a.Hkv, a.D, a.cache_cap);
+    if (a.D == 128) return launch_d<128>(a, pl, wl, s);
+    return launch_d<64>(a, pl, wl, s);
+}
+
+}  // namespace ddt

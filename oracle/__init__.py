@@ -49,7 +49,7 @@ def _load():
             i32, i64, f64, u64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_uint64
             lib.ddo_topk.argtypes = [P, i32, i32, i32, i64, i32, P, P, P, P]
             lib.ddo_build.argtypes = [P, P, P, P, i32, i32, i32, i32] + [P] * 9
-            lib.ddo_tree_attn_unit.argtypes = [i32, i32, P, P, P, i64, P, P, P, P, P, i32, i32,
+            lib.ddo_tree_attn_unit.argtypes = [i32, i32, i32, i32, P, P, P, i64, P, P, P, P, P, i32, i32,
                                                i32, i32, i32, f64, P, P]
             lib.ddo_tree_attn.argtypes = [P, P, P, i64, P, P, P, P, P, i32, i32, i32, i32, i32,
                                           f64, P, P]
@@ -117,11 +117,12 @@ def build_tree(logp32: np.ndarray, tok: np.ndarray, bonus: np.ndarray, prefix_le
 
 
 def tree_attn(q, k_cache, v_cache, k_tree, v_tree, prefix_len, n_nodes, anc_mask, scale=None,
-              units=None):
+              units=None, rows=None):
     """fp64 tree attention of one layer (pages §4.1: ancestor-only mask over the
     tree, full prefix).  bf16-bit inputs: q [B][N+1][Hq][D], caches
     [B][Hkv][cap][D], tree K/V [B][N+1][Hkv][D].  ``units`` optionally limits
-    the work to a list of (b, kv_head) pairs; other rows are left NaN.
+    the work to a list of (b, kv_head) pairs and ``rows`` to a node range
+    (lo, hi); rows not computed are left NaN.
     Returns (out float64 [B][N+1][Hq][D], lse float64 [B][N+1][Hq])."""
     B, R, Hq, D = q.shape
     Hkv, cap = k_cache.shape[1], k_cache.shape[2]
@@ -136,8 +137,9 @@ def tree_attn(q, k_cache, v_cache, k_tree, v_tree, prefix_len, n_nodes, anc_mask
     lib = _load()
     if units is None:
         units = [(b, g) for b in range(B) for g in range(Hkv)]
+    lo, hi = rows if rows is not None else (0, R)
     for b, g in units:
-        _check(lib.ddo_tree_attn_unit(b, g, _p(arrs[0]), _p(arrs[1]), _p(arrs[2]), cap,
+        _check(lib.ddo_tree_attn_unit(b, g, lo, hi, _p(arrs[0]), _p(arrs[1]), _p(arrs[2]), cap,
                                       _p(arrs[3]), _p(arrs[4]), _p(pl), _p(nn), _p(am), B, N, Hq,
                                       Hkv, D, scale, _p(out), _p(lse)), "tree_attn")
     return out, lse

@@ -222,13 +222,13 @@ int ddo_build(const float* logp, const int32_t* tok, const int32_t* bonus,
 /* Step 3: tree attention of one target layer (§4.1 ancestor-only mask).     */
 /* ------------------------------------------------------------------------ */
 
-/* One (sequence b, KV head g) unit: every node u <= n_nodes[b] and every query
+/* One (sequence b, KV head g) unit: every node u in [u_lo, u_hi) and every query
  * head h with h / G == g.  Layouts (bf16 bits):
  *   q [B][N+1][Hq][D], k_cache/v_cache [B][Hkv][cache_cap][D],
  *   k_tree/v_tree [B][N+1][Hkv][D];  out fp64 [B][N+1][Hq][D], lse fp64 [B][N+1][Hq].
  * Key set of node u: prefix positions 0..P_b-1, then tree nodes a whose bit is
  * set in u's ancestor row.  Rows past n_nodes get out = 0 and lse = -inf. */
-int ddo_tree_attn_unit(int b, int g, const uint16_t* q, const uint16_t* k_cache,
+int ddo_tree_attn_unit(int b, int g, int u_lo, int u_hi, const uint16_t* q, const uint16_t* k_cache,
                        const uint16_t* v_cache, int64_t cache_cap, const uint16_t* k_tree,
                        const uint16_t* v_tree, const int32_t* prefix_len,
                        const int32_t* n_nodes, const uint32_t* anc_mask, int B, int N, int Hq,
@@ -244,7 +244,9 @@ int ddo_tree_attn_unit(int b, int g, const uint16_t* q, const uint16_t* k_cache,
     if (!s || !use) { free(s); free(use); return -1; }
     const uint16_t* kc = k_cache + ((int64_t)b * Hkv + g) * cache_cap * D;
     const uint16_t* vc = v_cache + ((int64_t)b * Hkv + g) * cache_cap * D;
-    for (int u = 0; u < R; ++u) {
+    if (u_lo < 0) u_lo = 0;
+    if (u_hi > R) u_hi = R;
+    for (int u = u_lo; u < u_hi; ++u) {
         for (int h = g * G; h < (g + 1) * G; ++h) {
             double* o = out + (((int64_t)b * R + u) * Hq + h) * D;
             double* l_out = lse ? lse + ((int64_t)b * R + u) * Hq + h : NULL;
@@ -299,7 +301,7 @@ int ddo_tree_attn(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_
 {
     for (int b = 0; b < B; ++b)
         for (int g = 0; g < Hkv; ++g) {
-            int rc = ddo_tree_attn_unit(b, g, q, k_cache, v_cache, cache_cap, k_tree, v_tree,
+            int rc = ddo_tree_attn_unit(b, g, 0, N + 1, q, k_cache, v_cache, cache_cap, k_tree, v_tree,
                                         prefix_len, n_nodes, anc_mask, B, N, Hq, Hkv, D, scale,
                                         out, lse);
             if (rc) return rc;

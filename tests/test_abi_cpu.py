@@ -1,0 +1,83 @@
+"""CPU-only checks of the C-ABI library: it loads without a GPU driver, exports
+every entry point include/ddtree.h declares, and rejects bad arguments on the
+host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build_library()
+    from diffusion_draft_tree_gb300 import ops
+    return ops
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "ddtree.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:[\w\s\*]+?)\b(ddtree_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_round(lib):
+    names = _declared()
+    for n in ("ddtree_topk", "ddtree_build", "ddtree_tree_attn", "ddtree_accept",
+              "ddtree_workspace_size", "ddtree_device_check", "ddtree_status_str"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    so = ctypes.CDLL(lib.LIB_PATH)
+    for n in _declared():
+        assert hasattr(so, n), n
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert lib.lib.ddtree_status_str(s)
+
+
+def test_workspace_sizes(lib):
+    # 8B-class single stream: 16 rows of V=151936 bf16 split into chunks
+    assert lib.workspace_size(lib.OP_TOPK, B=1, L=16, V=151936, dtype=lib.BF16) > 0
+    # tiny vocabulary fits one chunk: no workspace
+    assert lib.workspace_size(lib.OP_TOPK, B=1, L=4, V=1000, dtype=lib.FP32) == 0
+    assert lib.workspace_size(lib.OP_ACCEPT, B=1, N=64, V=151936, dtype=lib.BF16) > 0
+    assert lib.workspace_size(lib.OP_TREE_ATTN, B=1, N=64, Hq=32, Hkv=8, D=128,
+                              cache_cap=2048) > 0
+    assert lib.workspace_size(lib.OP_TOPK, B=0, L=1, V=10) == 0
+
+
+def test_invalid_arguments_rejected_before_launch(lib):
+    L = lib.lib
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    # null logits
+    assert L.ddtree_topk(None, 0, 1, 10, 10, 2, fake, fake, None, None, 0, None) == 1
+    # K > V
+    assert L.ddtree_topk(fake, 0, 1, 4, 4, 5, fake, fake, None, None, 0, None) == 1
+    # K above the implementation limit
+    assert L.ddtree_topk(fake, 0, 1, 4000, 4000, 33, fake, fake, None, None, 0, None) == 2
+    # row stride shorter than a row
+    assert L.ddtree_topk(fake, 0, 1, 10, 9, 2, fake, fake, None, None, 0, None) == 1
+    # unsupported head dim / non power-of-two group
+    args = [fake, fake, fake, 64, fake, fake, fake, fake, fake, 1, 4, 8, 2, 96, 0.1, fake, None,
+            None, 0, None]
+    assert L.ddtree_tree_attn(*args) == 2
+    args[11], args[12], args[13] = 12, 4, 128  # G = 3
+    assert L.ddtree_tree_attn(*args) == 2
+    args[11], args[12] = 8, 3  # Hq % Hkv != 0
+    assert L.ddtree_tree_attn(*args) == 1
+    # budget above the limit
+    assert L.ddtree_build(fake, fake, fake, fake, 1, 4, 4, 5000, *([fake] * 9), None) == 2
+    # negative temperature
+    assert L.ddtree_accept(fake, 0, 10, fake, fake, fake, 1, 4, 4, 10, -1.0, 0, 0, None, fake,
+                           fake, fake, fake, fake, 1 << 20, None) == 1
+    # accept without workspace
+    assert L.ddtree_accept(fake, 0, 10, fake, fake, fake, 1, 4, 4, 10, 0.0, 0, 0, None, fake,
+                           fake, fake, fake, None, 0, None) == 1

@@ -1,0 +1,40 @@
+"""One whole DDTree round on the GPU (top-K -> heap -> tree attention -> walk),
+each step fed by the previous GPU step, against the oracle's own chain."""
+import numpy as np
+import pytest
+
+import oracle
+from diffusion_draft_tree_gb300 import ops
+from diffusion_draft_tree_gb300 import workloads as wl
+from tests.gpu_util import dev_bf16, dev_i32, dev_logits, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name", ["tiny", "8b_single"])
+def test_round_chain_matches_oracle_chain(cuda_device, name):
+    w = wl.CONFIGS[name]
+    dev = cuda_device
+    draft, bonus, plen = wl.draft_logits(w), wl.bonus_tokens(w), wl.prefix_lengths(w)
+    o_idx, _, o_lp32, _ = oracle.topk(draft, w.dtype, w.K)
+    o_tree = oracle.build_tree(o_lp32, o_idx, bonus, plen, w.N)
+    x = wl.target_logits(w, draft, o_tree["depth"])
+    o_acc = oracle.accept(x, w.dtype, o_tree, w.L)
+
+    idx, lp, _ = ops.topk(dev_logits(draft, w.dtype, dev), w.K)
+    tree = ops.build(lp, idx, dev_i32(bonus, dev), dev_i32(plen, dev), w.N)
+    for k in ("parent", "depth", "rank", "token", "n_nodes"):
+        np.testing.assert_array_equal(host(tree[k]), o_tree[k], err_msg=k)
+    q, kc, vc, kt, vt = (wl.queries(w), wl.kv_cache(w, 0), wl.kv_cache(w, 1), wl.kv_tree(w, 0),
+                         wl.kv_tree(w, 1))
+    out, _ = ops.tree_attn(dev_bf16(q, dev), dev_bf16(kc, dev), dev_bf16(vc, dev),
+                           dev_bf16(kt, dev), dev_bf16(vt, dev), dev_i32(plen, dev),
+                           tree["n_nodes"], tree["anc_mask"])
+    ref, _ = oracle.tree_attn(q, kc, vc, kt, vt, plen, o_tree["n_nodes"], o_tree["anc_mask"],
+                              units=[(0, 0)])
+    G = w.Hq // w.Hkv
+    assert np.abs(host(out)[0, :, :G] - ref[0, :, :G]).max() <= 1e-2
+    acc = ops.accept(dev_logits(x, w.dtype, dev), tree, w.L)
+    ops.ddtree_device_check()
+    for k in ("accept_len", "accepted_nodes", "out_tokens", "next_bonus"):
+        np.testing.assert_array_equal(host(acc[k]), o_acc[k], err_msg=k)

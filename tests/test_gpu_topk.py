@@ -1,0 +1,63 @@
+"""GPU parity of step 1 (log-softmax + top-K) against the oracle.
+Criteria: indices bit-exact; log-probs and logsumexp within 1e-5 absolute of
+the oracle's fp64 values."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from diffusion_draft_tree_gb300 import ops
+from diffusion_draft_tree_gb300 import workloads as wl
+from tests.gpu_util import dev_logits, host
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-5
+
+
+def _check(raw, dtype, K, dev, unaligned=False):
+    rows, V = raw.shape
+    o_idx, o_lp64, _, o_lse = oracle.topk(raw, dtype, K)
+    x = dev_logits(raw, dtype, dev)
+    if unaligned:  # same values, row starts shifted off the 16-byte grid
+        buf = torch.empty(rows * V + 1, dtype=x.dtype, device=dev)
+        buf[1:] = x.reshape(-1)
+        x = buf[1:].view(rows, V)
+        assert x.data_ptr() % 16 != 0
+    idx, lp, lse = ops.topk(x, K)
+    np.testing.assert_array_equal(host(idx), o_idx)
+    assert np.abs(host(lp) - o_lp64).max() <= TOL
+    assert np.abs(host(lse) - o_lse).max() <= TOL
+    ops.ddtree_device_check()
+
+
+@pytest.mark.parametrize("name", ["tiny", "8b_single", "budget_sweep_n64", "long_context_70b",
+                                  "ragged_serving"])
+def test_topk_workloads(cuda_device, name):
+    w = wl.CONFIGS[name]
+    raw = wl.draft_logits(w).reshape(w.B * w.L, w.V)
+    _check(raw, w.dtype, w.K, cuda_device)
+
+
+@pytest.mark.parametrize("V,K,dtype,unaligned", [
+    (1001, 3, wl.BF16, False), (1001, 3, wl.BF16, True), (8191, 16, wl.BF16, False),
+    (16384, 32, wl.BF16, False), (16385, 1, wl.BF16, True), (40000, 8, wl.FP32, False),
+    (40001, 8, wl.FP32, True), (50, 32, wl.BF16, False), (7, 1, wl.FP32, False),
+    (151936, 2, wl.BF16, False), (300000, 16, wl.BF16, False)])
+def test_topk_edge_shapes_and_ties(cuda_device, V, K, dtype, unaligned):
+    rng = np.random.default_rng(V + K)
+    x = (rng.standard_normal((6, V)) * 3).astype(np.float32)
+    x[1, :] = 0.0                                     # a constant row: ties everywhere
+    top = x[2].max() + 1
+    x[2, [3, V // 2, V - 1]] = top                    # equal maxima far apart
+    x[3, ::2] = np.float32(-0.0)                      # signed zeros tie by index
+    x[3, 1::2] = np.float32(0.0)
+    x[4, :] = np.round(x[4] * 2) / 2                  # heavy quantisation: many ties
+    raw = wl.bf16_bits(x) if dtype == wl.BF16 else x
+    _check(raw, dtype, K, cuda_device, unaligned)
+
+
+def test_topk_spike_is_top1(cuda_device):
+    w = wl.CONFIGS["8b_single"]
+    raw = wl.draft_logits(w).reshape(w.L, w.V)
+    idx, _, _ = ops.topk(dev_logits(raw, w.dtype, cuda_device), w.K)
+    np.testing.assert_array_equal(host(idx)[:, 0], np.argmax(wl.bf16_to_f32(raw), axis=1))
