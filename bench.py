@@ -45,6 +45,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-x36", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--profile-rounds", type=int, default=0,
+                    help="only run this many eager rounds (rotating input copies) and exit; "
+                         "for kernel profilers")
     return ap.parse_args()
 
 
@@ -246,6 +249,12 @@ def gpu_arm(args, rank, world, dev):
         r.run()
     torch.cuda.synchronize()
     ops.ddtree_device_check()
+    if args.profile_rounds:
+        for i in range(args.profile_rounds):
+            rounds[i % R].run()
+        torch.cuda.synchronize()
+        ops.ddtree_device_check()
+        return {"profile_only": True, "w": w, "R": R}
 
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
@@ -500,6 +509,11 @@ def main():
         dev = torch.device("cuda", 0)
     res = gpu_arm(args, rank, world, dev)
     w = res["w"]
+    if res.get("profile_only"):
+        if rank == 0:
+            print(json.dumps({"profile_rounds": args.profile_rounds, "workload": w.name,
+                              "copies": res["R"]}), flush=True)
+        return
     ms_total = res["ms_total"]
     if world > 1:
         import torch.distributed as dist

@@ -24,6 +24,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kItems = 8;
+constexpr int kMaxChunks = 128;
 
 struct AcceptWs {
     unsigned int* row_tickets;  // [B][N+1]
@@ -152,12 +153,15 @@ accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nc
     if (!s_flag) return;
 
     // ---- last CTA of this row: resolve the row's token ---------------------------
+    __shared__ float2 s_part[kMaxChunks];
+    for (int c = tid; c < nchunks; c += kThreads) s_part[c] = __ldcg(&rparts[c]);
+    __syncthreads();
     int pick = -1;
     if (!sample) {
         if (tid == 0) {
             float bv = 0.f;
             for (int c = 0; c < nchunks; ++c) {
-                const float2 p = __ldcg(&rparts[c]);
+                const float2 p = s_part[c];
                 const int pi = __float_as_int(p.y);
                 if (pi >= 0 && (pick < 0 || p.x > bv)) { bv = p.x; pick = pi; }
             }
@@ -170,24 +174,22 @@ accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nc
         __shared__ int s_cstar;
         __shared__ float s_tloc;
         if (tid == 0) {
+            // the few chunk sums are combined in fp64
             float M = -INFINITY;
-            for (int c = 0; c < nchunks; ++c) M = fmaxf(M, __ldcg(&rparts[c].x));
-            float Z = 0.f;
-            for (int c = 0; c < nchunks; ++c) {
-                const float2 p = __ldcg(&rparts[c]);
-                Z += p.y * fast_exp2((p.x - M) * c_exp);
-            }
-            const float target = node_uniform(seed, step, (uint64_t)b, (uint64_t)u) * Z;
-            float cum = 0.f;
+            for (int c = 0; c < nchunks; ++c) M = fmaxf(M, s_part[c].x);
+            double Z = 0.0;
+            for (int c = 0; c < nchunks; ++c)
+                Z += (double)s_part[c].y * (double)fast_exp2((s_part[c].x - M) * c_exp);
+            const double target = (double)node_uniform(seed, step, (uint64_t)b, (uint64_t)u) * Z;
+            double cum = 0.0;
             int cs = nchunks - 1;
             float tloc = 0.f;
             for (int c = 0; c < nchunks; ++c) {
-                const float2 p = __ldcg(&rparts[c]);
-                const float scale = fast_exp2((p.x - M) * c_exp);
-                const float contrib = p.y * scale;
+                const double scale = (double)fast_exp2((s_part[c].x - M) * c_exp);
+                const double contrib = (double)s_part[c].y * scale;
                 if (cum + contrib > target || c == nchunks - 1) {
                     cs = c;
-                    tloc = (scale > 0.f) ? (target - cum) / scale : 0.f;
+                    tloc = (scale > 0.0) ? (float)((target - cum) / scale) : 0.f;
                     break;
                 }
                 cum += contrib;
@@ -198,7 +200,7 @@ accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nc
         __syncthreads();
         const int cs = s_cstar;
         const float tloc = s_tloc;
-        const float mref = fmaxf(__ldcg(&rparts[cs].x), -3.0e38f);
+        const float mref = fmaxf(s_part[cs].x, -3.0e38f);
         // Rescan chunk cs with a contiguous segment per thread, in token order.
         constexpr int SEG = Chunk::SIZE / kThreads;
         const int e0 = cs * Chunk::SIZE + tid * SEG;
@@ -305,6 +307,16 @@ WsLayout accept_layout(int B, int N, int nch) {
     l.total = align_up(l.tok + (size_t)B * R * 4, 256);
     return l;
 }
+
+}  // namespace
+
+bool accept_supported(int V, int dtype) {
+    const int size = dtype == DDTREE_BF16 ? RowChunk<true, kItems>::SIZE
+                                          : RowChunk<false, kItems>::SIZE;
+    return (V + size - 1) / size <= kMaxChunks;
+}
+
+namespace {
 
 int accept_chunks(int V, int dtype) {
     const int size = dtype == DDTREE_BF16 ? RowChunk<true, kItems>::SIZE

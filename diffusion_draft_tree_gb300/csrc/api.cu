@@ -77,7 +77,7 @@ ddtree_status ddtree_topk(const void* draft_logits, int dtype, int rows, int V,
     if (dtype != DDTREE_BF16 && dtype != DDTREE_FP32) return DDTREE_ERR_INVALID_ARG;
     if (rows <= 0 || rows > 65535 || V <= 0 || row_stride < V || K < 1 || K > V)
         return DDTREE_ERR_INVALID_ARG;
-    if (K > DDTREE_MAX_K) return DDTREE_ERR_UNSUPPORTED;
+    if (K > DDTREE_MAX_K || !ddt::topk_supported(V, dtype, K)) return DDTREE_ERR_UNSUPPORTED;
     if (!aligned(draft_logits, dtype == DDTREE_BF16 ? 2 : 4)) return DDTREE_ERR_INVALID_ARG;
     const size_t need = ddt::topk_workspace_bytes(rows, V, dtype);
     if (need && (!workspace || ws_bytes < need || !aligned(workspace, 256)))
@@ -140,7 +140,8 @@ ddtree_status ddtree_accept(const void* target_logits, int dtype, int64_t row_st
     if (B <= 0 || B > 65535 || L <= 0 || N < 0 || V <= 0 || row_stride < V ||
         !(temperature >= 0.f) || temperature > 1e30f)
         return DDTREE_ERR_INVALID_ARG;
-    if (N > DDTREE_MAX_N || L > DDTREE_MAX_L) return DDTREE_ERR_UNSUPPORTED;
+    if (N > DDTREE_MAX_N || L > DDTREE_MAX_L || !ddt::accept_supported(V, dtype))
+        return DDTREE_ERR_UNSUPPORTED;
     if (!aligned(target_logits, dtype == DDTREE_BF16 ? 2 : 4)) return DDTREE_ERR_INVALID_ARG;
     const size_t need = ddt::accept_workspace_bytes(B, N, V, dtype);
     if (!workspace || ws_bytes < need || !aligned(workspace, 256)) return DDTREE_ERR_INVALID_ARG;

@@ -22,6 +22,7 @@ struct TopkArgs {
     uint32_t* err;
 };
 int topk_chunks(int V, int dtype);
+bool topk_supported(int V, int dtype, int K);
 size_t topk_workspace_bytes(int rows, int V, int dtype);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 
@@ -73,6 +74,7 @@ struct AcceptArgs {
     uint32_t* err;
 };
 size_t accept_workspace_bytes(int B, int N, int V, int dtype);
+bool accept_supported(int V, int dtype);
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

@@ -10,10 +10,11 @@
 //   m_c = max, s_c = sum exp(x - m_c), and its K best (value, index) keys.
 // Top-K selection avoids per-element insertion: every warp finds tau_w, the
 // K-th largest of its 32 lane maxima (a warp bitonic sort), the CTA takes
-// tau = max_w tau_w -- a lower bound on the chunk's K-th largest key -- and only
-// elements with key >= tau (typically ~2K of 16K) are appended to a shared
-// buffer that warp 0 sorts and merges.  The last CTA of a row (atomic ticket,
-// no spinning) merges the chunk partials and writes the row's outputs.
+// tau = max_w tau_w -- a lower bound on the chunk's K-th largest value -- and
+// only elements >= tau (typically ~2K of 16K) are appended to a shared buffer
+// from which warp 0 selects the K largest (value, index) keys.  The last CTA
+// of a row (atomic ticket, no spinning) loads every chunk partial in parallel,
+// merges them and writes the row's outputs.
 #include "chunk.cuh"
 #include "internal.h"
 
@@ -33,8 +34,48 @@ struct TopkPartial {
     uint64_t keys[DDTREE_MAX_K];
 };
 
+// The K largest keys of cand[0..cnt) into sel[0..K), sorted descending, 0 where
+// fewer than K exist.  One warp.  Small sets: each key's rank is counted
+// directly (no shuffles on the critical path); large sets: bitonic sort/merge.
+DDT_DEV void warp_select(const uint64_t* cand, int cnt, int K, uint64_t* sel) {
+    const int lane = threadIdx.x & 31;
+    if (cnt <= 64) {
+        if (lane < K) sel[lane] = 0ull;
+        __syncwarp();
+        for (int i = lane; i < cnt; i += 32) {
+            const uint64_t ki = cand[i];
+            int rank = 0;
+            for (int j = 0; j < cnt; ++j) rank += (cand[j] > ki) ? 1 : 0;
+            if (rank < K) sel[rank] = ki;
+        }
+    } else {
+        uint64_t best = 0ull;
+        for (int g = 0; g < cnt; g += 32) {
+            const uint64_t v = (g + lane < cnt) ? cand[g + lane] : 0ull;
+            best = warp_merge_desc(best, warp_sort_desc(v));
+        }
+        if (lane < K) sel[lane] = best;
+    }
+    __syncwarp();
+}
+
+// Warp-wide bitonic sort of one uint32 per lane, descending.
+DDT_DEV uint32_t warp_sort_desc_u32(uint32_t v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const uint32_t o = __shfl_xor_sync(0xffffffffu, v, j);
+            const bool keep_max = (((lane & k) == 0) == ((lane & j) == 0));
+            v = keep_max ? max(v, o) : min(v, o);
+        }
+    }
+    return v;
+}
+
 template <bool BF16>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, int nchunks,
             bool aligned, int32_t* __restrict__ topk_idx, float* __restrict__ topk_logp,
             float* __restrict__ lse, TopkPartial* __restrict__ parts,
@@ -43,7 +84,8 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     __shared__ uint64_t s_cand[kCandCap];
     __shared__ uint64_t s_sel[DDTREE_MAX_K];
     __shared__ float s_wmax[kThreads / 32], s_wsum[kThreads / 32];
-    __shared__ uint64_t s_wtau[kThreads / 32];
+    __shared__ uint32_t s_wtau[kThreads / 32];
+    __shared__ float s_m[kCandCap / 8], s_s[kCandCap / 8];
     __shared__ int s_cnt;
     __shared__ bool s_last;
 
@@ -56,25 +98,26 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     Chunk x;
     x.load(rowp, c0, V, aligned);
 
-    // ---- lane maxima, warp thresholds, CTA max ---------------------------
+    // ---- lane maxima; tau_w = K-th largest lane maximum of the warp -------------
     float vmax;
     int vidx;
     x.thread_max(c0, V, vmax, vidx);
-    const uint64_t lane_key = (vidx >= 0) ? value_index_key(vmax, (uint32_t)vidx) : 0ull;
-    const uint64_t sorted = warp_sort_desc(lane_key);
-    const uint64_t tau_w = shfl_u64(sorted, K - 1);
+    const uint32_t lane_ord = (vidx >= 0) ? ord_from_float(vmax) : 0u;
+    const uint32_t tau_w = __shfl_sync(0xffffffffu, warp_sort_desc_u32(lane_ord), K - 1);
     const float wmax = warp_max(vmax);
     if (lane == 0) {
         s_wmax[warp] = wmax;
         s_wtau[warp] = tau_w;
     }
     __syncthreads();
+    // The chunk has >= K elements >= the value with order tau (K lane maxima of
+    // one warp), so its top K are among the elements >= that value.
     float m = s_wmax[0];
-    uint64_t tau = s_wtau[0];
+    uint32_t tau = s_wtau[0];
 #pragma unroll
     for (int i = 1; i < kThreads / 32; ++i) {
         m = fmaxf(m, s_wmax[i]);
-        tau = umax64(tau, s_wtau[i]);
+        tau = max(tau, s_wtau[i]);
     }
 
     // ---- sum of exponentials ------------------------------------------------
@@ -82,19 +125,16 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     const float ws = warp_sum(x.thread_exp_sum(ref, kLog2e));
     if (lane == 0) s_wsum[warp] = ws;
 
-    // ---- candidates: keys >= tau ------------------------------------------
-    if (lane_key != 0ull && lane_key >= tau) {
-        const float tv = key_value(tau);
-        const uint32_t ti = key_index(tau);
+    // ---- candidates ---------------------------------------------------------
+    if (vidx >= 0 && lane_ord >= tau) {
+        const float tv = float_from_ord(tau);
 #pragma unroll
         for (int it = 0; it < kItems; ++it) {
 #pragma unroll
             for (int k = 0; k < Chunk::VEC; ++k) {
                 const float v = x.elem(it, k);
                 const int e = Chunk::index(c0, it, k);
-                const bool cand = (tau == 0ull)
-                                      ? (e < V)
-                                      : (v > tv || (v == tv && (uint32_t)e <= ti));
+                const bool cand = (tau == 0u) ? (e < V) : (v >= tv);
                 if (cand) {
                     const int pos = atomicAdd(&s_cnt, 1);
                     if (pos < kCandCap) s_cand[pos] = value_index_key(v, (uint32_t)e);
@@ -105,14 +145,8 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     __syncthreads();
     const int cnt = s_cnt;
 
-    uint64_t best = 0ull;  // warp 0: the chunk's top keys, sorted, one per lane
     if (cnt <= kCandCap) {
-        if (warp == 0) {
-            for (int g = 0; g < cnt; g += 32) {
-                const uint64_t v = (g + lane < cnt) ? s_cand[g + lane] : 0ull;
-                best = warp_merge_desc(best, warp_sort_desc(v));
-            }
-        }
+        if (warp == 0) warp_select(s_cand, cnt, K, s_sel);
     } else {
         // Degenerate ties overflowed the buffer: exact K-round selection over
         // the registers (rare path; correctness only).
@@ -140,58 +174,71 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
             prev = cb;
             __syncthreads();
         }
-        if (warp == 0) best = (lane < K) ? s_sel[lane] : 0ull;
     }
-
-    if (warp != 0) return;
 
     float S = 0.f;
-    if (lane == 0) {
-        for (int i = 0; i < kThreads / 32; ++i) S += s_wsum[i];
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int i = 0; i < kThreads / 32; ++i) S += s_wsum[i];
+        }
+        S = __shfl_sync(0xffffffffu, S, 0);
     }
-    S = __shfl_sync(0xffffffffu, S, 0);
     float M = ref;
 
     if (nchunks > 1) {
-        TopkPartial* p = parts + (size_t)row * nchunks + chunk;
-        if (lane < K) p->keys[lane] = best;
-        if (lane == 0) {
-            p->m = m;
-            p->s = S;
+        if (warp == 0) {
+            TopkPartial* p = parts + (size_t)row * nchunks + chunk;
+            if (lane < K) p->keys[lane] = s_sel[lane];
+            if (lane == 0) {
+                p->m = m;
+                p->s = S;
+            }
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) s_last = ticket_is_last(&tickets[row], (unsigned)nchunks);
         }
-        __threadfence();
-        __syncwarp();
-        bool last = false;
-        if (lane == 0) last = ticket_is_last(&tickets[row], (unsigned)nchunks);
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (!last) return;
-        // ---- last CTA of the row: merge the chunk partials -----------------
+        __syncthreads();
+        if (!s_last) return;
+        // ---- last CTA of the row: merge the chunk partials (loads in parallel) ----
         const TopkPartial* rp = parts + (size_t)row * nchunks;
-        best = 0ull;
+        const int nk = nchunks * K;
+        for (int t = tid; t < nk; t += kThreads) {
+            const int c = t / K, k = t - c * K;
+            s_cand[t] = __ldcg((const unsigned long long*)&rp[c].keys[k]);
+        }
+        for (int c = tid; c < nchunks; c += kThreads) {
+            s_m[c] = __ldcg(&rp[c].m);
+            s_s[c] = __ldcg(&rp[c].s);
+        }
+        __syncthreads();
+        if (warp != 0) return;
         float mm = -INFINITY;
-        for (int c = lane; c < nchunks; c += 32) mm = fmaxf(mm, __ldcg(&rp[c].m));
+        for (int c = lane; c < nchunks; c += 32) mm = fmaxf(mm, s_m[c]);
         mm = warp_max(mm);
         M = (mm == -INFINITY) ? 0.f : mm;
         float ss = 0.f;
-        for (int c = lane; c < nchunks; c += 32)
-            ss += __ldcg(&rp[c].s) * fast_exp2((__ldcg(&rp[c].m) - M) * kLog2e);
+        for (int c = lane; c < nchunks; c += 32) ss += s_s[c] * fast_exp2((s_m[c] - M) * kLog2e);
         S = warp_sum(ss);
-        for (int c = 0; c < nchunks; ++c) {
-            const uint64_t v = (lane < K) ? __ldcg((const unsigned long long*)&rp[c].keys[lane])
-                                          : 0ull;
-            best = warp_merge_desc(best, v);
-        }
+        warp_select(s_cand, nk, K, s_sel);
+    } else if (warp != 0) {
+        return;
     }
     const float logS = logf(S);
     if (lane < K) {
-        const float v = key_value(best);
-        topk_idx[(size_t)row * K + lane] = (int32_t)key_index(best);
+        const uint64_t key = s_sel[lane];
+        const float v = key_value(key);
+        topk_idx[(size_t)row * K + lane] = (int32_t)key_index(key);
         topk_logp[(size_t)row * K + lane] = (v - M) - logS;
     }
     if (lane == 0 && lse) lse[row] = M + logS;
 }
 
 }  // namespace
+
+bool topk_supported(int V, int dtype, int K) {
+    const int nch = topk_chunks(V, dtype);
+    return nch <= kCandCap / 8 && nch * K <= kCandCap;
+}
 
 int topk_chunks(int V, int dtype) {
     const int size = dtype == DDTREE_BF16 ? RowChunk<true, kItems>::SIZE

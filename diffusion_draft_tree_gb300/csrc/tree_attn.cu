@@ -479,16 +479,39 @@ struct Plan {
     int mtiles, tps, smax;
 };
 
+// Streaming multiprocessors of the current device (148 if the query fails).
+int num_sms() {
+    static int cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+// Split the prefix of each (sequence, KV head, M tile) unit into KV splits of
+// `tps` tiles.  Few units: split until one wave of CTAs (one per SM) is full.
+// Many units: cap a split at a quarter of the longest prefix so that long
+// sequences of a ragged batch do not leave a tail of lone CTAs.
 Plan make_plan(int B, int N, int Hq, int Hkv, int64_t cache_cap) {
     Plan pl;
     const int G = Hq / Hkv;
     pl.mtiles = ((N + 1) * G + BM - 1) / BM;
     const int max_tiles = (int)((cache_cap + BN - 1) / BN);
     const long units = (long)B * Hkv * pl.mtiles;
-    const long target = 2 * 148;  // CTAs for about two waves on one GPU
-    int splits = (int)((target + units - 1) / units);
-    splits = std::max(1, std::min(splits, std::max(1, max_tiles)));
-    pl.tps = max_tiles > 0 ? (max_tiles + splits - 1) / splits : 1;
+    const int sms = num_sms();
+    if (max_tiles <= 1) {
+        pl.tps = 1;
+    } else if (units < sms) {
+        const int splits = (int)std::max(1L, std::min<long>(sms / units, max_tiles));
+        pl.tps = (max_tiles + splits - 1) / splits;
+    } else {
+        pl.tps = max_tiles > 64 ? std::max(32, (max_tiles + 3) / 4) : max_tiles;
+    }
     pl.smax = max_tiles > 0 ? (max_tiles + pl.tps - 1) / pl.tps : 1;
     return pl;
 }

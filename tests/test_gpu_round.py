@@ -1,5 +1,9 @@
 """One whole DDTree round on the GPU (top-K -> heap -> tree attention -> walk),
-each step fed by the previous GPU step, against the oracle's own chain."""
+each step fed by the previous GPU step, against the oracle's own chain.
+
+The GPU's fp32 log-probs agree with the oracle's to ~1e-6, so prefixes whose
+scores differ by less than that may be popped in the other order: node ids
+are compared through their token paths, and the accepted tokens exactly."""
 import numpy as np
 import pytest
 
@@ -23,8 +27,12 @@ def test_round_chain_matches_oracle_chain(cuda_device, name):
 
     idx, lp, _ = ops.topk(dev_logits(draft, w.dtype, dev), w.K)
     tree = ops.build(lp, idx, dev_i32(bonus, dev), dev_i32(plen, dev), w.N)
-    for k in ("parent", "depth", "rank", "token", "n_nodes"):
-        np.testing.assert_array_equal(host(tree[k]), o_tree[k], err_msg=k)
+    g_paths = _paths(host(tree["parent"])[0], host(tree["token"])[0], host(tree["n_nodes"])[0])
+    o_paths = _paths(o_tree["parent"][0], o_tree["token"][0], o_tree["n_nodes"][0])
+    assert set(g_paths) == set(o_paths)
+    g_score = dict(zip(g_paths, host(tree["score"])[0]))
+    for p, s in zip(o_paths, o_tree["score"][0]):
+        assert abs(g_score[p] - s) <= 1e-5 * max(1, len(p))
     q, kc, vc, kt, vt = (wl.queries(w), wl.kv_cache(w, 0), wl.kv_cache(w, 1), wl.kv_tree(w, 0),
                          wl.kv_tree(w, 1))
     out, _ = ops.tree_attn(dev_bf16(q, dev), dev_bf16(kc, dev), dev_bf16(vc, dev),
@@ -36,5 +44,20 @@ def test_round_chain_matches_oracle_chain(cuda_device, name):
     assert np.abs(host(out)[0, :, :G] - ref[0, :, :G]).max() <= 1e-2
     acc = ops.accept(dev_logits(x, w.dtype, dev), tree, w.L)
     ops.ddtree_device_check()
-    for k in ("accept_len", "accepted_nodes", "out_tokens", "next_bonus"):
+    for k in ("accept_len", "out_tokens", "next_bonus"):
         np.testing.assert_array_equal(host(acc[k]), o_acc[k], err_msg=k)
+    n_acc = o_acc["accept_len"][0]
+    assert [g_paths[u] for u in host(acc["accepted_nodes"])[0, :n_acc]] == \
+        [o_paths[u] for u in o_acc["accepted_nodes"][0, :n_acc]]
+
+
+def _paths(parent, token, n):
+    """Token path (root excluded) of every node 0..n."""
+    out = []
+    for u in range(n + 1):
+        p, a = [], u
+        while a > 0:
+            p.append(int(token[a]))
+            a = parent[a]
+        out.append(tuple(reversed(p)))
+    return out
