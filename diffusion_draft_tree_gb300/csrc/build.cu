@@ -68,7 +68,7 @@ build_kernel(const float* __restrict__ topk_logp, const int32_t* __restrict__ to
         uint64_t best = 0ull;
         int best_i = 0;
         if (N > 0 && lane == 0) {
-            slot[0] = make_key(s_lp[0], 1, 0, 0);
+            slot[0] = make_key(__fadd_rn(0.f, s_lp[0]), 1, 0, 0);
             best = slot[0];
         }
         int n = 0, sib_pos = 1;

@@ -186,7 +186,7 @@ int ddo_build(const float* logp, const int32_t* tok, const int32_t* bonus,
         dep[0] = 0; tkn[0] = bonus[b]; pos[0] = prefix_len[b]; sc[0] = 0.0f;
         int hn = 0, n = 0;
         if (N > 0) {
-            orc_cand c0 = { lp[0], 1, 0, 0 };
+            orc_cand c0 = { sc[0] + lp[0], 1, 0, 0 }; /* root score + log-prob */
             orc_heap_push(heap, &hn, c0);
         }
         while (n < N && hn > 0) {
