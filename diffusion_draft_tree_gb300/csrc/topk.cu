@@ -15,6 +15,8 @@
 // from which warp 0 selects the K largest (value, index) keys.  The last CTA
 // of a row (atomic ticket, no spinning) loads every chunk partial in parallel,
 // merges them and writes the row's outputs.
+#include <mutex>
+
 #include "chunk.cuh"
 #include "internal.h"
 
@@ -276,3 +278,63 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
 }
 
 }  // namespace ddt
+
+// ---------------------------------------------------------------------------
+// ddtree_topk_noalloc: the same top-K for callers that may not allocate device
+// memory, so cannot supply a workspace.  Its cross-CTA partials and counters
+// live in one library-owned array of fixed size instead.
+// ---------------------------------------------------------------------------
+
+static __device__ __align__(256) unsigned char g_topk_noalloc_scratch[DDTREE_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevicesNoAlloc = 64;
+void* g_noalloc_ptr[kMaxDevicesNoAlloc];
+std::mutex g_noalloc_mu;
+
+// Device address of this device's scratch array, looked up on the first call
+// made with that device current.  In host code the array's name is only a
+// stand-in, so the address must come from cudaGetSymbolAddress.
+cudaError_t noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevicesNoAlloc) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> g(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_topk_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" ddtree_status ddtree_topk_noalloc(const void* draft_logits, int dtype, int rows, int V,
+                                             int64_t row_stride, int K, int32_t* topk_idx,
+                                             float* topk_logp, float* lse, void* stream) {
+    if (!draft_logits || !topk_idx || !topk_logp) return DDTREE_ERR_INVALID_ARG;
+    if (dtype != DDTREE_BF16 && dtype != DDTREE_FP32) return DDTREE_ERR_INVALID_ARG;
+    if (rows <= 0 || rows > 65535 || V <= 0 || row_stride < V || K < 1 || K > V)
+        return DDTREE_ERR_INVALID_ARG;
+    if (K > DDTREE_MAX_K || !ddt::topk_supported(V, dtype, K)) return DDTREE_ERR_UNSUPPORTED;
+    if ((uintptr_t)draft_logits % (dtype == DDTREE_BF16 ? 2 : 4)) return DDTREE_ERR_INVALID_ARG;
+    const size_t need = ddt::topk_workspace_bytes(rows, V, dtype);
+    if (need > DDTREE_NOALLOC_SCRATCH_BYTES) return DDTREE_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    if (need) {
+        if (noalloc_scratch(&scratch) != cudaSuccess) return DDTREE_ERR_CUDA;
+        // The array keeps whatever the previous call left in it; the row
+        // counters must start at zero.
+        const size_t counters = ddt::align_up((size_t)rows * sizeof(unsigned int), 256);
+        if (cudaMemsetAsync(scratch, 0, counters, (cudaStream_t)stream) != cudaSuccess)
+            return DDTREE_ERR_CUDA;
+    }
+    ddt::TopkArgs a{draft_logits, dtype, rows, V, row_stride, K, topk_idx, topk_logp, lse,
+                    scratch, nullptr};
+    return ddt::launch_topk(a, (cudaStream_t)stream) == cudaSuccess ? DDTREE_OK : DDTREE_ERR_CUDA;
+}

@@ -92,6 +92,30 @@ ddtree_status ddtree_topk(const void* draft_logits, int dtype, int rows, int V,
                           int64_t row_stride, int K, int32_t* topk_idx, float* topk_logp,
                           float* lse, void* workspace, size_t ws_bytes, void* stream);
 
+/* Bytes of device scratch built into the library for ddtree_topk_noalloc. */
+#define DDTREE_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/* ddtree_topk without a workspace argument.  The paper has no counterpart:
+ * this exists for callers that may not allocate device memory themselves --
+ * code that runs inside a host framework whose memory pool it does not own,
+ * or a latency-critical path where cudaMalloc's implicit synchronisation is
+ * not allowed -- and so cannot hand in a workspace.
+ * Arguments, outputs and results are those of ddtree_topk.  The cross-CTA
+ * partials use one array of DDTREE_NOALLOC_SCRATCH_BYTES inside the library
+ * (a static device array: every GPU that loads the library holds it until the
+ * process exits); the call allocates nothing.  It needs
+ * ddtree_workspace_size(DDTREE_OP_TOPK, ...) bytes of it; a larger problem is
+ * rejected with DDTREE_ERR_UNSUPPORTED before anything is enqueued (for
+ * V = 151936 bf16 that is about 390 rows).
+ * The first call made on a device looks up the array's device address on that
+ * device (make it with the device current, before any stream capture).  Each
+ * call zeroes the counters it needs with cudaMemsetAsync on `stream`.  All
+ * calls share the one array: calls whose kernels can overlap on the GPU (other
+ * streams, other threads) race and give wrong results; serialise them. */
+ddtree_status ddtree_topk_noalloc(const void* draft_logits, int dtype, int rows, int V,
+                                  int64_t row_stride, int K, int32_t* topk_idx,
+                                  float* topk_logp, float* lse, void* stream);
+
 /* Step 2 -- best-first heap tree build (Algorithm 1).
  * Pages: §4.1 (the bonus token is the root), §4.2 (the best valid tree under
  * the surrogate is the set of the N most probable prefixes), §4.3 / App. A
