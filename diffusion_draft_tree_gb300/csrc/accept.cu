@@ -23,7 +23,7 @@ namespace ddt {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kItems = 8;
+constexpr int kChunkBytes = 16384;
 constexpr int kMaxChunks = 128;
 
 struct AcceptWs {
@@ -86,7 +86,11 @@ accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nc
               int32_t* __restrict__ accept_len, int32_t* __restrict__ accepted_nodes,
               int32_t* __restrict__ out_tokens, int32_t* __restrict__ next_bonus, AcceptWs ws,
               uint32_t* err) {
-    using Chunk = RowChunk<BF16, kItems>;
+    using Chunk = SmemChunk<BF16, kChunkBytes / (BF16 ? 2 : 4)>;
+    constexpr int VEC = Chunk::VEC;
+    constexpr int PER = Chunk::NVEC / kThreads;  // vectors per thread
+    __shared__ __align__(128) uint8_t s_buf[Chunk::BYTES];
+    __shared__ __align__(8) uint64_t s_bar;
     __shared__ float s_red[2 * (kThreads / 32)];
     __shared__ int s_ired[kThreads / 32];
     __shared__ bool s_flag;
@@ -105,40 +109,64 @@ accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nc
     const size_t row = (size_t)b * R + u;
     const char* rowp = (const char*)logits + row * (size_t)row_stride * Chunk::ES;
     const int c0 = chunk * Chunk::SIZE;
-    Chunk x;
-    x.load(rowp, c0, V, aligned);
+    if (!Chunk::load(s_buf, &s_bar, rowp, c0, V, aligned)) {
+        if (tid == 0) record_error(err, ERR_ACCEPT | ERR_WAIT_TIMEOUT);
+        return;
+    }
+    const uint4* vec = reinterpret_cast<const uint4*>(s_buf);
 
     // ---- per-chunk partial ----------------------------------------------------
-    float vmax;
-    int vidx;
-    x.thread_max(c0, V, vmax, vidx);
-    // warp argmax: larger value, then lower index (vidx < 0 = empty)
+    float tmax = -INFINITY;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, vmax, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, vidx, o);
-        const bool take = (oi >= 0) && (vidx < 0 || ov > vmax || (ov == vmax && oi < vidx));
-        vmax = take ? ov : vmax;
-        vidx = take ? oi : vidx;
-    }
-    if (lane == 0) { s_red[warp] = vmax; s_ired[warp] = vidx; }
+    for (int i = 0; i < PER; ++i) tmax = fmaxf(tmax, Chunk::vmax(vec[tid + i * kThreads]));
+    const float wmax = warp_max(tmax);
+    if (lane == 0) s_red[warp] = wmax;
     __syncthreads();
     float cmax = s_red[0];
-    int cidx = s_ired[0];
 #pragma unroll
-    for (int i = 1; i < kThreads / 32; ++i) {
-        const float ov = s_red[i];
-        const int oi = s_ired[i];
-        const bool take = (oi >= 0) && (cidx < 0 || ov > cmax || (ov == cmax && oi < cidx));
-        cmax = take ? ov : cmax;
-        cidx = take ? oi : cidx;
-    }
+    for (int i = 1; i < kThreads / 32; ++i) cmax = fmaxf(cmax, s_red[i]);
     const bool sample = temperature > 0.f;
     float csum = 0.f;
-    if (sample) {
-        const float ref = (cmax == -INFINITY) ? 0.f : cmax;
-        const float w = warp_sum(x.thread_exp_sum(ref, c_exp));
+    int cidx = -1;
+    if (!sample) {
+        // lowest index holding the chunk maximum: only threads that hold it scan
+        int first = 0x7fffffff;
+        if (tmax == cmax) {
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int v = tid + i * kThreads;
+                const uint4 w = vec[v];
+                if (first == 0x7fffffff && Chunk::vmax(w) == cmax) {
+                    float x[VEC];
+                    Chunk::unpack(w, x);
+#pragma unroll
+                    for (int k = 0; k < VEC; ++k) {
+                        const int e = c0 + v * VEC + k;
+                        if (x[k] == cmax && e < V && e < first) first = e;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(0xffffffffu, first, o));
+        if (lane == 0) s_ired[warp] = first;
         __syncthreads();
+        first = s_ired[0];
+#pragma unroll
+        for (int i = 1; i < kThreads / 32; ++i) first = min(first, s_ired[i]);
+        cidx = (first == 0x7fffffff) ? -1 : first;
+    } else {
+        const float ref = (cmax == -INFINITY) ? 0.f : cmax;
+        const float off = -ref * c_exp;
+        float ts = 0.f;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            float x[VEC];
+            Chunk::unpack(vec[tid + i * kThreads], x);
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) ts += fast_exp2(fmaf(x[k], c_exp, off));
+        }
+        const float w = warp_sum(ts);
         if (lane == 0) s_red[kThreads / 32 + warp] = w;
         __syncthreads();
         for (int i = 0; i < kThreads / 32; ++i) csum += s_red[kThreads / 32 + i];
@@ -311,16 +339,14 @@ WsLayout accept_layout(int B, int N, int nch) {
 }  // namespace
 
 bool accept_supported(int V, int dtype) {
-    const int size = dtype == DDTREE_BF16 ? RowChunk<true, kItems>::SIZE
-                                          : RowChunk<false, kItems>::SIZE;
+    const int size = kChunkBytes / (dtype == DDTREE_BF16 ? 2 : 4);
     return (V + size - 1) / size <= kMaxChunks;
 }
 
 namespace {
 
 int accept_chunks(int V, int dtype) {
-    const int size = dtype == DDTREE_BF16 ? RowChunk<true, kItems>::SIZE
-                                          : RowChunk<false, kItems>::SIZE;
+    const int size = kChunkBytes / (dtype == DDTREE_BF16 ? 2 : 4);
     return (V + size - 1) / size;
 }
 

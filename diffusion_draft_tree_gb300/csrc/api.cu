@@ -87,19 +87,41 @@ ddtree_status ddtree_topk(const void* draft_logits, int dtype, int rows, int V,
     return launched(ddt::launch_topk(a, (cudaStream_t)stream));
 }
 
-ddtree_status ddtree_build(const float* topk_logp, const int32_t* topk_idx, const int32_t* bonus,
-                           const int32_t* prefix_len, int B, int L, int K, int N,
-                           int32_t* parent, int32_t* depth, int32_t* rank, int32_t* token,
+namespace {
+ddtree_status build_common(bool heap, const float* topk_logp, const int32_t* topk_idx,
+                           const int32_t* bonus, const int32_t* prefix_len, int B, int L, int K,
+                           int N, int32_t* parent, int32_t* depth, int32_t* rank, int32_t* token,
                            int32_t* pos_id, float* score, int32_t* child_count,
                            uint32_t* anc_mask, int32_t* n_nodes, void* stream) {
     if (!topk_logp || !topk_idx || !bonus || !prefix_len || !parent || !depth || !rank ||
         !token || !pos_id || !score || !child_count || !anc_mask || !n_nodes)
         return DDTREE_ERR_INVALID_ARG;
-    if (B <= 0 || L <= 0 || K <= 0 || N < 0) return DDTREE_ERR_INVALID_ARG;
+    if (B <= 0 || B > 65535 || L <= 0 || K <= 0 || N < 0) return DDTREE_ERR_INVALID_ARG;
     if (L > DDTREE_MAX_L || K > DDTREE_MAX_K || N > DDTREE_MAX_N) return DDTREE_ERR_UNSUPPORTED;
     ddt::BuildArgs a{topk_logp, topk_idx, bonus, prefix_len, B, L, K, N, parent, depth, rank,
                      token, pos_id, score, child_count, anc_mask, n_nodes, error_word()};
-    return launched(ddt::launch_build(a, (cudaStream_t)stream));
+    return launched(heap ? ddt::launch_build(a, (cudaStream_t)stream)
+                         : ddt::launch_build_level(a, (cudaStream_t)stream));
+}
+}  // namespace
+
+ddtree_status ddtree_build(const float* topk_logp, const int32_t* topk_idx, const int32_t* bonus,
+                           const int32_t* prefix_len, int B, int L, int K, int N,
+                           int32_t* parent, int32_t* depth, int32_t* rank, int32_t* token,
+                           int32_t* pos_id, float* score, int32_t* child_count,
+                           uint32_t* anc_mask, int32_t* n_nodes, void* stream) {
+    return build_common(false, topk_logp, topk_idx, bonus, prefix_len, B, L, K, N, parent, depth,
+                        rank, token, pos_id, score, child_count, anc_mask, n_nodes, stream);
+}
+
+ddtree_status ddtree_build_heap(const float* topk_logp, const int32_t* topk_idx,
+                                const int32_t* bonus, const int32_t* prefix_len, int B, int L,
+                                int K, int N, int32_t* parent, int32_t* depth, int32_t* rank,
+                                int32_t* token, int32_t* pos_id, float* score,
+                                int32_t* child_count, uint32_t* anc_mask, int32_t* n_nodes,
+                                void* stream) {
+    return build_common(true, topk_logp, topk_idx, bonus, prefix_len, B, L, K, N, parent, depth,
+                        rank, token, pos_id, score, child_count, anc_mask, n_nodes, stream);
 }
 
 ddtree_status ddtree_tree_attn(const void* q, const void* k_cache, const void* v_cache,

@@ -1,0 +1,294 @@
+// build_level.cu -- step 2 of a DDTree round computed level by level.
+//
+// Algorithm 1 of "Accelerating Speculative Decoding with Block Diffusion Draft
+// Trees" (§4.3, App. A) pops the N best prefixes one at a time.  Its result is
+// fixed by the priority order alone: the first N prefixes of the restricted
+// set in that order (score desc, depth asc, earlier parent, lower rank), in
+// that order (§4.2 / App. A: ancestors are at least as probable as their
+// descendants, so the top N are prefix-closed).  That set can be built with L
+// parallel steps instead of N sequential pops:
+//
+//   T_0 = {}; for d = 1..L:  T_d = top-N( T_{d-1}  U  children of the
+//                                          depth-(d-1) nodes of T_{d-1} )
+//
+// T_d is the top N among all prefixes of depth <= d (a depth-d prefix in it
+// has its parent in it, and that parent is among the top N of depth <= d-1).
+// When T_{d-1} is full, a child must beat its last element: a strictly higher
+// score, because the child is deeper.  Children of one parent are generated in
+// rank order, sorted (bitonic, shared memory) and merged into T with a
+// rank-by-binary-search merge.  The result -- nodes, their order, fp32 scores
+// formed as parent score + log-prob -- is identical to the heap's.
+//
+// One CTA of 512 threads per sequence.  T holds 64-bit keys:
+//   [63:32] orderable fp32 score, [31:27] 31 - depth,
+//   [26:16] 2046 - parent position (2047 for the root), [15:10] 63 - rank.
+// Parent positions refer to T_{d-1} while level d is built and are remapped to
+// the new positions when the level ends (the relative order of survivors, and
+// so every comparison, is unchanged by the remap).
+#include "common.cuh"
+#include "internal.h"
+
+#include "../../include/ddtree.h"
+
+namespace ddt {
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kCandCap = 2048;  // children merged per batch
+constexpr int kPairsPerThread = kCandCap / kThreads;
+
+DDT_DEV uint64_t lkey(float score, int depth, int ppos, int rank) {
+    return ((uint64_t)ord_from_float(score) << 32) | ((uint32_t)(31 - depth) << 27) |
+           ((uint32_t)(2046 - ppos) << 16) | ((uint32_t)(63 - rank) << 10);
+}
+DDT_DEV float lk_score(uint64_t k) { return float_from_ord((uint32_t)(k >> 32)); }
+DDT_DEV int lk_depth(uint64_t k) { return 31 - (int)((uint32_t)k >> 27); }
+DDT_DEV int lk_ppos(uint64_t k) { return 2046 - (int)(((uint32_t)k >> 16) & 0x7ffu); }
+DDT_DEV int lk_rank(uint64_t k) { return 63 - (int)(((uint32_t)k >> 10) & 0x3fu); }
+DDT_DEV uint64_t lk_with_ppos(uint64_t k, int ppos) {
+    return (k & ~(0x7ffull << 16)) | ((uint64_t)(2046 - ppos) << 16);
+}
+
+// Exclusive scan of one int per thread over the CTA; *total gets the sum.
+DDT_DEV int block_scan(int v, int* s_warp, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    int before = 0, tot = 0;
+#pragma unroll
+    for (int i = 0; i < kThreads / 32; ++i) {
+        const int w = s_warp[i];
+        before += (i < warp) ? w : 0;
+        tot += w;
+    }
+    *total = tot;
+    __syncthreads();
+    return before + incl - v;
+}
+
+// Number of keys of the descending array a[0..n) that are larger than x.
+DDT_DEV int count_greater(const uint64_t* a, int n, uint64_t x) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (a[mid] > x) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(kThreads)
+build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restrict__ topk_idx,
+                   const int32_t* __restrict__ bonus, const int32_t* __restrict__ prefix_len,
+                   int L, int K, int N, int32_t* __restrict__ parent, int32_t* __restrict__ depth,
+                   int32_t* __restrict__ rank, int32_t* __restrict__ token,
+                   int32_t* __restrict__ pos_id, float* __restrict__ score,
+                   int32_t* __restrict__ child_count, uint32_t* __restrict__ anc_mask,
+                   int32_t* __restrict__ n_nodes) {
+    __shared__ uint64_t s_T[2][DDTREE_MAX_N];
+    __shared__ int16_t s_orig[2][DDTREE_MAX_N];
+    __shared__ __align__(16) uint64_t s_cand[kCandCap];
+    __shared__ int16_t s_plist[DDTREE_MAX_N];  // parents: T_{d-1} positions
+    __shared__ float s_pscore[DDTREE_MAX_N];   // ... and their scores
+    __shared__ int16_t s_map[DDTREE_MAX_N];
+    __shared__ float s_lp[DDTREE_MAX_L * DDTREE_MAX_K];
+    __shared__ int s_warp[kThreads / 32];
+    __shared__ int s_flag;
+
+    const int b = blockIdx.x, tid = threadIdx.x;
+    const int LK = L * K;
+    for (int i = tid; i < LK; i += kThreads) s_lp[i] = topk_logp[(size_t)b * LK + i];
+    __syncthreads();
+
+    int t = 0, cur = 0;
+    for (int d = 1; d <= L && N > 0; ++d) {
+        // ---- parents: the depth-(d-1) nodes of T, in T order -----------------------
+        int npar;
+        if (d == 1) {
+            npar = 1;
+            if (tid == 0) {
+                s_plist[0] = -1;
+                s_pscore[0] = 0.f;  // the root: the empty prefix, probability 1
+            }
+            __syncthreads();
+        } else {
+            int f[2] = {0, 0};
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int i = tid * 2 + j;
+                f[j] = (i < t && lk_depth(s_T[cur][i]) == d - 1) ? 1 : 0;
+            }
+            int tot;
+            int pos = block_scan(f[0] + f[1], s_warp, &tot);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                if (f[j]) {
+                    s_plist[pos] = (int16_t)(tid * 2 + j);
+                    s_pscore[pos] = lk_score(s_T[cur][tid * 2 + j]);
+                    ++pos;
+                }
+            }
+            npar = tot;
+            __syncthreads();
+        }
+        if (npar == 0) break;
+        for (int i = tid; i < t; i += kThreads) s_orig[cur][i] = (int16_t)i;
+
+        // ---- children in batches of kCandCap (parent, rank) pairs --------------------
+        const int pairs = npar * K;
+        const float* lp = s_lp + (d - 1) * K;
+        for (int base = 0; base < pairs; base += kCandCap) {
+            const bool full = (t == N);
+            const float theta = full ? lk_score(s_T[cur][t - 1]) : 0.f;
+            uint64_t key[kPairsPerThread];
+            int cnt = 0;
+#pragma unroll
+            for (int j = 0; j < kPairsPerThread; ++j) {
+                const int q = base + tid * kPairsPerThread + j;
+                key[j] = 0ull;
+                if (q < pairs) {
+                    const int pi = q / K, r = q - pi * K;
+                    const int pp = s_plist[pi];
+                    const float sc = __fadd_rn(s_pscore[pi], lp[r]);
+                    if (!full || sc > theta) {
+                        key[j] = lkey(sc, d, pp, r);
+                        ++cnt;
+                    }
+                }
+            }
+            int c;
+            int pos = block_scan(cnt, s_warp, &c);
+#pragma unroll
+            for (int j = 0; j < kPairsPerThread; ++j)
+                if (key[j]) s_cand[pos++] = key[j];
+            if (c == 0) {
+                __syncthreads();
+                continue;
+            }
+            // bitonic sort, descending; pad to a power of two with zeros
+            int p2 = 1;
+            while (p2 < c) p2 <<= 1;
+            for (int i = c + tid; i < p2; i += kThreads) s_cand[i] = 0ull;
+            __syncthreads();
+            for (int k2 = 2; k2 <= p2; k2 <<= 1) {
+                for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
+                    for (int i = tid; i < p2; i += kThreads) {
+                        const int ix = i ^ j2;
+                        if (ix > i) {
+                            const uint64_t a = s_cand[i], e = s_cand[ix];
+                            const bool desc = (i & k2) == 0;
+                            if (desc ? (a < e) : (a > e)) {
+                                s_cand[i] = e;
+                                s_cand[ix] = a;
+                            }
+                        }
+                    }
+                    __syncthreads();
+                }
+            }
+            // merge T[0..t) and cand[0..c) by output rank; keep the first N
+            const int nxt = cur ^ 1;
+            for (int i = tid; i < t + c; i += kThreads) {
+                if (i < t) {
+                    const uint64_t a = s_T[cur][i];
+                    const int rk = i + count_greater(s_cand, c, a);
+                    if (rk < N) {
+                        s_T[nxt][rk] = a;
+                        s_orig[nxt][rk] = s_orig[cur][i];
+                    }
+                } else {
+                    const int j = i - t;
+                    const uint64_t e = s_cand[j];
+                    const int rk = j + count_greater(s_T[cur], t, e);
+                    if (rk < N) {
+                        s_T[nxt][rk] = e;
+                        s_orig[nxt][rk] = -1;
+                    }
+                }
+            }
+            t = min(N, t + c);
+            cur = nxt;
+            __syncthreads();
+        }
+
+        // ---- level end: parent positions T_{d-1} -> T_d; stop when nothing is deep --
+        if (tid == 0) s_flag = 0;
+        for (int i = tid; i < t; i += kThreads) {
+            const int o = s_orig[cur][i];
+            if (o >= 0) s_map[o] = (int16_t)i;
+        }
+        __syncthreads();
+        for (int i = tid; i < t; i += kThreads) {
+            const uint64_t k = s_T[cur][i];
+            const int pp = lk_ppos(k);
+            if (pp >= 0) s_T[cur][i] = lk_with_ppos(k, s_map[pp]);
+            if (lk_depth(k) == d) s_flag = 1;
+        }
+        __syncthreads();
+        if (!s_flag) break;
+    }
+
+    // ---- outputs: node u = position u-1 of T ------------------------------------------
+    const int n = t;
+    int16_t* s_par = (int16_t*)s_cand;                    // [N+1]
+    int* s_cc = (int*)(s_cand + (DDTREE_MAX_N + 8) / 4);  // [N+1]
+    for (int u = tid; u <= n; u += kThreads) {
+        s_par[u] = (u == 0) ? (int16_t)-1 : (int16_t)(lk_ppos(s_T[cur][u - 1]) + 1);
+        s_cc[u] = 0;
+    }
+    __syncthreads();
+    for (int u = 1 + tid; u <= n; u += kThreads) atomicAdd(&s_cc[s_par[u]], 1);
+    __syncthreads();
+    const int R = N + 1, W = (N + 1 + 31) / 32;
+    const int P = prefix_len[b];
+    for (int u = tid; u < R; u += kThreads) {
+        const size_t o = (size_t)b * R + u;
+        if (u == 0) {
+            parent[o] = -1; depth[o] = 0; rank[o] = -1; token[o] = bonus[b]; pos_id[o] = P;
+            score[o] = 0.f; child_count[o] = s_cc[0];
+        } else if (u <= n) {
+            const uint64_t k = s_T[cur][u - 1];
+            const int dp = lk_depth(k), rk = lk_rank(k);
+            parent[o] = s_par[u];
+            depth[o] = dp;
+            rank[o] = rk;
+            token[o] = topk_idx[(size_t)b * LK + (dp - 1) * K + rk];
+            pos_id[o] = P + dp;
+            score[o] = lk_score(k);
+            child_count[o] = s_cc[u];
+        } else {
+            parent[o] = -1; depth[o] = -1; rank[o] = -1; token[o] = -1; pos_id[o] = -1;
+            score[o] = -INFINITY;
+            child_count[o] = 0;
+        }
+    }
+    for (int i = tid; i < R * W; i += kThreads) {
+        const int u = i / W, w = i - u * W;
+        uint32_t word = 0u;
+        if (u <= n) {
+            for (int a = u; a >= 0; a = s_par[a])
+                if ((a >> 5) == w) word |= 1u << (a & 31);
+        }
+        anc_mask[(size_t)b * R * W + i] = word;
+    }
+    if (tid == 0) n_nodes[b] = n;
+}
+
+}  // namespace
+
+cudaError_t launch_build_level(const BuildArgs& a, cudaStream_t s) {
+    build_level_kernel<<<a.B, kThreads, 0, s>>>(a.topk_logp, a.topk_idx, a.bonus, a.prefix_len,
+                                                a.L, a.K, a.N, a.parent, a.depth, a.rank,
+                                                a.token, a.pos_id, a.score, a.child_count,
+                                                a.anc_mask, a.n_nodes);
+    return cudaGetLastError();
+}
+
+}  // namespace ddt

@@ -1,92 +1,99 @@
-// chunk.cuh -- one CTA's slice of a vocabulary-sized logit row, held in
-// registers.  256 threads each own ITEMS 16-byte vectors; vector slot j of the
-// chunk is (it * 256 + tid), so every load instruction of a warp touches 512
-// contiguous bytes (fully coalesced).  Elements past the row's end read -inf.
+// chunk.cuh -- one CTA's slice of a vocabulary-sized logit row, staged in
+// shared memory.  Thread 0 issues one bulk copy (cp.async.bulk, completing on
+// an mbarrier) for the 16-byte-aligned body of the slice; the few elements of
+// an unaligned row or of a ragged tail are loaded by the threads themselves.
+// Elements past the row's end read -inf.  Every thread then reads the slice
+// from shared memory as 16-byte vectors.
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace ddt {
 
-template <bool BF16, int ITEMS>
-struct RowChunk {
+template <bool BF16, int SIZE_>
+struct SmemChunk {
     static constexpr int THREADS = 256;
-    static constexpr int ES = BF16 ? 2 : 4;          // element bytes
-    static constexpr int VEC = 16 / ES;               // elements per vector
-    static constexpr int SIZE = THREADS * ITEMS * VEC;  // elements per chunk
+    static constexpr int SIZE = SIZE_;          // elements per chunk
+    static constexpr int ES = BF16 ? 2 : 4;     // element bytes
+    static constexpr int VEC = 16 / ES;         // elements per 16-byte vector
+    static constexpr int NVEC = SIZE / VEC;     // vectors per chunk
+    static constexpr int BYTES = SIZE * ES;
+    static_assert(NVEC % THREADS == 0, "whole vectors per thread");
 
-    uint32_t w[ITEMS][4];
-
-    // Loads elements [c0, c0 + SIZE) of a row that starts at `rowp`.
-    // `aligned`: the row start is 16-byte aligned (vector loads allowed).
-    DDT_DEV void load(const char* __restrict__ rowp, int c0, int V, bool aligned) {
-#pragma unroll
-        for (int it = 0; it < ITEMS; ++it) {
-            const int e0 = c0 + (it * THREADS + (int)threadIdx.x) * VEC;
-            if (aligned && e0 + VEC <= V) {
-                const uint4 r = ld_stream_v4(rowp + (size_t)e0 * ES);
-                w[it][0] = r.x; w[it][1] = r.y; w[it][2] = r.z; w[it][3] = r.w;
-            } else if (BF16) {
-#pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    const int e = e0 + 2 * p;
-                    const uint32_t lo = (e < V) ? (uint32_t)__ldg((const unsigned short*)rowp + e)
-                                                : 0xff80u;
-                    const uint32_t hi = (e + 1 < V)
-                                            ? (uint32_t)__ldg((const unsigned short*)rowp + e + 1)
-                                            : 0xff80u;
-                    w[it][p] = lo | (hi << 16);
-                }
+    // Stages elements [c0, c0 + SIZE) of the row at `rowp` into `buf`
+    // (16-byte aligned, BYTES long).  All threads call it; returns once the
+    // data is visible to every thread (false if the copy never completed).
+    DDT_DEV static bool load(uint8_t* buf, uint64_t* bar, const char* rowp, int c0, int V,
+                             bool aligned) {
+        __shared__ int s_no_abort;
+        const int n_in = max(0, min(SIZE, V - c0));             // elements of the row
+        const int n_bulk = aligned ? (n_in / VEC) * VEC : 0;    // by the copy engine
+        if (threadIdx.x == 0) {
+            s_no_abort = 0;
+            sm100::mbar_init(bar, 1);
+            sm100::mbar_init_fence();
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            if (n_bulk > 0) {
+                sm100::mbar_arrive_expect_tx(bar, (uint32_t)(n_bulk * ES));
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+                    " [%0], [%1], %2, [%3];" ::"r"(sm100::smem_u32(buf)),
+                    "l"(rowp + (size_t)c0 * ES), "r"((uint32_t)(n_bulk * ES)),
+                    "r"(sm100::smem_u32(bar))
+                    : "memory");
             } else {
-#pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    const int e = e0 + p;
-                    w[it][p] = (e < V) ? __ldg((const unsigned int*)rowp + e) : 0xff800000u;
-                }
+                sm100::mbar_arrive(bar);
             }
         }
-    }
-
-    DDT_DEV float elem(int it, int k) const {
-        if (BF16) return (k & 1) ? bf16hi(w[it][k >> 1]) : bf16lo(w[it][k >> 1]);
-        return __uint_as_float(w[it][k]);
-    }
-
-    DDT_DEV static int index(int c0, int it, int k) {
-        return c0 + (it * THREADS + (int)threadIdx.x) * VEC + k;
-    }
-
-    // Largest element of this thread and its lowest index (-1 if the thread
-    // holds no element of the row).
-    DDT_DEV void thread_max(int c0, int V, float& vmax, int& vidx) const {
-        vmax = -INFINITY;
-        vidx = -1;
-#pragma unroll
-        for (int it = 0; it < ITEMS; ++it) {
-#pragma unroll
-            for (int k = 0; k < VEC; ++k) {
-                const float x = elem(it, k);
-                if (it == 0 && k == 0) {
-                    const int e = index(c0, 0, 0);
-                    if (e < V) { vmax = x; vidx = e; }
-                } else if (x > vmax) {
-                    vmax = x;
-                    vidx = index(c0, it, k);
-                }
+        for (int i = n_bulk + (int)threadIdx.x; i < SIZE; i += THREADS) {
+            if (BF16) {
+                const unsigned short v =
+                    (i < n_in) ? __ldg((const unsigned short*)rowp + c0 + i) : (unsigned short)0xff80u;
+                ((unsigned short*)buf)[i] = v;
+            } else {
+                const unsigned int v = (i < n_in) ? __ldg((const unsigned int*)rowp + c0 + i)
+                                                  : 0xff800000u;
+                ((unsigned int*)buf)[i] = v;
             }
         }
+        const bool ok = sm100::mbar_wait(bar, 0, (volatile int*)&s_no_abort);
+        return __syncthreads_and(ok) != 0;  // uniform across the CTA
     }
 
-    // sum over this thread's elements of 2^((x - ref) * c); -inf elements add 0.
-    DDT_DEV float thread_exp_sum(float ref, float c) const {
-        float s = 0.f;
-        const float off = -ref * c;
+    // Vector v of the chunk as 8 (bf16) or 4 (fp32) floats.
+    DDT_DEV static void unpack(const uint4& w, float (&x)[VEC]) {
+        if (BF16) {
+            const uint32_t a[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int it = 0; it < ITEMS; ++it) {
-#pragma unroll
-            for (int k = 0; k < VEC; ++k) s += fast_exp2(fmaf(elem(it, k), c, off));
+            for (int p = 0; p < 4; ++p) {
+                x[2 * p] = bf16lo(a[p]);
+                x[2 * p + 1] = bf16hi(a[p]);
+            }
+        } else {
+            x[0] = __uint_as_float(w.x);
+            x[1] = __uint_as_float(w.y);
+            x[2] = __uint_as_float(w.z);
+            x[3] = __uint_as_float(w.w);
         }
-        return s;
+    }
+
+    // Largest element of a vector (bf16: packed max, two elements per op).
+    DDT_DEV static float vmax(const uint4& w) {
+        if (BF16) {
+            const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&w.x);
+            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w.y);
+            const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&w.z);
+            const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&w.w);
+            const __nv_bfloat162 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
+            return fmaxf(__low2float(m), __high2float(m));
+        }
+        return fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
+                     fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
     }
 };
 

@@ -40,7 +40,8 @@ struct BuildArgs {
     int32_t* n_nodes;
     uint32_t* err;
 };
-cudaError_t launch_build(const BuildArgs& a, cudaStream_t s);
+cudaError_t launch_build(const BuildArgs& a, cudaStream_t s);        // warp heap
+cudaError_t launch_build_level(const BuildArgs& a, cudaStream_t s);  // level-synchronous
 
 // ---- step 3: tree attention --------------------------------------------------
 struct AttnArgs {

@@ -4,17 +4,17 @@
 // prefix set).
 //
 // One row = one (sequence, draft position), V logits.  A row is split into
-// chunks of RowChunk::SIZE elements, one CTA per (chunk, row), so even a single
-// sequence fills the GPU.  Each CTA streams its chunk once from HBM into
-// registers and then computes, without touching memory again:
+// chunks of 16 KB (8192 bf16 or 4096 fp32 logits), one CTA per (chunk, row),
+// so even a single sequence fills the GPU.  A CTA brings its chunk into shared
+// memory with one bulk copy and computes from there, touching HBM once:
 //   m_c = max, s_c = sum exp(x - m_c), and its K best (value, index) keys.
 // Top-K selection avoids per-element insertion: every warp finds tau_w, the
 // K-th largest of its 32 lane maxima (a warp bitonic sort), the CTA takes
 // tau = max_w tau_w -- a lower bound on the chunk's K-th largest value -- and
-// only elements >= tau (typically ~2K of 16K) are appended to a shared buffer
-// from which warp 0 selects the K largest (value, index) keys.  The last CTA
-// of a row (atomic ticket, no spinning) loads every chunk partial in parallel,
-// merges them and writes the row's outputs.
+// only elements >= tau (typically ~2K of 8K) are appended to a shared buffer.
+// Each candidate's rank is then counted by its own thread (no sort).  The last
+// CTA of a row (atomic ticket, no spinning) loads every chunk partial in
+// parallel and ranks them the same way.
 #include <mutex>
 
 #include "chunk.cuh"
@@ -27,39 +27,15 @@ namespace ddt {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kItems = 8;
+constexpr int kChunkBytes = 16384;
 constexpr int kCandCap = 1024;
+constexpr int kMaxChunks = 128;
 
 struct TopkPartial {
     float m;   // chunk max
     float s;   // sum exp(x - m) over the chunk
     uint64_t keys[DDTREE_MAX_K];
 };
-
-// The K largest keys of cand[0..cnt) into sel[0..K), sorted descending, 0 where
-// fewer than K exist.  One warp.  Small sets: each key's rank is counted
-// directly (no shuffles on the critical path); large sets: bitonic sort/merge.
-DDT_DEV void warp_select(const uint64_t* cand, int cnt, int K, uint64_t* sel) {
-    const int lane = threadIdx.x & 31;
-    if (cnt <= 64) {
-        if (lane < K) sel[lane] = 0ull;
-        __syncwarp();
-        for (int i = lane; i < cnt; i += 32) {
-            const uint64_t ki = cand[i];
-            int rank = 0;
-            for (int j = 0; j < cnt; ++j) rank += (cand[j] > ki) ? 1 : 0;
-            if (rank < K) sel[rank] = ki;
-        }
-    } else {
-        uint64_t best = 0ull;
-        for (int g = 0; g < cnt; g += 32) {
-            const uint64_t v = (g + lane < cnt) ? cand[g + lane] : 0ull;
-            best = warp_merge_desc(best, warp_sort_desc(v));
-        }
-        if (lane < K) sel[lane] = best;
-    }
-    __syncwarp();
-}
 
 // Warp-wide bitonic sort of one uint32 per lane, descending.
 DDT_DEV uint32_t warp_sort_desc_u32(uint32_t v) {
@@ -76,18 +52,33 @@ DDT_DEV uint32_t warp_sort_desc_u32(uint32_t v) {
     return v;
 }
 
+// Rank of every key of cand[0..cnt) (keys are distinct) by counting the larger
+// ones; keys of rank < K land in sel[rank].  Whole CTA; sel must be zeroed.
+DDT_DEV void cta_rank_select(const uint64_t* cand, int cnt, int K, uint64_t* sel) {
+    for (int i = threadIdx.x; i < cnt; i += kThreads) {
+        const uint64_t ki = cand[i];
+        int rank = 0;
+        for (int j = 0; j < cnt; ++j) rank += (cand[j] > ki) ? 1 : 0;
+        if (rank < K) sel[rank] = ki;
+    }
+}
+
 template <bool BF16>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads)
 topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, int nchunks,
             bool aligned, int32_t* __restrict__ topk_idx, float* __restrict__ topk_logp,
             float* __restrict__ lse, TopkPartial* __restrict__ parts,
             unsigned int* __restrict__ tickets) {
-    using Chunk = RowChunk<BF16, kItems>;
+    using Chunk = SmemChunk<BF16, kChunkBytes / (BF16 ? 2 : 4)>;
+    constexpr int VEC = Chunk::VEC;
+    constexpr int PER = Chunk::NVEC / kThreads;  // vectors per thread
+    __shared__ __align__(128) uint8_t s_buf[Chunk::BYTES];
+    __shared__ __align__(8) uint64_t s_bar;
     __shared__ uint64_t s_cand[kCandCap];
     __shared__ uint64_t s_sel[DDTREE_MAX_K];
     __shared__ float s_wmax[kThreads / 32], s_wsum[kThreads / 32];
     __shared__ uint32_t s_wtau[kThreads / 32];
-    __shared__ float s_m[kCandCap / 8], s_s[kCandCap / 8];
+    __shared__ float s_m[kMaxChunks], s_s[kMaxChunks];
     __shared__ int s_cnt;
     __shared__ bool s_last;
 
@@ -96,17 +87,18 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     const int c0 = chunk * Chunk::SIZE;
     const char* rowp = (const char*)logits + (size_t)row * (size_t)row_stride * Chunk::ES;
     if (tid == 0) s_cnt = 0;
+    if (tid < K) s_sel[tid] = 0ull;
+    if (!Chunk::load(s_buf, &s_bar, rowp, c0, V, aligned)) return;  // copy never landed
+    const uint4* vec = reinterpret_cast<const uint4*>(s_buf);
 
-    Chunk x;
-    x.load(rowp, c0, V, aligned);
-
-    // ---- lane maxima; tau_w = K-th largest lane maximum of the warp -------------
-    float vmax;
-    int vidx;
-    x.thread_max(c0, V, vmax, vidx);
-    const uint32_t lane_ord = (vidx >= 0) ? ord_from_float(vmax) : 0u;
+    // ---- pass 1: lane maxima; tau_w = K-th largest lane maximum of the warp ------
+    float tmax = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) tmax = fmaxf(tmax, Chunk::vmax(vec[tid + i * kThreads]));
+    const bool has = c0 + tid * VEC < V;
+    const uint32_t lane_ord = has ? ord_from_float(tmax) : 0u;
     const uint32_t tau_w = __shfl_sync(0xffffffffu, warp_sort_desc_u32(lane_ord), K - 1);
-    const float wmax = warp_max(vmax);
+    const float wmax = warp_max(tmax);
     if (lane == 0) {
         s_wmax[warp] = wmax;
         s_wtau[warp] = tau_w;
@@ -122,46 +114,51 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
         tau = max(tau, s_wtau[i]);
     }
 
-    // ---- sum of exponentials ------------------------------------------------
+    // ---- pass 2: sum of exponentials; candidates -----------------------------------
     const float ref = (m == -INFINITY) ? 0.f : m;
-    const float ws = warp_sum(x.thread_exp_sum(ref, kLog2e));
-    if (lane == 0) s_wsum[warp] = ws;
-
-    // ---- candidates ---------------------------------------------------------
-    if (vidx >= 0 && lane_ord >= tau) {
-        const float tv = float_from_ord(tau);
+    const float off = -ref * kLog2e;
+    const float tv = (tau == 0u) ? -INFINITY : float_from_ord(tau);
+    float ssum = 0.f;
 #pragma unroll
-        for (int it = 0; it < kItems; ++it) {
+    for (int i = 0; i < PER; ++i) {
+        const int v = tid + i * kThreads;
+        const uint4 w = vec[v];
+        float x[VEC];
+        Chunk::unpack(w, x);
 #pragma unroll
-            for (int k = 0; k < Chunk::VEC; ++k) {
-                const float v = x.elem(it, k);
-                const int e = Chunk::index(c0, it, k);
-                const bool cand = (tau == 0u) ? (e < V) : (v >= tv);
-                if (cand) {
+        for (int k = 0; k < VEC; ++k) ssum += fast_exp2(fmaf(x[k], kLog2e, off));
+        if (Chunk::vmax(w) >= tv) {
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) {
+                const int e = c0 + v * VEC + k;
+                if (x[k] >= tv && e < V) {
                     const int pos = atomicAdd(&s_cnt, 1);
-                    if (pos < kCandCap) s_cand[pos] = value_index_key(v, (uint32_t)e);
+                    if (pos < kCandCap) s_cand[pos] = value_index_key(x[k], (uint32_t)e);
                 }
             }
         }
     }
+    ssum = warp_sum(ssum);
+    if (lane == 0) s_wsum[warp] = ssum;
     __syncthreads();
     const int cnt = s_cnt;
 
     if (cnt <= kCandCap) {
-        if (warp == 0) warp_select(s_cand, cnt, K, s_sel);
+        cta_rank_select(s_cand, cnt, K, s_sel);
     } else {
-        // Degenerate ties overflowed the buffer: exact K-round selection over
-        // the registers (rare path; correctness only).
+        // Degenerate ties overflowed the buffer: exact K-round selection
+        // (rare path; correctness only).
         uint64_t prev = ~0ull;
         for (int r = 0; r < K; ++r) {
             uint64_t tb = 0ull;
-#pragma unroll
-            for (int it = 0; it < kItems; ++it) {
-#pragma unroll
-                for (int k = 0; k < Chunk::VEC; ++k) {
-                    const int e = Chunk::index(c0, it, k);
+            for (int i = 0; i < PER; ++i) {
+                const int v = tid + i * kThreads;
+                float x[VEC];
+                Chunk::unpack(vec[v], x);
+                for (int k = 0; k < VEC; ++k) {
+                    const int e = c0 + v * VEC + k;
                     if (e < V) {
-                        const uint64_t key = value_index_key(x.elem(it, k), (uint32_t)e);
+                        const uint64_t key = value_index_key(x[k], (uint32_t)e);
                         if (key < prev && key > tb) tb = key;
                     }
                 }
@@ -177,14 +174,11 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
             __syncthreads();
         }
     }
+    __syncthreads();
 
     float S = 0.f;
-    if (warp == 0) {
-        if (lane == 0) {
-            for (int i = 0; i < kThreads / 32; ++i) S += s_wsum[i];
-        }
-        S = __shfl_sync(0xffffffffu, S, 0);
-    }
+#pragma unroll
+    for (int i = 0; i < kThreads / 32; ++i) S += s_wsum[i];
     float M = ref;
 
     if (nchunks > 1) {
@@ -212,6 +206,9 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
             s_m[c] = __ldcg(&rp[c].m);
             s_s[c] = __ldcg(&rp[c].s);
         }
+        if (tid < K) s_sel[tid] = 0ull;
+        __syncthreads();
+        cta_rank_select(s_cand, nk, K, s_sel);  // zero keys (short lists) rank last
         __syncthreads();
         if (warp != 0) return;
         float mm = -INFINITY;
@@ -221,7 +218,6 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
         float ss = 0.f;
         for (int c = lane; c < nchunks; c += 32) ss += s_s[c] * fast_exp2((s_m[c] - M) * kLog2e);
         S = warp_sum(ss);
-        warp_select(s_cand, nk, K, s_sel);
     } else if (warp != 0) {
         return;
     }
@@ -235,16 +231,17 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     if (lane == 0 && lse) lse[row] = M + logS;
 }
 
+int chunk_elems(int dtype) { return kChunkBytes / (dtype == DDTREE_BF16 ? 2 : 4); }
+
 }  // namespace
 
 bool topk_supported(int V, int dtype, int K) {
     const int nch = topk_chunks(V, dtype);
-    return nch <= kCandCap / 8 && nch * K <= kCandCap;
+    return nch <= kMaxChunks && nch * K <= kCandCap;
 }
 
 int topk_chunks(int V, int dtype) {
-    const int size = dtype == DDTREE_BF16 ? RowChunk<true, kItems>::SIZE
-                                          : RowChunk<false, kItems>::SIZE;
+    const int size = chunk_elems(dtype);
     return (V + size - 1) / size;
 }
 

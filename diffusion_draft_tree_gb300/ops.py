@@ -51,6 +51,7 @@ def _load() -> ctypes.CDLL:
     lib.ddtree_workspace_size.restype = sz
     lib.ddtree_topk.argtypes = [P, i32, i32, i32, i64, i32, P, P, P, P, sz, P]
     lib.ddtree_build.argtypes = [P, P, P, P, i32, i32, i32, i32] + [P] * 9 + [P]
+    lib.ddtree_build_heap.argtypes = lib.ddtree_build.argtypes
     lib.ddtree_tree_attn.argtypes = [P, P, P, i64, P, P, P, P, P, i32, i32, i32, i32, i32, f32,
                                      P, P, P, sz, P]
     lib.ddtree_accept.argtypes = [P, i32, i64, P, P, P, i32, i32, i32, i32, f32, u64, u64, P, P,
@@ -58,16 +59,16 @@ def _load() -> ctypes.CDLL:
     lib.ddtree_device_check.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
     lib.ddtree_status_str.argtypes = [i32]
     lib.ddtree_status_str.restype = ctypes.c_char_p
-    for f in ("ddtree_topk", "ddtree_build", "ddtree_tree_attn", "ddtree_accept",
-              "ddtree_device_check"):
+    for f in ("ddtree_topk", "ddtree_build", "ddtree_build_heap", "ddtree_tree_attn",
+              "ddtree_accept", "ddtree_device_check"):
         getattr(lib, f).restype = i32
     return lib
 
 
 lib = _load()
 
-EXPORTED = ("ddtree_workspace_size", "ddtree_topk", "ddtree_build", "ddtree_tree_attn",
-            "ddtree_accept", "ddtree_device_check", "ddtree_status_str")
+EXPORTED = ("ddtree_workspace_size", "ddtree_topk", "ddtree_build", "ddtree_build_heap",
+            "ddtree_tree_attn", "ddtree_accept", "ddtree_device_check", "ddtree_status_str")
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -122,9 +123,12 @@ def ddtree_topk(draft_logits, K, topk_idx, topk_logp, lse=None, workspace=None, 
         _stream(stream)))
 
 
-def ddtree_build(topk_logp, topk_idx, bonus, prefix_len, N, out: dict, stream=None):
+def ddtree_build(topk_logp, topk_idx, bonus, prefix_len, N, out: dict, stream=None,
+                 heap=False):
+    """heap=False: the level-synchronous build; heap=True: ddtree_build_heap."""
     B, L, K = topk_logp.shape
-    _check("ddtree_build", lib.ddtree_build(
+    fn = lib.ddtree_build_heap if heap else lib.ddtree_build
+    _check("ddtree_build", fn(
         _ptr(topk_logp), _ptr(topk_idx), _ptr(bonus), _ptr(prefix_len), B, L, K, N,
         _ptr(out["parent"]), _ptr(out["depth"]), _ptr(out["rank"]), _ptr(out["token"]),
         _ptr(out["pos_id"]), _ptr(out["score"]), _ptr(out["child_count"]),
@@ -193,10 +197,10 @@ def tree_buffers(B: int, N: int, device) -> dict:
     return t
 
 
-def build(topk_logp, topk_idx, bonus, prefix_len, N: int, stream=None) -> dict:
+def build(topk_logp, topk_idx, bonus, prefix_len, N: int, stream=None, heap=False) -> dict:
     B = topk_logp.shape[0]
     t = tree_buffers(B, N, topk_logp.device)
-    ddtree_build(topk_logp, topk_idx, bonus, prefix_len, N, t, stream)
+    ddtree_build(topk_logp, topk_idx, bonus, prefix_len, N, t, stream, heap)
     return t
 
 

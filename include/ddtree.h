@@ -106,7 +106,7 @@ ddtree_status ddtree_topk(const void* draft_logits, int dtype, int rows, int V,
  * process exits); the call allocates nothing.  It needs
  * ddtree_workspace_size(DDTREE_OP_TOPK, ...) bytes of it; a larger problem is
  * rejected with DDTREE_ERR_UNSUPPORTED before anything is enqueued (for
- * V = 151936 bf16 that is about 390 rows).
+ * V = 151936 bf16 that is about 200 rows).
  * The first call made on a device looks up the array's device address on that
  * device (make it with the device current, before any stream capture).  Each
  * call zeroes the counters it needs with cudaMemsetAsync on `stream`.  All
@@ -116,7 +116,7 @@ ddtree_status ddtree_topk_noalloc(const void* draft_logits, int dtype, int rows,
                                   int64_t row_stride, int K, int32_t* topk_idx,
                                   float* topk_logp, float* lse, void* stream);
 
-/* Step 2 -- best-first heap tree build (Algorithm 1).
+/* Step 2 -- the tree of the N most probable prefixes (Algorithm 1's result).
  * Pages: §4.1 (the bonus token is the root), §4.2 (the best valid tree under
  * the surrogate is the set of the N most probable prefixes), §4.3 / App. A
  * (pop N times; after each pop offer the prefix's next sibling and best child).
@@ -133,12 +133,29 @@ ddtree_status ddtree_topk_noalloc(const void* draft_logits, int dtype, int rows,
  *            a is u itself or an ancestor of u (the ancestor-only mask)
  *   n_nodes int32 [B]
  * pos_id = prefix_len + depth.  Rows past n: ints -1, child_count 0,
- * score -inf, mask 0.  No workspace. */
+ * score -inf, mask 0.  No workspace.
+ * This call builds the tree level by level (depth 1, 2, ...: the top N of all
+ * prefixes up to depth d are the top N of those up to depth d-1 plus the
+ * children of their depth-(d-1) nodes), one CTA per sequence, in L parallel
+ * steps; ddtree_build_heap below runs the heap itself.  Both return the same
+ * arrays bit for bit. */
 ddtree_status ddtree_build(const float* topk_logp, const int32_t* topk_idx, const int32_t* bonus,
                            const int32_t* prefix_len, int B, int L, int K, int N,
                            int32_t* parent, int32_t* depth, int32_t* rank, int32_t* token,
                            int32_t* pos_id, float* score, int32_t* child_count,
                            uint32_t* anc_mask, int32_t* n_nodes, void* stream);
+
+/* Algorithm 1 as the pages state it: a best-first heap (§4.3, App. A) that pops
+ * N times, after each pop offering the popped prefix's next sibling and best
+ * child; one warp per sequence keeps the frontier in registers.  Same
+ * arguments, outputs and results as ddtree_build; its N pops are sequential,
+ * so it is slower for large N. */
+ddtree_status ddtree_build_heap(const float* topk_logp, const int32_t* topk_idx,
+                                const int32_t* bonus, const int32_t* prefix_len, int B, int L,
+                                int K, int N, int32_t* parent, int32_t* depth, int32_t* rank,
+                                int32_t* token, int32_t* pos_id, float* score,
+                                int32_t* child_count, uint32_t* anc_mask, int32_t* n_nodes,
+                                void* stream);
 
 /* Step 3 -- tree attention of one target layer.
  * Pages: §4.1 and the abstract (all drafted nodes are verified in one target

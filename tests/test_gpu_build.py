@@ -13,10 +13,10 @@ pytestmark = pytest.mark.gpu
 KEYS = ("parent", "depth", "rank", "token", "pos_id", "child_count", "n_nodes")
 
 
-def _check(lp32, tok, bonus, plen, N, dev):
+def _check(lp32, tok, bonus, plen, N, dev, heap):
     ref = oracle.build_tree(lp32, tok, bonus, plen, N)
     got = ops.build(dev_f32(lp32, dev), dev_i32(tok, dev), dev_i32(bonus, dev),
-                    dev_i32(plen, dev), N)
+                    dev_i32(plen, dev), N, heap=heap)
     for k in KEYS:
         np.testing.assert_array_equal(host(got[k]), ref[k], err_msg=k)
     np.testing.assert_array_equal(host(got["score"]).view(np.uint32),
@@ -29,10 +29,11 @@ def _check(lp32, tok, bonus, plen, N, dev):
 @pytest.mark.parametrize("name", ["tiny", "8b_single", "budget_sweep_n32", "budget_sweep_n128",
                                   "budget_sweep_n256", "budget_sweep_n512", "ragged_serving",
                                   "long_context_70b"])
-def test_build_workloads(cuda_device, name):
+@pytest.mark.parametrize("heap", [False, True], ids=["level", "heap"])
+def test_build_workloads(cuda_device, name, heap):
     w = wl.CONFIGS[name]
     idx, _, lp32, _ = oracle.topk(wl.draft_logits(w), w.dtype, w.K)
-    ref = _check(lp32, idx, wl.bonus_tokens(w), wl.prefix_lengths(w), w.N, cuda_device)
+    ref = _check(lp32, idx, wl.bonus_tokens(w), wl.prefix_lengths(w), w.N, cuda_device, heap)
     assert np.all(ref["n_nodes"] == w.N)
 
 
@@ -53,9 +54,10 @@ def _table(rng, B, L, K, ties):
     (4, 1, 7, 7, True),        # one position
     (1, 16, 16, 543, True), (1, 16, 16, 544, True), (1, 9, 5, 95, False), (1, 9, 5, 96, False),
     (5, 16, 8, 63, True), (5, 16, 8, 64, False)])
-def test_build_edge_cases(cuda_device, B, L, K, N, ties):
+@pytest.mark.parametrize("heap", [False, True], ids=["level", "heap"])
+def test_build_edge_cases(cuda_device, B, L, K, N, ties, heap):
     rng = np.random.default_rng(B * 1000 + L * 100 + K * 10 + N)
     lp, tok = _table(rng, B, L, K, ties)
     bonus = rng.integers(0, 1000, size=B).astype(np.int32)
     plen = rng.integers(0, 5000, size=B).astype(np.int32)
-    _check(lp, tok, bonus, plen, N, cuda_device)
+    _check(lp, tok, bonus, plen, N, cuda_device, heap)
