@@ -9,10 +9,12 @@
 //   T = 0: each CTA finds its chunk's (max, lowest index);
 //   T > 0: each CTA finds its chunk's max m_c and s_c = sum 2^((x - m_c) c),
 //          c = log2(e) / T.
-// The last CTA of a row (atomic ticket, no spinning) resolves the row's token:
-// the argmax over chunks, or the inverse-CDF sample -- it locates the chunk in
-// which the running sum crosses U * Z and rescans only that chunk (from L2).
-// The last row of a sequence to resolve runs the walk.
+// Greedy: each CTA folds its (value, lowest index) key into the row's 64-bit
+// slot with one atomicMax, and the last CTA of the sequence (atomic ticket over
+// all its rows and chunks, no spinning) walks the tree.  Sampling: the last
+// CTA of a row resolves its inverse-CDF sample -- it locates the chunk in which
+// the running sum crosses U * Z and rescans only that chunk (from L2) -- and
+// the last row of a sequence to resolve runs the walk.
 #include "chunk.cuh"
 #include "internal.h"
 
@@ -27,10 +29,11 @@ constexpr int kChunkBytes = 16384;
 constexpr int kMaxChunks = 128;
 
 struct AcceptWs {
-    unsigned int* row_tickets;  // [B][N+1]
-    unsigned int* seq_tickets;  // [B]
-    float2* parts;              // [B][N+1][nchunks]: (max, idx-as-bits) or (m_c, s_c)
-    int32_t* tok;               // [B][N+1] resolved target tokens
+    unsigned int* row_tickets;    // [B][N+1] (sampling)
+    unsigned int* seq_tickets;    // [B]
+    float2* parts;                // [B][N+1][nchunks]: (m_c, s_c) (sampling)
+    int32_t* tok;                 // [B][N+1] sampled target tokens
+    unsigned long long* row_best; // [B][N+1] greedy: max (value, lowest index) key
 };
 
 // Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two 64x64
@@ -99,17 +102,22 @@ accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nc
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int chunk = blockIdx.x, u = blockIdx.y, b = blockIdx.z;
     const int R = N + 1;
+    const size_t row = (size_t)b * R + u;
+    const char* rowp = (const char*)logits + row * (size_t)row_stride * Chunk::ES;
+    const int c0 = chunk * Chunk::SIZE;
+    pdl_trigger();
+    pdl_wait();
+    // Start the row's bulk copy before the tree size arrives; rows past the
+    // tree wait for their copy and leave.
+    Chunk::issue(s_buf, &s_bar, rowp, c0, V, aligned);
     const int n = n_nodes[b];
+    const bool ok = Chunk::wait(&s_bar);
     if (n < 0 || n > N) {
         if (tid == 0 && chunk == 0 && u == 0) record_error(err, ERR_ACCEPT | ERR_BAD_N_NODES);
         return;
     }
     if (u > n) return;
-
-    const size_t row = (size_t)b * R + u;
-    const char* rowp = (const char*)logits + row * (size_t)row_stride * Chunk::ES;
-    const int c0 = chunk * Chunk::SIZE;
-    if (!Chunk::load(s_buf, &s_bar, rowp, c0, V, aligned)) {
+    if (!ok) {
         if (tid == 0) record_error(err, ERR_ACCEPT | ERR_WAIT_TIMEOUT);
         return;
     }
@@ -172,9 +180,28 @@ accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nc
         for (int i = 0; i < kThreads / 32; ++i) csum += s_red[kThreads / 32 + i];
     }
 
+    __shared__ int s_tok[DDTREE_MAX_N + 1];
+    if (!sample) {
+        // greedy: one 64-bit atomicMax per CTA resolves the row; the last CTA of
+        // the whole sequence (all rows, all chunks) walks the tree.
+        if (tid == 0) {
+            if (cidx >= 0) atomicMax(&ws.row_best[row], value_index_key(cmax, (uint32_t)cidx));
+            s_flag = ticket_is_last(&ws.seq_tickets[b], (unsigned)((n + 1) * nchunks));
+        }
+        __syncthreads();
+        if (!s_flag) return;
+        for (int i = tid; i <= n; i += kThreads) {
+            unsigned long long* rb = &ws.row_best[(size_t)b * R + i];
+            const unsigned long long k = __ldcg(rb);
+            s_tok[i] = (int)key_index(k);
+            *rb = 0ull;  // ready for the next call
+            if (target_token) target_token[(size_t)b * R + i] = (int)key_index(k);
+        }
+        __syncthreads();
+    } else {
     float2* rparts = ws.parts + row * nchunks;
     if (tid == 0) {
-        rparts[chunk] = sample ? make_float2(cmax, csum) : make_float2(cmax, __int_as_float(cidx));
+        rparts[chunk] = make_float2(cmax, csum);
         s_flag = ticket_is_last(&ws.row_tickets[row], (unsigned)nchunks);
     }
     __syncthreads();
@@ -185,19 +212,7 @@ accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nc
     for (int c = tid; c < nchunks; c += kThreads) s_part[c] = __ldcg(&rparts[c]);
     __syncthreads();
     int pick = -1;
-    if (!sample) {
-        if (tid == 0) {
-            float bv = 0.f;
-            for (int c = 0; c < nchunks; ++c) {
-                const float2 p = s_part[c];
-                const int pi = __float_as_int(p.y);
-                if (pi >= 0 && (pick < 0 || p.x > bv)) { bv = p.x; pick = pi; }
-            }
-            s_pick = pick;
-        }
-        __syncthreads();
-        pick = s_pick;
-    } else {
+    {
         // Z = sum_c s_c 2^((m_c - M) c); target = U * Z; find the crossing chunk.
         __shared__ int s_cstar;
         __shared__ float s_tloc;
@@ -281,6 +296,9 @@ accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nc
     }
     __syncthreads();
     if (!s_flag) return;
+    for (int i = tid; i <= n; i += kThreads) s_tok[i] = __ldcg(&ws.tok[(size_t)b * R + i]);
+    __syncthreads();
+    }  // sampling
 
     // ---- last row of the sequence: the walk ---------------------------------------
     // chosen[p] = the child c of p whose token equals the target's token at p.
@@ -289,14 +307,13 @@ accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nc
     __syncthreads();
     const int32_t* par = parent + (size_t)b * R;
     const int32_t* tk = token + (size_t)b * R;
-    const int32_t* tt = ws.tok + (size_t)b * R;
     for (int c = 1 + tid; c <= n; c += kThreads) {
         const int p = par[c];
         if (p < 0 || p >= c) {
             record_error(err, ERR_ACCEPT | ERR_BAD_TREE);
             continue;
         }
-        if (tk[c] == __ldcg(&tt[p])) s_chosen[p] = c;  // children have distinct tokens
+        if (tk[c] == s_tok[p]) s_chosen[p] = c;  // children have distinct tokens
     }
     __syncthreads();
     if (tid == 0) {
@@ -310,7 +327,7 @@ accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nc
             ++len;
         }
         for (int i = len; i < L; ++i) acc[i] = -1;
-        const int bonus = __ldcg(&tt[cur]);
+        const int bonus = s_tok[cur];
         ot[len] = bonus;
         for (int i = len + 1; i <= L; ++i) ot[i] = -1;
         accept_len[b] = len;
@@ -322,7 +339,7 @@ accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nc
 }
 
 struct WsLayout {
-    size_t row_tickets, seq_tickets, parts, tok, total;
+    size_t row_tickets, seq_tickets, parts, tok, row_best, total;
 };
 
 WsLayout accept_layout(int B, int N, int nch) {
@@ -332,7 +349,8 @@ WsLayout accept_layout(int B, int N, int nch) {
     l.seq_tickets = align_up(l.row_tickets + (size_t)B * R * 4, 256);
     l.parts = align_up(l.seq_tickets + (size_t)B * 4, 256);
     l.tok = align_up(l.parts + (size_t)B * R * nch * sizeof(float2), 256);
-    l.total = align_up(l.tok + (size_t)B * R * 4, 256);
+    l.row_best = align_up(l.tok + (size_t)B * R * 4, 256);
+    l.total = align_up(l.row_best + (size_t)B * R * 8, 256);
     return l;
 }
 
@@ -361,22 +379,17 @@ cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s) {
     const WsLayout l = accept_layout(a.B, a.N, nch);
     char* base = (char*)a.ws;
     AcceptWs ws{(unsigned int*)(base + l.row_tickets), (unsigned int*)(base + l.seq_tickets),
-                (float2*)(base + l.parts), (int32_t*)(base + l.tok)};
+                (float2*)(base + l.parts), (int32_t*)(base + l.tok),
+                (unsigned long long*)(base + l.row_best)};
     const int es = a.dtype == DDTREE_BF16 ? 2 : 4;
     const bool aligned = ((uintptr_t)a.logits % 16 == 0) && ((a.row_stride * es) % 16 == 0);
     const float c_exp = a.temperature > 0.f ? kLog2e / a.temperature : 0.f;
     dim3 grid(nch, a.N + 1, a.B);
-    if (a.dtype == DDTREE_BF16)
-        accept_kernel<true><<<grid, kThreads, 0, s>>>(
-            a.logits, a.V, a.row_stride, nch, aligned, a.parent, a.token, a.n_nodes, a.L, a.N,
-            a.temperature, c_exp, a.seed, a.step, a.target_token, a.accept_len, a.accepted_nodes,
-            a.out_tokens, a.next_bonus, ws, a.err);
-    else
-        accept_kernel<false><<<grid, kThreads, 0, s>>>(
-            a.logits, a.V, a.row_stride, nch, aligned, a.parent, a.token, a.n_nodes, a.L, a.N,
-            a.temperature, c_exp, a.seed, a.step, a.target_token, a.accept_len, a.accepted_nodes,
-            a.out_tokens, a.next_bonus, ws, a.err);
-    return cudaGetLastError();
+    auto kern = (a.dtype == DDTREE_BF16) ? accept_kernel<true> : accept_kernel<false>;
+    return launch_pdl(kern, grid, dim3(kThreads), 0, s, a.logits, a.V, a.row_stride, nch, aligned,
+                      a.parent, a.token, a.n_nodes, a.L, a.N, a.temperature, c_exp, a.seed,
+                      a.step, a.target_token, a.accept_len, a.accepted_nodes, a.out_tokens,
+                      a.next_bonus, ws, a.err);
 }
 
 }  // namespace ddt

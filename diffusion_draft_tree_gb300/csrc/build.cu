@@ -51,6 +51,8 @@ build_kernel(const float* __restrict__ topk_logp, const int32_t* __restrict__ to
 
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
     const int LK = L * K;
+    pdl_trigger();
+    pdl_wait();
     for (int i = tid; i < LK; i += kThreads) {
         s_lp[i] = topk_logp[(size_t)b * LK + i];
         s_tok[i] = topk_idx[(size_t)b * LK + i];
@@ -154,11 +156,9 @@ build_kernel(const float* __restrict__ topk_logp, const int32_t* __restrict__ to
 
 template <int S>
 cudaError_t launch_s(const BuildArgs& a, cudaStream_t s) {
-    build_kernel<S><<<a.B, kThreads, 0, s>>>(a.topk_logp, a.topk_idx, a.bonus, a.prefix_len, a.L,
-                                             a.K, a.N, a.parent, a.depth, a.rank, a.token,
-                                             a.pos_id, a.score, a.child_count, a.anc_mask,
-                                             a.n_nodes, a.err);
-    return cudaGetLastError();
+    return launch_pdl(build_kernel<S>, dim3(a.B), dim3(kThreads), 0, s, a.topk_logp, a.topk_idx,
+                      a.bonus, a.prefix_len, a.L, a.K, a.N, a.parent, a.depth, a.rank, a.token,
+                      a.pos_id, a.score, a.child_count, a.anc_mask, a.n_nodes, a.err);
 }
 
 }  // namespace

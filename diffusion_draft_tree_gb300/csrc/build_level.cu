@@ -15,8 +15,8 @@
 // has its parent in it, and that parent is among the top N of depth <= d-1).
 // When T_{d-1} is full, a child must beat its last element: a strictly higher
 // score, because the child is deeper.  Children of one parent are generated in
-// rank order, sorted (bitonic, shared memory) and merged into T with a
-// rank-by-binary-search merge.  The result -- nodes, their order, fp32 scores
+// rank order, sorted (rank counting for small batches, bitonic otherwise, in
+// shared memory) and merged into T with a rank-by-binary-search merge.  The result -- nodes, their order, fp32 scores
 // formed as parent score + log-prob -- is identical to the heap's.
 //
 // One CTA of 512 threads per sequence.  T holds 64-bit keys:
@@ -37,6 +37,7 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kCandCap = 2048;  // children merged per batch
 constexpr int kPairsPerThread = kCandCap / kThreads;
+constexpr int kRankCountMax = 256;  // batches up to this size are ranked by counting
 
 DDT_DEV uint64_t lkey(float score, int depth, int ppos, int rank) {
     return ((uint64_t)ord_from_float(score) << 32) | ((uint32_t)(31 - depth) << 27) |
@@ -104,6 +105,8 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
 
     const int b = blockIdx.x, tid = threadIdx.x;
     const int LK = L * K;
+    pdl_trigger();
+    pdl_wait();
     for (int i = tid; i < LK; i += kThreads) s_lp[i] = topk_logp[(size_t)b * LK + i];
     __syncthreads();
 
@@ -172,25 +175,41 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
                 __syncthreads();
                 continue;
             }
-            // bitonic sort, descending; pad to a power of two with zeros
-            int p2 = 1;
-            while (p2 < c) p2 <<= 1;
-            for (int i = c + tid; i < p2; i += kThreads) s_cand[i] = 0ull;
-            __syncthreads();
-            for (int k2 = 2; k2 <= p2; k2 <<= 1) {
-                for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
-                    for (int i = tid; i < p2; i += kThreads) {
-                        const int ix = i ^ j2;
-                        if (ix > i) {
-                            const uint64_t a = s_cand[i], e = s_cand[ix];
-                            const bool desc = (i & k2) == 0;
-                            if (desc ? (a < e) : (a > e)) {
-                                s_cand[i] = e;
-                                s_cand[ix] = a;
+            // Sort the batch, descending.  Small batches: each key's rank is
+            // counted by its own thread and the key is scattered to that rank in
+            // the upper half of the buffer (one barrier).  Large batches: an
+            // in-place bitonic sort padded to a power of two.
+            const uint64_t* sorted = s_cand;
+            if (c <= kRankCountMax) {
+                __syncthreads();  // the batch's keys are in place
+                for (int i = tid; i < c; i += kThreads) {
+                    const uint64_t k = s_cand[i];
+                    int r = 0;
+                    for (int j = 0; j < c; ++j) r += (s_cand[j] > k) ? 1 : 0;
+                    s_cand[kCandCap / 2 + r] = k;
+                }
+                sorted = s_cand + kCandCap / 2;
+                __syncthreads();
+            } else {
+                int p2 = 1;
+                while (p2 < c) p2 <<= 1;
+                for (int i = c + tid; i < p2; i += kThreads) s_cand[i] = 0ull;
+                __syncthreads();
+                for (int k2 = 2; k2 <= p2; k2 <<= 1) {
+                    for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
+                        for (int i = tid; i < p2; i += kThreads) {
+                            const int ix = i ^ j2;
+                            if (ix > i) {
+                                const uint64_t a = s_cand[i], e = s_cand[ix];
+                                const bool desc = (i & k2) == 0;
+                                if (desc ? (a < e) : (a > e)) {
+                                    s_cand[i] = e;
+                                    s_cand[ix] = a;
+                                }
                             }
                         }
+                        __syncthreads();
                     }
-                    __syncthreads();
                 }
             }
             // merge T[0..t) and cand[0..c) by output rank; keep the first N
@@ -198,14 +217,14 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
             for (int i = tid; i < t + c; i += kThreads) {
                 if (i < t) {
                     const uint64_t a = s_T[cur][i];
-                    const int rk = i + count_greater(s_cand, c, a);
+                    const int rk = i + count_greater(sorted, c, a);
                     if (rk < N) {
                         s_T[nxt][rk] = a;
                         s_orig[nxt][rk] = s_orig[cur][i];
                     }
                 } else {
                     const int j = i - t;
-                    const uint64_t e = s_cand[j];
+                    const uint64_t e = sorted[j];
                     const int rk = j + count_greater(s_T[cur], t, e);
                     if (rk < N) {
                         s_T[nxt][rk] = e;
@@ -284,11 +303,9 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
 }  // namespace
 
 cudaError_t launch_build_level(const BuildArgs& a, cudaStream_t s) {
-    build_level_kernel<<<a.B, kThreads, 0, s>>>(a.topk_logp, a.topk_idx, a.bonus, a.prefix_len,
-                                                a.L, a.K, a.N, a.parent, a.depth, a.rank,
-                                                a.token, a.pos_id, a.score, a.child_count,
-                                                a.anc_mask, a.n_nodes);
-    return cudaGetLastError();
+    return launch_pdl(build_level_kernel, dim3(a.B), dim3(kThreads), 0, s, a.topk_logp, a.topk_idx,
+                      a.bonus, a.prefix_len, a.L, a.K, a.N, a.parent, a.depth, a.rank, a.token,
+                      a.pos_id, a.score, a.child_count, a.anc_mask, a.n_nodes);
 }
 
 }  // namespace ddt

@@ -23,16 +23,14 @@ struct SmemChunk {
     static constexpr int BYTES = SIZE * ES;
     static_assert(NVEC % THREADS == 0, "whole vectors per thread");
 
-    // Stages elements [c0, c0 + SIZE) of the row at `rowp` into `buf`
-    // (16-byte aligned, BYTES long).  All threads call it; returns once the
-    // data is visible to every thread (false if the copy never completed).
-    DDT_DEV static bool load(uint8_t* buf, uint64_t* bar, const char* rowp, int c0, int V,
-                             bool aligned) {
-        __shared__ int s_no_abort;
+    // Starts staging elements [c0, c0 + SIZE) of the row at `rowp` into `buf`
+    // (16-byte aligned, BYTES long).  All threads call it; the data may be used
+    // only after wait().  A CTA that issues must wait before it exits.
+    DDT_DEV static void issue(uint8_t* buf, uint64_t* bar, const char* rowp, int c0, int V,
+                              bool aligned) {
         const int n_in = max(0, min(SIZE, V - c0));             // elements of the row
         const int n_bulk = aligned ? (n_in / VEC) * VEC : 0;    // by the copy engine
         if (threadIdx.x == 0) {
-            s_no_abort = 0;
             sm100::mbar_init(bar, 1);
             sm100::mbar_init_fence();
         }
@@ -61,8 +59,19 @@ struct SmemChunk {
                 ((unsigned int*)buf)[i] = v;
             }
         }
-        const bool ok = sm100::mbar_wait(bar, 0, (volatile int*)&s_no_abort);
-        return __syncthreads_and(ok) != 0;  // uniform across the CTA
+    }
+
+    // Waits (bounded) for the staged chunk; returns, uniformly across the CTA,
+    // whether it arrived.  Every thread sees the whole chunk afterwards.
+    DDT_DEV static bool wait(uint64_t* bar) {
+        const bool ok = sm100::mbar_wait(bar, 0, nullptr);
+        return __syncthreads_and(ok) != 0;
+    }
+
+    DDT_DEV static bool load(uint8_t* buf, uint64_t* bar, const char* rowp, int c0, int V,
+                             bool aligned) {
+        issue(buf, bar, rowp, c0, V, aligned);
+        return wait(bar);
     }
 
     // Vector v of the chunk as 8 (bf16) or 4 (fp32) floats.

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #define DDT_DEV __device__ __forceinline__
 
 namespace ddt {
@@ -123,6 +125,33 @@ DDT_DEV bool ticket_is_last(unsigned int* counter, unsigned int expected) {
         *counter = 0u;
     }
     return last;
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Kernels are launched so that they may start
+// while the previous kernel on the stream is finishing: each one first lets its
+// own successor start (pdl_trigger) and then waits (pdl_wait) until every
+// earlier kernel on the stream has completed and its writes are visible, before
+// it reads or writes any global memory.  What overlaps is launch latency and
+// CTA start-up, never data.
+// ---------------------------------------------------------------------------
+DDT_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+DDT_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace ddt

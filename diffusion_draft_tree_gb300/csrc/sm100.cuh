@@ -51,14 +51,15 @@ DDT_DEV uint64_t globaltimer_ns() {
     return t;
 }
 // Waits for the phase with the given parity to complete.  Gives up after
-// `limit_ns` of wall time, or at once when *abort is set; returns false then.
+// `limit_ns` of wall time, or at once when *abort is set (abort may be null);
+// returns false then.
 DDT_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                        uint64_t limit_ns = 2000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*abort) return false;
+        if (abort && *abort) return false;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }

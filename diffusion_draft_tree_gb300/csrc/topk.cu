@@ -88,6 +88,8 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     const char* rowp = (const char*)logits + (size_t)row * (size_t)row_stride * Chunk::ES;
     if (tid == 0) s_cnt = 0;
     if (tid < K) s_sel[tid] = 0ull;
+    pdl_trigger();
+    pdl_wait();
     if (!Chunk::load(s_buf, &s_bar, rowp, c0, V, aligned)) return;  // copy never landed
     const uint4* vec = reinterpret_cast<const uint4*>(s_buf);
 
@@ -263,15 +265,9 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
         parts = (TopkPartial*)((char*)a.ws + align_up((size_t)a.rows * sizeof(unsigned int), 256));
     }
     dim3 grid(nch, a.rows);
-    if (a.dtype == DDTREE_BF16)
-        topk_kernel<true><<<grid, kThreads, 0, s>>>(a.logits, a.V, a.row_stride, a.K, nch, aligned,
-                                                     a.topk_idx, a.topk_logp, a.lse, parts,
-                                                     tickets);
-    else
-        topk_kernel<false><<<grid, kThreads, 0, s>>>(a.logits, a.V, a.row_stride, a.K, nch,
-                                                      aligned, a.topk_idx, a.topk_logp, a.lse,
-                                                      parts, tickets);
-    return cudaGetLastError();
+    auto kern = (a.dtype == DDTREE_BF16) ? topk_kernel<true> : topk_kernel<false>;
+    return launch_pdl(kern, grid, dim3(kThreads), 0, s, a.logits, a.V, a.row_stride, a.K, nch,
+                      aligned, a.topk_idx, a.topk_logp, a.lse, parts, tickets);
 }
 
 }  // namespace ddt

@@ -112,6 +112,8 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int b = idx / p.Hkv;
     const int unit = (b * p.Hkv + g) * p.mtiles + mtile;
     const int R = p.N + 1, G = p.G;
+    pdl_trigger();
+    pdl_wait();
     const int P = p.prefix_len[b];
     const int n = p.n_nodes[b];
     if (P < 0 || P > p.cache_cap || n < 0 || n > p.N) {
@@ -570,8 +572,8 @@ cudaError_t launch_d(const AttnArgs& a, const Plan& pl, const WsLayout& wl, cuda
     p.scale_log2 = a.scale * kLog2e;
     p.err = a.err;
     const long grid = (long)a.B * a.Hkv * pl.mtiles * pl.smax;
-    tree_attn_kernel<D><<<(unsigned)grid, kThreads, Cfg<D>::SMEM, s>>>(mq, mkc, mvc, mkt, mvt, p);
-    return cudaGetLastError();
+    return launch_pdl(tree_attn_kernel<D>, dim3((unsigned)grid), dim3(kThreads),
+                      (size_t)Cfg<D>::SMEM, s, mq, mkc, mvc, mkt, mvt, p);
 }
 
 }  // namespace
