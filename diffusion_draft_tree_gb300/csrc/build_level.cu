@@ -19,7 +19,7 @@
 // shared memory) and merged into T with a rank-by-binary-search merge.  The result -- nodes, their order, fp32 scores
 // formed as parent score + log-prob -- is identical to the heap's.
 //
-// One CTA of 512 threads per sequence.  T holds 64-bit keys:
+// One CTA per sequence (128 threads for budgets up to 128, else 512).  T holds 64-bit keys:
 //   [63:32] orderable fp32 score, [31:27] 31 - depth,
 //   [26:16] 2046 - parent position (2047 for the root), [15:10] 63 - rank.
 // Parent positions refer to T_{d-1} while level d is built and are remapped to
@@ -34,9 +34,7 @@ namespace ddt {
 
 namespace {
 
-constexpr int kThreads = 512;
 constexpr int kCandCap = 2048;  // children merged per batch
-constexpr int kPairsPerThread = kCandCap / kThreads;
 constexpr int kRankCountMax = 256;  // batches up to this size are ranked by counting
 
 DDT_DEV uint64_t lkey(float score, int depth, int ppos, int rank) {
@@ -52,6 +50,7 @@ DDT_DEV uint64_t lk_with_ppos(uint64_t k, int ppos) {
 }
 
 // Exclusive scan of one int per thread over the CTA; *total gets the sum.
+template <int kThreads>
 DDT_DEV int block_scan(int v, int* s_warp, int* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = v;
@@ -85,6 +84,7 @@ DDT_DEV int count_greater(const uint64_t* a, int n, uint64_t x) {
     return lo;
 }
 
+template <int kThreads>
 __global__ void __launch_bounds__(kThreads)
 build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restrict__ topk_idx,
                    const int32_t* __restrict__ bonus, const int32_t* __restrict__ prefix_len,
@@ -102,6 +102,8 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
     __shared__ float s_lp[DDTREE_MAX_L * DDTREE_MAX_K];
     __shared__ int s_warp[kThreads / 32];
     __shared__ int s_flag;
+    constexpr int kPairsPerThread = kCandCap / kThreads;
+    constexpr int kPosPerThread = DDTREE_MAX_N / kThreads;
 
     const int b = blockIdx.x, tid = threadIdx.x;
     const int LK = L * K;
@@ -122,19 +124,21 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
             }
             __syncthreads();
         } else {
-            int f[2] = {0, 0};
+            int f[kPosPerThread];
+            int fs = 0;
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int i = tid * 2 + j;
+            for (int j = 0; j < kPosPerThread; ++j) {
+                const int i = tid * kPosPerThread + j;
                 f[j] = (i < t && lk_depth(s_T[cur][i]) == d - 1) ? 1 : 0;
+                fs += f[j];
             }
             int tot;
-            int pos = block_scan(f[0] + f[1], s_warp, &tot);
+            int pos = block_scan<kThreads>(fs, s_warp, &tot);
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
+            for (int j = 0; j < kPosPerThread; ++j) {
                 if (f[j]) {
-                    s_plist[pos] = (int16_t)(tid * 2 + j);
-                    s_pscore[pos] = lk_score(s_T[cur][tid * 2 + j]);
+                    s_plist[pos] = (int16_t)(tid * kPosPerThread + j);
+                    s_pscore[pos] = lk_score(s_T[cur][tid * kPosPerThread + j]);
                     ++pos;
                 }
             }
@@ -167,7 +171,7 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
                 }
             }
             int c;
-            int pos = block_scan(cnt, s_warp, &c);
+            int pos = block_scan<kThreads>(cnt, s_warp, &c);
 #pragma unroll
             for (int j = 0; j < kPairsPerThread; ++j)
                 if (key[j]) s_cand[pos++] = key[j];
@@ -303,7 +307,13 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
 }  // namespace
 
 cudaError_t launch_build_level(const BuildArgs& a, cudaStream_t s) {
-    return launch_pdl(build_level_kernel, dim3(a.B), dim3(kThreads), 0, s, a.topk_logp, a.topk_idx,
+    // small budgets: fewer threads make each of the level's barriers cheaper
+    if (a.N <= 128)
+        return launch_pdl(build_level_kernel<128>, dim3(a.B), dim3(128), 0, s, a.topk_logp,
+                          a.topk_idx, a.bonus, a.prefix_len, a.L, a.K, a.N, a.parent, a.depth,
+                          a.rank, a.token, a.pos_id, a.score, a.child_count, a.anc_mask,
+                          a.n_nodes);
+    return launch_pdl(build_level_kernel<512>, dim3(a.B), dim3(512), 0, s, a.topk_logp, a.topk_idx,
                       a.bonus, a.prefix_len, a.L, a.K, a.N, a.parent, a.depth, a.rank, a.token,
                       a.pos_id, a.score, a.child_count, a.anc_mask, a.n_nodes);
 }

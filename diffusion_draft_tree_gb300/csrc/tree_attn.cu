@@ -4,22 +4,24 @@
 // with an ancestor-only attention mask; App. B: the pages' runs used a dense
 // masked attention because FlashAttention-2 cannot express the pattern).
 //
-// Work unit = (sequence b, KV head g, M tile, KV split).  An M tile holds 128
-// query rows: 128/G tree nodes x the G query heads that share KV head g, so the
-// GQA group turns the tree's (N+1) rows into a real dense contraction.  The
-// unit streams its KV range in 128-key tiles: prefix tiles from the cache, then
-// (last split only) the tree tiles, where the ancestor bitmask is applied.
+// Work unit = (sequence b, KV head g, pair of query tiles, KV split).  A query
+// tile holds 128 rows: 128/G tree nodes x the G query heads that share KV head
+// g, so the GQA group turns the tree's (N+1) rows into a real dense
+// contraction.  The unit streams its KV range in 128-key tiles: prefix tiles
+// from the cache, then (last split only) the tree tiles, where the ancestor
+// bitmask is applied.
 //
-// Per CTA: warp 0 issues TMA loads (K and V tiles, 128-byte swizzled) into a
-// 2-3 stage ring; warp 1 owns TMEM and issues tcgen05.mma: S = Q K^T into one
-// of two TMEM S buffers while the softmax warps read the other, then O += P V
-// into a TMEM accumulator; warps 2-5 (one thread per query row) run the online
-// softmax in the log2 domain (row max with lazy rescaling: O is rescaled only
-// when the max grows by more than 2^8), write P as bf16 into shared memory in
-// the swizzled K-major layout the MMA reads, and finally normalise O.  When a
-// unit's prefix is split, each split writes (O, m, l) partials and the last
-// split's CTA (atomic ticket) merges them.  Every mbarrier wait is bounded in
-// wall time; a timeout records an error and the CTA unwinds.
+// Per CTA: warp 0 issues TMA loads (Q tiles, K and V tiles, 128-byte swizzled)
+// into a 2-3 stage K/V ring; warp 1 owns TMEM and issues tcgen05.mma; two
+// groups of four warps (one thread per query row) run the online softmax of
+// the two query tiles in the log2 domain, with lazy rescaling (O is rescaled
+// only when the row max grows by more than 2^8).  P goes back into TMEM as
+// bf16 over the S columns it came from and feeds the P V product directly, so
+// shared memory holds only Q, K and V.  The two groups alternate on the tensor
+// core: while one exponentiates, the other's products run.  When a unit's
+// prefix is split, each split writes (O, m, l) partials and the last split's
+// CTA (atomic ticket) merges them.  Every mbarrier wait is bounded in wall
+// time; a timeout records an error and the CTA unwinds.
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -37,7 +39,7 @@ using namespace sm100;
 
 constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per KV tile
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
 constexpr int kHalfBytes = 128 * 128;  // [128 rows][64 bf16], one 128B-swizzled slab
 constexpr float kRescaleLog2 = 8.f;
 constexpr uint32_t kTmemCols = 512;
@@ -45,11 +47,10 @@ constexpr uint32_t kTmemCols = 512;
 template <int D>
 struct Cfg {
     static constexpr int NH = D / 64;
-    static constexpr int Q_BYTES = NH * kHalfBytes;
+    static constexpr int QT_BYTES = NH * kHalfBytes;  // one 128-row query tile
     static constexpr int KV_BYTES = NH * kHalfBytes;  // one K (or V) tile
-    static constexpr int P_BYTES = 2 * kHalfBytes;
     static constexpr int NS = (D == 128) ? 2 : 3;
-    static constexpr int SMEM = 1024 + Q_BYTES + NS * 2 * KV_BYTES + P_BYTES;
+    static constexpr int SMEM = 1024 + 2 * QT_BYTES + NS * 2 * KV_BYTES;
 };
 
 struct Params {
@@ -58,10 +59,10 @@ struct Params {
     const uint32_t* anc_mask;
     uint16_t* out;
     float* lse;
-    float* part_o;   // [unit][smax][D][128]
-    float* part_ml;  // [unit][smax][2][128]
-    unsigned int* tickets;
-    int B, N, Hq, Hkv, G, W, mtiles, tps, smax;
+    float* part_o;   // [B*Hkv*mtiles][smax][D][128]
+    float* part_ml;  // [B*Hkv*mtiles][smax][2][128]
+    unsigned int* tickets;  // [B*Hkv*mpairs]
+    int B, N, Hq, Hkv, G, W, mtiles, mpairs, tps, smax;
     int64_t cache_cap;
     float scale_log2;
     uint32_t* err;
@@ -72,21 +73,28 @@ DDT_DEV uint32_t pack_bf16x2(float lo, float hi) {
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
-DDT_DEV void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-// Named barrier over the 128 softmax threads that also ANDs a flag.
+// Named barrier over the 256 softmax threads (both query tiles).
+DDT_DEV void softmax_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 DDT_DEV bool softmax_bar_and(bool v) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        "bar.red.and.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
         : "r"((uint32_t)v)
         : "memory");
     return r != 0;
 }
 
+// One CTA = one (sequence b, KV head g, pair of 128-row query tiles, KV split).
+// Warp 0: TMA producer.  Warp 1: TMEM owner and MMA issuer.  Warps 2-5: softmax
+// of query tile 0; warps 6-9: softmax of query tile 1.  Per KV tile j the
+// tensor core runs S_k = Q_k K_j^T into TMEM columns [128k, 128k+128); softmax
+// group k reads S_k, writes P_k (bf16) over the first 64 of those columns, and
+// the tensor core runs O_k += P_k V_j with P_k read straight from TMEM.  While
+// one group exponentiates, the tensor core works on the other group's tile.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(200)
 tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
                  const __grid_constant__ CUtensorMap tm_vc,
                  const __grid_constant__ CUtensorMap tm_kt,
@@ -95,7 +103,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     constexpr int NS = C::NS;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_q, bar_full[NS], bar_empty[NS], bar_sfull[2],
-        bar_sfree[2], bar_pfull, bar_odone;
+        bar_pfull[2], bar_odone[2];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
     __shared__ bool s_last;
@@ -104,33 +112,35 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     // ---- decode the unit --------------------------------------------------------
     int idx = blockIdx.x;
-    const int mtile = idx % p.mtiles;
-    idx /= p.mtiles;
+    const int mpair = idx % p.mpairs;
+    idx /= p.mpairs;
     const int split = idx % p.smax;
     idx /= p.smax;
     const int g = idx % p.Hkv;
     const int b = idx / p.Hkv;
-    const int unit = (b * p.Hkv + g) * p.mtiles + mtile;
     const int R = p.N + 1, G = p.G;
     pdl_trigger();
     pdl_wait();
     const int P = p.prefix_len[b];
     const int n = p.n_nodes[b];
     if (P < 0 || P > p.cache_cap || n < 0 || n > p.N) {
-        if (tid == 0 && split == 0 && mtile == 0 && g == 0)
+        if (tid == 0 && split == 0 && mpair == 0 && g == 0)
             record_error(p.err, ERR_ATTN | (n < 0 || n > p.N ? ERR_BAD_N_NODES : ERR_BAD_PREFIX_LEN));
         return;
     }
     const int npt = (P + BN - 1) / BN;
     const int splits = npt > 0 ? (npt + p.tps - 1) / p.tps : 1;
     if (split >= splits) return;
-    const int rows_per_node = G;  // query rows of one node
-    const int u0 = mtile * (BM / G);
-    if (u0 > n) {  // every query row of this tile is padding: zeros, once
+    const int nodes_per_tile = BM / G;
+    const int mt0 = 2 * mpair, mt1 = mt0 + 1;
+    const int u00 = mt0 * nodes_per_tile, u01 = mt1 * nodes_per_tile;
+    const bool tile1 = mt1 < p.mtiles;          // the second tile exists
+    const bool has1 = tile1 && (u01 <= n);      // ... and holds a live node
+    if (u00 > n) {  // every query row of both tiles is padding: zeros, once
         if (split != 0) return;
-        for (int r = tid; r < BM; r += kThreads) {
-            const int u = u0 + r / rows_per_node, h = g * G + r % rows_per_node;
-            if (u >= R) continue;
+        for (int r = tid; r < 2 * BM; r += kThreads) {
+            const int u = u00 + r / G, h = g * G + r % G;
+            if (u >= R || (r >= BM && !tile1)) continue;
             uint4* o = (uint4*)(p.out + (((size_t)b * R + u) * p.Hq + h) * D);
 #pragma unroll
             for (int i = 0; i < D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
@@ -148,10 +158,9 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // ---- shared memory carve-up (1024-byte aligned for the 128B swizzle) ----------
     const uint32_t base_u32 = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* base = smem_raw + (base_u32 - smem_u32(smem_raw));
-    uint8_t* sq = base;
-    uint8_t* sk = sq + C::Q_BYTES;           // NS stages of K
-    uint8_t* sv = sk + NS * C::KV_BYTES;     // NS stages of V
-    uint8_t* sp = sv + NS * C::KV_BYTES;     // P tile
+    uint8_t* sq = base;                          // two query tiles
+    uint8_t* sk = sq + 2 * C::QT_BYTES;          // NS stages of K
+    uint8_t* sv = sk + NS * C::KV_BYTES;         // NS stages of V
 
     if (tid == 0) {
         mbar_init(&bar_q, 1);
@@ -159,12 +168,11 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             mbar_init(&bar_full[s], 1);
             mbar_init(&bar_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bar_sfull[s], 1);
-            mbar_init(&bar_sfree[s], 128);
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(&bar_sfull[k], 1);
+            mbar_init(&bar_pfull[k], 128);
+            mbar_init(&bar_odone[k], 1);
         }
-        mbar_init(&bar_pfull, 128);
-        mbar_init(&bar_odone, 1);
         s_abort = 0;
         mbar_init_fence();
     }
@@ -173,7 +181,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    const uint32_t tm_s = tmem, tm_o = tmem + 256;
+    // S_k / P_k at columns 128k; O_k at 256 + D*k
 
     auto fail = [&]() {
         record_error(p.err, ERR_ATTN | ERR_WAIT_TIMEOUT);
@@ -188,9 +196,13 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tma_prefetch_desc(&tm_vc);
             tma_prefetch_desc(&tm_kt);
             tma_prefetch_desc(&tm_vt);
-            mbar_arrive_expect_tx(&bar_q, C::Q_BYTES);
-            for (int h = 0; h < C::NH; ++h)
-                tma_load_3d(sq + h * kHalfBytes, &tm_q, &bar_q, 64 * h, g * G, b * R + u0);
+            mbar_arrive_expect_tx(&bar_q, (has1 ? 2 : 1) * C::QT_BYTES);
+            for (int h = 0; h < C::NH; ++h) {
+                tma_load_3d(sq + h * kHalfBytes, &tm_q, &bar_q, 64 * h, g * G, b * R + u00);
+                if (has1)
+                    tma_load_3d(sq + C::QT_BYTES + h * kHalfBytes, &tm_q, &bar_q, 64 * h, g * G,
+                                b * R + u01);
+            }
             for (int j = 0; j < nt; ++j) {
                 const int s = j % NS;
                 if (!mbar_wait(&bar_empty[s], ((j / NS) & 1) ^ 1, &s_abort)) { fail(); break; }
@@ -217,85 +229,100 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, 0, 1);
-            const uint32_t q_addr = smem_u32(sq), p_addr = smem_u32(sp);
-            bool ok = mbar_wait(&bar_q, 0, &s_abort);
+            const uint32_t q_addr = smem_u32(sq);
+            auto qk = [&](int j, int k) {
+                const uint32_t k_addr = smem_u32(sk + (j % NS) * C::KV_BYTES);
+                const uint32_t qa = q_addr + k * C::QT_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                    mma_bf16_ss(tmem + k * BN, smem_desc_sw128(qa + off, 16, 1024),
+                                smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0);
+                }
+                mma_commit(&bar_sfull[k]);
+            };
+            auto pv = [&](int j, int k) {
+                const uint32_t v_addr = smem_u32(sv + (j % NS) * C::KV_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_bf16_ts(tmem + 256 + k * D, tmem + k * BN + kk * 8,
+                                smem_desc_sw128(v_addr + kk * 2048, kHalfBytes, 1024), idesc_pv,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&bar_odone[k]);
+            };
+            bool ok = mbar_wait(&bar_q, 0, &s_abort) && mbar_wait(&bar_full[0], 0, &s_abort);
             if (!ok) fail();
-            for (int j = 0; ok && j <= nt; ++j) {
-                if (j < nt) {
-                    const int s = j % NS, sb = j & 1, use = j >> 1;
-                    if (!mbar_wait(&bar_full[s], (j / NS) & 1, &s_abort)) { fail(); break; }
-                    if (use >= 1 && !mbar_wait(&bar_sfree[sb], (use - 1) & 1, &s_abort)) { fail(); break; }
+            if (ok) {
+                tc_fence_after();
+                qk(0, 0);
+                if (has1) qk(0, 1);
+            }
+            for (int j = 0; ok && j < nt; ++j) {
+                if (!mbar_wait(&bar_pfull[0], j & 1, &s_abort)) { fail(); break; }
+                tc_fence_after();
+                pv(j, 0);
+                if (j + 1 < nt) {
+                    if (!mbar_wait(&bar_full[(j + 1) % NS], ((j + 1) / NS) & 1, &s_abort)) { fail(); break; }
                     tc_fence_after();
-                    const uint32_t k_addr = smem_u32(sk + s * C::KV_BYTES);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                        mma_bf16_ss(tm_s + sb * BN, smem_desc_sw128(q_addr + off, 16, 1024),
-                                    smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0);
-                    }
-                    mma_commit(&bar_sfull[sb]);
+                    qk(j + 1, 0);  // issued after pv(j, 0): reuses S_0/P_0 in order
                 }
-                if (j >= 1) {
-                    const int jj = j - 1, s2 = jj % NS;
-                    if (!mbar_wait(&bar_pfull, jj & 1, &s_abort)) { fail(); break; }
+                if (has1) {
+                    if (!mbar_wait(&bar_pfull[1], j & 1, &s_abort)) { fail(); break; }
                     tc_fence_after();
-                    const uint32_t v_addr = smem_u32(sv + s2 * C::KV_BYTES);
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        const uint32_t aoff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                        mma_bf16_ss(tm_o, smem_desc_sw128(p_addr + aoff, 16, 1024),
-                                    smem_desc_sw128(v_addr + kk * 2048, kHalfBytes, 1024), idesc_pv,
-                                    (jj > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    mma_commit(&bar_odone);
-                    mma_commit(&bar_empty[s2]);
+                    pv(j, 1);
                 }
+                mma_commit(&bar_empty[j % NS]);
+                if (has1 && j + 1 < nt) qk(j + 1, 1);
             }
         }
     } else {
-        // ====================== softmax / epilogue (128 threads) ======================
+        // ==================== softmax / epilogue, one thread per query row ====================
+        const int k = (warp - 2) >> 2;            // query tile of this group
         const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;  // query row == TMEM lane
+        const int r = quarter * 32 + lane;         // query row == TMEM lane
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const int u = u0 + r / rows_per_node;
-        const int hh = g * G + r % rows_per_node;
-        const bool row_valid = (u <= n);
-        float m_run = -INFINITY, l = 0.f;
+        const uint32_t tm_s = tmem + lane_off + k * BN;
+        const uint32_t tm_o = tmem + lane_off + 256 + k * D;
+        const int mt = mt0 + k;
+        const bool mine = (k == 0) || has1;        // this group has work
+        const int u = (k == 0 ? u00 : u01) + r / G;
+        const int hh = g * G + r % G;
+        const bool row_valid = mine && (u <= n);
+        const float sl2 = p.scale_log2;
+        float m_run = -INFINITY, l = 0.f;          // running max (scaled, log2), sum
         bool ok = true;
-        for (int j = 0; j < nt; ++j) {
-            const int sb = j & 1, use = j >> 1, s = j % NS;
-            if (!mbar_wait(&bar_sfull[sb], use & 1, &s_abort)) { fail(); ok = false; break; }
+        for (int j = 0; mine && j < nt; ++j) {
+            const int s = j % NS;
+            if (!mbar_wait(&bar_sfull[k], j & 1, &s_abort)) { fail(); ok = false; break; }
             tc_fence_after();
             float sc[BN];
             {
                 uint32_t t[32];
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) {
-                    tmem_ld32(tm_s + lane_off + sb * BN + c * 32, t);
+                    tmem_ld32(tm_s + c * 32, t);
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) sc[c * 32 + i] = __uint_as_float(t[i]);
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&bar_sfree[sb]);
-
-            // ---- mask + scale (log2 domain) ----
+            // ---- mask (partial prefix tile: key range; tree tile: ancestor bits) ----
             const bool is_tree = (j >= nprefix);
-            bool key_r_valid;
-            float mt = -INFINITY;
-            if (!is_tree) {
-                const int lim = P - (t_begin + j) * BN;  // keys c < lim are real
-                key_r_valid = r < lim;
+            const int lim = is_tree ? (n + 1 - (j - nprefix) * BN) : (P - (t_begin + j) * BN);
+            const bool key_r_valid = r < lim;
+            float mt_raw = -INFINITY;
+            if (!is_tree && lim >= BN) {
+#pragma unroll
+                for (int c = 0; c < BN; ++c) mt_raw = fmaxf(mt_raw, sc[c]);
+            } else if (!is_tree) {
 #pragma unroll
                 for (int c = 0; c < BN; ++c) {
-                    const float v = (c < lim) ? sc[c] * p.scale_log2 : -INFINITY;
+                    const float v = (c < lim) ? sc[c] : -INFINITY;
                     sc[c] = v;
-                    mt = fmaxf(mt, v);
+                    mt_raw = fmaxf(mt_raw, v);
                 }
             } else {
                 const int a0 = (j - nprefix) * BN;
-                key_r_valid = (a0 + r) <= n;
                 uint32_t wd[4];
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
@@ -304,60 +331,53 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                 ? __ldg(&p.anc_mask[((size_t)b * R + u) * p.W + wi])
                                 : 0u;
                 }
-                const int lim = n + 1 - a0;  // tree keys c < lim exist
 #pragma unroll
                 for (int c = 0; c < BN; ++c) {
                     const bool on = ((wd[c >> 5] >> (c & 31)) & 1u) && (c < lim);
-                    const float v = on ? sc[c] * p.scale_log2 : -INFINITY;
+                    const float v = on ? sc[c] : -INFINITY;
                     sc[c] = v;
-                    mt = fmaxf(mt, v);
+                    mt_raw = fmaxf(mt_raw, v);
                 }
             }
-            const float m_new = fmaxf(m_run, mt);
+            const float m_new = fmaxf(m_run, mt_raw * sl2);
             const bool resc = m_new > m_run + kRescaleLog2;
             const float m_use = resc ? m_new : m_run;
             const float factor = resc ? fast_exp2(m_run - m_new) : 1.f;
-
-            // PV of the previous tile must be done before O or P is touched.
-            if (j >= 1) {
-                if (!mbar_wait(&bar_odone, (j - 1) & 1, &s_abort)) { fail(); ok = false; break; }
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, factor != 1.f)) {
-                    uint32_t t[32];
+            // O_k is stable here: the commit that signalled S_k covers the
+            // previous tile's P_k V product.
+            if (j >= 1 && __any_sync(0xffffffffu, factor != 1.f)) {
+                uint32_t t[32];
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        tmem_ld32(tm_o + lane_off + c * 32, t);
-                        tmem_ld_wait();
+                for (int c = 0; c < D / 32; ++c) {
+                    tmem_ld32(tm_o + c * 32, t);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            t[i] = __float_as_uint(__uint_as_float(t[i]) * factor);
-                        tmem_st32(tm_o + lane_off + c * 32, t);
-                    }
-                    tmem_st_wait();
+                    for (int i = 0; i < 32; ++i)
+                        t[i] = __float_as_uint(__uint_as_float(t[i]) * factor);
+                    tmem_st32(tm_o + c * 32, t);
                 }
             }
             l *= factor;
             m_run = m_use;
 
-            // ---- P = 2^(s - m) as bf16, row r of the swizzled K-major P tile ----
-            const float mref = (m_use == -INFINITY) ? 0.f : m_use;
+            // ---- P = 2^(s*scale*log2e - m) as bf16 pairs, written over S_k ----
+            const float neg = (m_use == -INFINITY) ? 0.f : -m_use;
             float sum = 0.f;
 #pragma unroll
-            for (int c16 = 0; c16 < BN / 8; ++c16) {
-                uint32_t w4[4];
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = fast_exp2(sc[c16 * 8 + 2 * e] - mref);
-                    const float p1 = fast_exp2(sc[c16 * 8 + 2 * e + 1] - mref);
-                    w4[e] = pack_bf16x2(p0, p1);
-                    sum += __uint_as_float(w4[e] << 16) + __uint_as_float(w4[e] & 0xffff0000u);
+                for (int c = 0; c < 32; ++c) {
+                    const float p0 = fast_exp2(fmaf(sc[half * 64 + 2 * c], sl2, neg));
+                    const float p1 = fast_exp2(fmaf(sc[half * 64 + 2 * c + 1], sl2, neg));
+                    sum += p0 + p1;
+                    pk[c] = pack_bf16x2(p0, p1);
                 }
-                const int half = c16 >> 3, chunk = c16 & 7;
-                uint8_t* dst = sp + half * kHalfBytes + r * 128 + ((chunk ^ (r & 7)) << 4);
-                *(uint4*)dst = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                tmem_st32(tm_s + half * 32, pk);
             }
+            tmem_st_wait();
             l += sum;
-            if (!key_r_valid) {
+            if (k == 0 && !key_r_valid) {
                 // key r of this tile is past the sequence: zero its V row so that
                 // uninitialised cache memory (possibly NaN) cannot reach O.
                 if (!mbar_wait(&bar_full[s], (j / NS) & 1, &s_abort)) { fail(); ok = false; break; }
@@ -367,33 +387,37 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         *(uint4*)(vrow + h * kHalfBytes + i * 16) = make_uint4(0, 0, 0, 0);
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&bar_pfull);
+            mbar_arrive(&bar_pfull[k]);
         }
 
         // ---- epilogue (every softmax thread runs the same barrier sequence) ----
-        if (ok && !mbar_wait(&bar_odone, (nt - 1) & 1, &s_abort)) { fail(); ok = false; }
+        if (mine && ok && !mbar_wait(&bar_odone[k], (nt - 1) & 1, &s_abort)) { fail(); ok = false; }
         const bool all_ok = softmax_bar_and(ok);
         float o[D];
-        if (all_ok) {
+        if (all_ok && mine) {
             tc_fence_after();
             uint32_t t[32];
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                tmem_ld32(tm_o + lane_off + c * 32, t);
+                tmem_ld32(tm_o + c * 32, t);
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) o[c * 32 + i] = __uint_as_float(t[i]);
             }
+        } else {
+#pragma unroll
+            for (int d = 0; d < D; ++d) o[d] = 0.f;
         }
         tc_fence_before();
         float M = m_run, Lsum = l;
-        bool write = all_ok;
+        bool write = all_ok && (mine || (tile1 && split == 0));
+        const size_t tslot = ((size_t)(b * p.Hkv + g) * p.mtiles + mt) * p.smax;
         if (splits > 1) {
-            const size_t slot = (size_t)unit * p.smax + split;
-            if (all_ok) {
+            if (all_ok && mine) {
+                const size_t slot = tslot + split;
                 float* po = p.part_o + slot * D * BM;
 #pragma unroll
                 for (int d = 0; d < D; ++d) po[d * BM + r] = o[d];
@@ -402,19 +426,21 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 __threadfence();
             }
             softmax_bar();
-            if (tid == 64) s_last = all_ok && ticket_is_last(&p.tickets[unit], (unsigned)splits);
+            if (tid == 64)
+                s_last = all_ok && ticket_is_last(&p.tickets[(b * p.Hkv + g) * p.mpairs + mpair],
+                                                  (unsigned)splits);
             softmax_bar();
-            write = s_last;
-            if (write) {
+            write = s_last && (mine || tile1);
+            if (s_last && mine) {
                 M = -INFINITY;
                 for (int s2 = 0; s2 < splits; ++s2)
-                    M = fmaxf(M, __ldcg(&p.part_ml[((size_t)unit * p.smax + s2) * 2 * BM + r]));
+                    M = fmaxf(M, __ldcg(&p.part_ml[(tslot + s2) * 2 * BM + r]));
                 const float mref = (M == -INFINITY) ? 0.f : M;
                 Lsum = 0.f;
 #pragma unroll
                 for (int d = 0; d < D; ++d) o[d] = 0.f;
                 for (int s2 = 0; s2 < splits; ++s2) {
-                    const size_t sl = (size_t)unit * p.smax + s2;
+                    const size_t sl = tslot + s2;
                     const float w = fast_exp2(__ldcg(&p.part_ml[sl * 2 * BM + r]) - mref);
                     Lsum += __ldcg(&p.part_ml[sl * 2 * BM + BM + r]) * w;
                     const float* q = p.part_o + sl * D * BM;
@@ -423,7 +449,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
             }
         }
-        if (write && u < R) {
+        if (write && u < R && (k == 0 || tile1)) {
             const bool live = row_valid && Lsum > 0.f;
             const float inv = live ? 1.f / Lsum : 0.f;
             uint4* dst = (uint4*)(p.out + (((size_t)b * R + u) * p.Hq + hh) * D);
@@ -478,7 +504,7 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_
 }
 
 struct Plan {
-    int mtiles, tps, smax;
+    int mtiles, mpairs, tps, smax;
 };
 
 // Streaming multiprocessors of the current device (148 if the query fails).
@@ -495,16 +521,17 @@ int num_sms() {
     return cached[dev];
 }
 
-// Split the prefix of each (sequence, KV head, M tile) unit into KV splits of
-// `tps` tiles.  Few units: split until one wave of CTAs (one per SM) is full.
-// Many units: cap a split at a quarter of the longest prefix so that long
-// sequences of a ragged batch do not leave a tail of lone CTAs.
+// Split the prefix of each (sequence, KV head, pair of query tiles) unit into
+// KV splits of `tps` tiles.  Few units: split until one wave of CTAs (one per
+// SM) is full.  Many units: cap a split at a quarter of the longest prefix so
+// that long sequences of a ragged batch do not leave a tail of lone CTAs.
 Plan make_plan(int B, int N, int Hq, int Hkv, int64_t cache_cap) {
     Plan pl;
     const int G = Hq / Hkv;
     pl.mtiles = ((N + 1) * G + BM - 1) / BM;
+    pl.mpairs = (pl.mtiles + 1) / 2;
     const int max_tiles = (int)((cache_cap + BN - 1) / BN);
-    const long units = (long)B * Hkv * pl.mtiles;
+    const long units = (long)B * Hkv * pl.mpairs;
     const int sms = num_sms();
     if (max_tiles <= 1) {
         pl.tps = 1;
@@ -525,10 +552,10 @@ struct WsLayout {
 WsLayout attn_layout(int B, int N, int Hq, int Hkv, int D, int64_t cache_cap) {
     const Plan pl = make_plan(B, N, Hq, Hkv, cache_cap);
     WsLayout w{};
-    const size_t units = (size_t)B * Hkv * pl.mtiles;
+    const size_t units = (size_t)B * Hkv * pl.mtiles;  // partials per query tile
     if (pl.smax <= 1) return w;
-    w.tickets = 0;
-    w.part_o = align_up(units * 4, 256);
+    w.tickets = 0;  // one counter per (sequence, KV head, tile pair)
+    w.part_o = align_up((size_t)B * Hkv * pl.mpairs * 4, 256);
     w.part_ml = align_up(w.part_o + units * pl.smax * (size_t)D * BM * 4, 256);
     w.total = align_up(w.part_ml + units * pl.smax * 2 * BM * 4, 256);
     return w;
@@ -567,11 +594,11 @@ cudaError_t launch_d(const AttnArgs& a, const Plan& pl, const WsLayout& wl, cuda
     p.part_o = pl.smax > 1 ? (float*)(ws + wl.part_o) : nullptr;
     p.part_ml = pl.smax > 1 ? (float*)(ws + wl.part_ml) : nullptr;
     p.B = a.B; p.N = a.N; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.W = (a.N + 1 + 31) / 32;
-    p.mtiles = pl.mtiles; p.tps = pl.tps; p.smax = pl.smax;
+    p.mtiles = pl.mtiles; p.mpairs = pl.mpairs; p.tps = pl.tps; p.smax = pl.smax;
     p.cache_cap = a.cache_cap;
     p.scale_log2 = a.scale * kLog2e;
     p.err = a.err;
-    const long grid = (long)a.B * a.Hkv * pl.mtiles * pl.smax;
+    const long grid = (long)a.B * a.Hkv * pl.mpairs * pl.smax;
     return launch_pdl(tree_attn_kernel<D>, dim3((unsigned)grid), dim3(kThreads),
                       (size_t)Cfg<D>::SMEM, s, mq, mkc, mvc, mkt, mvt, p);
 }
