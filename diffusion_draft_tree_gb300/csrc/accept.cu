@@ -25,7 +25,7 @@ namespace ddt {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kChunkBytes = 16384;
+constexpr int kChunkBytes = 32768;
 constexpr int kMaxChunks = 128;
 
 struct AcceptWs {
@@ -81,7 +81,7 @@ DDT_DEV float block_exclusive_scan(float v, float* s_warp, float& total) {
 }
 
 template <bool BF16>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 5)
 accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nchunks,
               bool aligned, const int32_t* __restrict__ parent, const int32_t* __restrict__ token,
               const int32_t* __restrict__ n_nodes, int L, int N, float temperature, float c_exp,
@@ -247,19 +247,17 @@ accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nc
         // Rescan chunk cs with a contiguous segment per thread, in token order.
         constexpr int SEG = Chunk::SIZE / kThreads;
         const int e0 = cs * Chunk::SIZE + tid * SEG;
-        float seg[SEG];
-        float tsum = 0.f;
-#pragma unroll
-        for (int i = 0; i < SEG; ++i) {
-            const int e = e0 + i;
+        auto weight = [&](int e) {
             float v = -INFINITY;
             if (e < V) {
                 if (BF16) v = bf16lo((uint32_t)__ldcg((const unsigned short*)rowp + e));
                 else v = __ldcg((const float*)rowp + e);
             }
-            seg[i] = fast_exp2((v - mref) * c_exp);
-            tsum += seg[i];
-        }
+            return fast_exp2((v - mref) * c_exp);
+        };
+        float tsum = 0.f;
+#pragma unroll 8
+        for (int i = 0; i < SEG; ++i) tsum += weight(e0 + i);
         float total;
         const float before = block_exclusive_scan(tsum, s_red, total);
         // The owner is the first thread whose running sum passes tloc; if
@@ -274,14 +272,14 @@ accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nc
         }
         __syncthreads();
         const int owner = (s_first != 0x7fffffff) ? s_first : s_lastnz;
-        if (tid == owner) {
+        if (tid == owner) {  // walks its segment again, in token order
             float acc = before;
             int p = -1, lastnz = -1;
-#pragma unroll
             for (int i = 0; i < SEG; ++i) {
-                acc += seg[i];
+                const float w = weight(e0 + i);
+                acc += w;
                 if (p < 0 && acc > tloc) p = e0 + i;
-                if (seg[i] > 0.f) lastnz = e0 + i;
+                if (w > 0.f) lastnz = e0 + i;
             }
             s_pick = (p >= 0) ? p : lastnz;
         }

@@ -35,11 +35,19 @@ uint32_t* error_word() {
 
 inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
-ddtree_status launched(cudaError_t e) { return e == cudaSuccess ? DDTREE_OK : DDTREE_ERR_CUDA; }
+thread_local const char* t_last_cuda_error = "no error";
+
+ddtree_status launched(cudaError_t e) {
+    if (e == cudaSuccess) return DDTREE_OK;
+    t_last_cuda_error = cudaGetErrorName(e);
+    return DDTREE_ERR_CUDA;
+}
 
 }  // namespace
 
 extern "C" {
+
+const char* ddtree_last_cuda_error(void) { return t_last_cuda_error; }
 
 const char* ddtree_status_str(ddtree_status s) {
     switch (s) {

@@ -94,7 +94,7 @@ DDT_DEV bool softmax_bar_and(bool v) {
 // the tensor core runs O_k += P_k V_j with P_k read straight from TMEM.  While
 // one group exponentiates, the tensor core works on the other group's tile.
 template <int D>
-__global__ void __maxnreg__(200)
+__global__ void __maxnreg__(192)
 tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
                  const __grid_constant__ CUtensorMap tm_vc,
                  const __grid_constant__ CUtensorMap tm_kt,

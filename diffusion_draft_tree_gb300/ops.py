@@ -33,6 +33,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "CUDA error
 class DDTreeError(RuntimeError):
     def __init__(self, fn: str, status: int, detail: int = 0):
         msg = f"{fn}: {STATUS.get(status, status)}"
+        if status == 3:
+            msg += f" ({lib.ddtree_last_cuda_error().decode()})"
         if detail:
             msg += f" (detail 0x{detail:08x})"
         super().__init__(msg)
@@ -57,6 +59,8 @@ def _load() -> ctypes.CDLL:
     lib.ddtree_accept.argtypes = [P, i32, i64, P, P, P, i32, i32, i32, i32, f32, u64, u64, P, P,
                                   P, P, P, P, sz, P]
     lib.ddtree_device_check.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.ddtree_last_cuda_error.argtypes = []
+    lib.ddtree_last_cuda_error.restype = ctypes.c_char_p
     lib.ddtree_status_str.argtypes = [i32]
     lib.ddtree_status_str.restype = ctypes.c_char_p
     for f in ("ddtree_topk", "ddtree_build", "ddtree_build_heap", "ddtree_tree_attn",
@@ -68,7 +72,8 @@ def _load() -> ctypes.CDLL:
 lib = _load()
 
 EXPORTED = ("ddtree_workspace_size", "ddtree_topk", "ddtree_build", "ddtree_build_heap",
-            "ddtree_tree_attn", "ddtree_accept", "ddtree_device_check", "ddtree_status_str")
+            "ddtree_tree_attn", "ddtree_accept", "ddtree_device_check", "ddtree_last_cuda_error",
+            "ddtree_status_str")
 
 
 def _ptr(t: Optional[torch.Tensor]):

@@ -208,6 +208,10 @@ ddtree_status ddtree_accept(const void* target_logits, int dtype, int64_t row_st
  * *detail when non-null: which kernel and what was wrong), or DDTREE_ERR_CUDA. */
 ddtree_status ddtree_device_check(void* stream, uint32_t* detail);
 
+/* Name of the CUDA error behind the calling thread's most recent
+ * DDTREE_ERR_CUDA (e.g. "cudaErrorInvalidValue"), or "no error". */
+const char* ddtree_last_cuda_error(void);
+
 /* Static description of a status code. */
 const char* ddtree_status_str(ddtree_status s);
 
