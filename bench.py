@@ -481,6 +481,20 @@ def reference_arm(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def aggregate_replicas(ms_local: float, world: int, B: int, steps: int, device):
+    """Replicas: every rank ran `steps` rounds of B sequences on its own GPU.
+    The job's time is the slowest rank's; its throughput counts every rank's
+    sequences.  Returns (max milliseconds over ranks, sequence-rounds per second)."""
+    ms = ms_local
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * B * steps / (ms / 1e3)
+
+
 def config_of(w, R):
     c = {"workload": w.name, "B": w.B, "L": w.L, "V": w.V, "K": w.K, "N": w.N,
          "P": list(w.P) if len(set(w.P)) > 1 else w.P[0], "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
@@ -514,14 +528,8 @@ def main():
             print(json.dumps({"profile_rounds": args.profile_rounds, "workload": w.name,
                               "copies": res["R"]}), flush=True)
         return
-    ms_total = res["ms_total"]
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total, value = aggregate_replicas(res["ms_total"], world, w.B, args.steps, dev)
     ms_step = ms_total / args.steps
-    value = world * w.B * args.steps / (ms_total / 1e3)
     peaks = load_peaks()
     model = work_model(w, res["tree_anc"])
     names = ["topk", "build", "tree_attn", "accept"]

@@ -94,7 +94,7 @@ DDT_DEV bool softmax_bar_and(bool v) {
 // the tensor core runs O_k += P_k V_j with P_k read straight from TMEM.  While
 // one group exponentiates, the tensor core works on the other group's tile.
 template <int D>
-__global__ void __maxnreg__(192)
+__global__ void __launch_bounds__(kThreads, 1)
 tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
                  const __grid_constant__ CUtensorMap tm_vc,
                  const __grid_constant__ CUtensorMap tm_kt,
@@ -295,35 +295,14 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int s = j % NS;
             if (!mbar_wait(&bar_sfull[k], j & 1, &s_abort)) { fail(); ok = false; break; }
             tc_fence_after();
-            float sc[BN];
-            {
-                uint32_t t[32];
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    tmem_ld32(tm_s + c * 32, t);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) sc[c * 32 + i] = __uint_as_float(t[i]);
-                }
-            }
             // ---- mask (partial prefix tile: key range; tree tile: ancestor bits) ----
             const bool is_tree = (j >= nprefix);
             const int lim = is_tree ? (n + 1 - (j - nprefix) * BN) : (P - (t_begin + j) * BN);
             const bool key_r_valid = r < lim;
-            float mt_raw = -INFINITY;
-            if (!is_tree && lim >= BN) {
-#pragma unroll
-                for (int c = 0; c < BN; ++c) mt_raw = fmaxf(mt_raw, sc[c]);
-            } else if (!is_tree) {
-#pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    const float v = (c < lim) ? sc[c] : -INFINITY;
-                    sc[c] = v;
-                    mt_raw = fmaxf(mt_raw, v);
-                }
-            } else {
+            const bool full = !is_tree && lim >= BN;  // a whole prefix tile: no mask
+            uint32_t wd[4] = {0u, 0u, 0u, 0u};
+            if (is_tree) {
                 const int a0 = (j - nprefix) * BN;
-                uint32_t wd[4];
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
                     const int wi = (a0 >> 5) + w;
@@ -331,13 +310,20 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                 ? __ldg(&p.anc_mask[((size_t)b * R + u) * p.W + wi])
                                 : 0u;
                 }
+            }
+            auto keep = [&](int c) {
+                return full || (c < lim && (!is_tree || ((wd[c >> 5] >> (c & 31)) & 1u)));
+            };
+            // pass 1: row max over the tile, 32 columns at a time
+            float mt_raw = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    const bool on = ((wd[c >> 5] >> (c & 31)) & 1u) && (c < lim);
-                    const float v = on ? sc[c] : -INFINITY;
-                    sc[c] = v;
-                    mt_raw = fmaxf(mt_raw, v);
-                }
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t t[32];
+                tmem_ld32(tm_s + c0, t);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (keep(c0 + i)) mt_raw = fmaxf(mt_raw, __uint_as_float(t[i]));
             }
             const float m_new = fmaxf(m_run, mt_raw * sl2);
             const bool resc = m_new > m_run + kRescaleLog2;
@@ -346,9 +332,9 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // O_k is stable here: the commit that signalled S_k covers the
             // previous tile's P_k V product.
             if (j >= 1 && __any_sync(0xffffffffu, factor != 1.f)) {
-                uint32_t t[32];
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
+                    uint32_t t[32];
                     tmem_ld32(tm_o + c * 32, t);
                     tmem_ld_wait();
 #pragma unroll
@@ -360,19 +346,30 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             l *= factor;
             m_run = m_use;
 
-            // ---- P = 2^(s*scale*log2e - m) as bf16 pairs, written over S_k ----
+            // pass 2: P = 2^(s*scale*log2e - m) as bf16 pairs, 64 columns at a
+            // time, written over the first half of those columns of S_k
             const float neg = (m_use == -INFINITY) ? 0.f : -m_use;
             float sum = 0.f;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t pk[32];
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const float p0 = fast_exp2(fmaf(sc[half * 64 + 2 * c], sl2, neg));
-                    const float p1 = fast_exp2(fmaf(sc[half * 64 + 2 * c + 1], sl2, neg));
-                    sum += p0 + p1;
-                    pk[c] = pack_bf16x2(p0, p1);
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t t[32];
+                    tmem_ld32(tm_s + half * 64 + q * 32, t);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int c = half * 64 + q * 32 + 2 * i;
+                        const float p0 = keep(c) ? fast_exp2(fmaf(__uint_as_float(t[2 * i]), sl2, neg)) : 0.f;
+                        const float p1 = keep(c + 1) ? fast_exp2(fmaf(__uint_as_float(t[2 * i + 1]), sl2, neg)) : 0.f;
+                        sum += p0 + p1;
+                        pk[q * 16 + i] = pack_bf16x2(p0, p1);
+                    }
                 }
+                // P columns [32*half, 32*half+32) hold keys [64*half, 64*half+64);
+                // S columns read above were [64*half, 64*half+64): no overlap
+                // with what this store overwrites in the next half's reads.
                 tmem_st32(tm_s + half * 32, pk);
             }
             tmem_st_wait();
@@ -396,31 +393,61 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // ---- epilogue (every softmax thread runs the same barrier sequence) ----
         if (mine && ok && !mbar_wait(&bar_odone[k], (nt - 1) & 1, &s_abort)) { fail(); ok = false; }
         const bool all_ok = softmax_bar_and(ok);
-        float o[D];
-        if (all_ok && mine) {
-            tc_fence_after();
-            uint32_t t[32];
+        const bool have = all_ok && mine;          // warp-uniform
+        tc_fence_after();
+        const size_t tslot = ((size_t)(b * p.Hkv + g) * p.mtiles + mt) * p.smax;
+        const bool row_out = (k == 0 || tile1) && u < R;
+        uint4* dst = (uint4*)(p.out + (((size_t)b * R + u) * p.Hq + hh) * D);
+        // writes 32 output columns of this row, scaled by inv
+        auto store32 = [&](int c, const float (&v)[32], float inv) {
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                tmem_ld32(tm_o + c * 32, t);
-                tmem_ld_wait();
+            for (int i = 0; i < 4; ++i)
+                dst[c * 4 + i] =
+                    make_uint4(pack_bf16x2(v[8 * i] * inv, v[8 * i + 1] * inv),
+                               pack_bf16x2(v[8 * i + 2] * inv, v[8 * i + 3] * inv),
+                               pack_bf16x2(v[8 * i + 4] * inv, v[8 * i + 5] * inv),
+                               pack_bf16x2(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
+        };
+        auto store_lse = [&](bool live, float M, float Ls) {
+            if (p.lse)
+                p.lse[((size_t)b * R + u) * p.Hq + hh] =
+                    live ? (M + __log2f(Ls)) * 0.6931471805599453f : -INFINITY;
+        };
+        if (splits == 1) {
+            if (have) {
+                const bool live = row_valid && l > 0.f;
+                const float inv = live ? 1.f / l : 0.f;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[c * 32 + i] = __uint_as_float(t[i]);
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t t[32];
+                    tmem_ld32(tm_o + c * 32, t);
+                    tmem_ld_wait();
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(t[i]);
+                    if (row_out) store32(c, v, inv);
+                }
+                if (row_out) store_lse(live, m_run, l);
+            } else if (all_ok && row_out && split == 0) {  // a tile of padding rows
+                float z[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) z[i] = 0.f;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) store32(c, z, 0.f);
+                store_lse(false, 0.f, 0.f);
             }
         } else {
-#pragma unroll
-            for (int d = 0; d < D; ++d) o[d] = 0.f;
-        }
-        tc_fence_before();
-        float M = m_run, Lsum = l;
-        bool write = all_ok && (mine || (tile1 && split == 0));
-        const size_t tslot = ((size_t)(b * p.Hkv + g) * p.mtiles + mt) * p.smax;
-        if (splits > 1) {
-            if (all_ok && mine) {
+            if (have) {
                 const size_t slot = tslot + split;
                 float* po = p.part_o + slot * D * BM;
 #pragma unroll
-                for (int d = 0; d < D; ++d) po[d * BM + r] = o[d];
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t t[32];
+                    tmem_ld32(tm_o + c * 32, t);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) po[(c * 32 + i) * BM + r] = __uint_as_float(t[i]);
+                }
                 p.part_ml[slot * 2 * BM + r] = m_run;
                 p.part_ml[slot * 2 * BM + BM + r] = l;
                 __threadfence();
@@ -430,39 +457,43 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 s_last = all_ok && ticket_is_last(&p.tickets[(b * p.Hkv + g) * p.mpairs + mpair],
                                                   (unsigned)splits);
             softmax_bar();
-            write = s_last && (mine || tile1);
             if (s_last && mine) {
-                M = -INFINITY;
+                float M = -INFINITY;
                 for (int s2 = 0; s2 < splits; ++s2)
                     M = fmaxf(M, __ldcg(&p.part_ml[(tslot + s2) * 2 * BM + r]));
                 const float mref = (M == -INFINITY) ? 0.f : M;
-                Lsum = 0.f;
+                float Ls = 0.f;
+                for (int s2 = 0; s2 < splits; ++s2)
+                    Ls += __ldcg(&p.part_ml[(tslot + s2) * 2 * BM + BM + r]) *
+                          fast_exp2(__ldcg(&p.part_ml[(tslot + s2) * 2 * BM + r]) - mref);
+                const bool live = row_valid && Ls > 0.f;
+                const float inv = live ? 1.f / Ls : 0.f;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    float v[32];
 #pragma unroll
-                for (int d = 0; d < D; ++d) o[d] = 0.f;
-                for (int s2 = 0; s2 < splits; ++s2) {
-                    const size_t sl = tslot + s2;
-                    const float w = fast_exp2(__ldcg(&p.part_ml[sl * 2 * BM + r]) - mref);
-                    Lsum += __ldcg(&p.part_ml[sl * 2 * BM + BM + r]) * w;
-                    const float* q = p.part_o + sl * D * BM;
+                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                    for (int s2 = 0; s2 < splits; ++s2) {
+                        const size_t sl = tslot + s2;
+                        const float w = fast_exp2(__ldcg(&p.part_ml[sl * 2 * BM + r]) - mref);
+                        const float* q = p.part_o + sl * D * BM + (size_t)(c * 32) * BM + r;
 #pragma unroll
-                    for (int d = 0; d < D; ++d) o[d] += __ldcg(&q[d * BM + r]) * w;
+                        for (int i = 0; i < 32; ++i) v[i] += __ldcg(&q[i * BM]) * w;
+                    }
+                    if (row_out) store32(c, v, inv);
                 }
+                if (row_out) store_lse(live, M, Ls);
+            }
+            if (all_ok && !mine && tile1 && row_out && split == 0) {  // padding tile: zeros
+                float z[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) z[i] = 0.f;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) store32(c, z, 0.f);
+                store_lse(false, 0.f, 0.f);
             }
         }
-        if (write && u < R && (k == 0 || tile1)) {
-            const bool live = row_valid && Lsum > 0.f;
-            const float inv = live ? 1.f / Lsum : 0.f;
-            uint4* dst = (uint4*)(p.out + (((size_t)b * R + u) * p.Hq + hh) * D);
-#pragma unroll
-            for (int i = 0; i < D / 8; ++i)
-                dst[i] = make_uint4(pack_bf16x2(o[8 * i] * inv, o[8 * i + 1] * inv),
-                                    pack_bf16x2(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
-                                    pack_bf16x2(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
-                                    pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
-            if (p.lse)
-                p.lse[((size_t)b * R + u) * p.Hq + hh] =
-                    live ? (M + __log2f(Lsum)) * 0.6931471805599453f : -INFINITY;
-        }
+        tc_fence_before();
     }
 
     // ---- teardown: every thread arrives here (all waits are bounded) -------------
