@@ -73,6 +73,27 @@ DDT_DEV uint32_t pack_bf16x2(float lo, float hi) {
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
+// Packed fp32x2 arithmetic (two lanes per instruction on sm_100-class GPUs).
+DDT_DEV float2 ffma2(float2 a, float b, float c) {
+    unsigned long long A, B, C, R;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(B) : "f"(b));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(C) : "f"(c));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(R) : "l"(A), "l"(B), "l"(C));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(R));
+    return r;
+}
+DDT_DEV float2 fadd2(float2 a, float2 b) {
+    unsigned long long A, B, R;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b.x), "f"(b.y));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(R) : "l"(A), "l"(B));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(R));
+    return r;
+}
+
 // Named barrier over the 256 softmax threads (both query tiles).
 DDT_DEV void softmax_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 DDT_DEV bool softmax_bar_and(bool v) {
@@ -295,36 +316,47 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int s = j % NS;
             if (!mbar_wait(&bar_sfull[k], j & 1, &s_abort)) { fail(); ok = false; break; }
             tc_fence_after();
-            // ---- mask (partial prefix tile: key range; tree tile: ancestor bits) ----
+            // ---- validity of the tile's keys: one 32-bit mask per 32 columns ----
+            // (a whole prefix tile needs none; the last, partial prefix tile keys
+            // below the prefix length; a tree tile the row's ancestor bits)
             const bool is_tree = (j >= nprefix);
             const int lim = is_tree ? (n + 1 - (j - nprefix) * BN) : (P - (t_begin + j) * BN);
             const bool key_r_valid = r < lim;
-            const bool full = !is_tree && lim >= BN;  // a whole prefix tile: no mask
-            uint32_t wd[4] = {0u, 0u, 0u, 0u};
+            const bool full = !is_tree && lim >= BN;
+            uint32_t vm[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int rem = lim - 32 * c;
+                vm[c] = rem >= 32 ? ~0u : (rem <= 0 ? 0u : ((1u << rem) - 1u));
+            }
             if (is_tree) {
                 const int a0 = (j - nprefix) * BN;
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const int wi = (a0 >> 5) + w;
-                    wd[w] = (row_valid && wi < p.W)
-                                ? __ldg(&p.anc_mask[((size_t)b * R + u) * p.W + wi])
-                                : 0u;
+                for (int c = 0; c < 4; ++c) {
+                    const int wi = (a0 >> 5) + c;
+                    vm[c] &= (row_valid && wi < p.W)
+                                 ? __ldg(&p.anc_mask[((size_t)b * R + u) * p.W + wi])
+                                 : 0u;
                 }
             }
-            auto keep = [&](int c) {
-                return full || (c < lim && (!is_tree || ((wd[c >> 5] >> (c & 31)) & 1u)));
-            };
-            // pass 1: row max over the tile, 32 columns at a time
-            float mt_raw = -INFINITY;
+            // ---- pass 1: row max, 32 columns at a time, four independent chains ----
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c0 = 0; c0 < BN; c0 += 32) {
+            for (int c0 = 0; c0 < 4; ++c0) {
                 uint32_t t[32];
-                tmem_ld32(tm_s + c0, t);
+                tmem_ld32(tm_s + 32 * c0, t);
                 tmem_ld_wait();
+                if (full) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (keep(c0 + i)) mt_raw = fmaxf(mt_raw, __uint_as_float(t[i]));
+                    for (int i = 0; i < 32; ++i) mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(t[i]));
+                } else {
+                    const uint32_t m = vm[c0];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        mx[i & 3] = fmaxf(mx[i & 3], ((m >> i) & 1u) ? __uint_as_float(t[i]) : -INFINITY);
+                }
             }
+            const float mt_raw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
             const float m_new = fmaxf(m_run, mt_raw * sl2);
             const bool resc = m_new > m_run + kRescaleLog2;
             const float m_use = resc ? m_new : m_run;
@@ -332,7 +364,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // O_k is stable here: the commit that signalled S_k covers the
             // previous tile's P_k V product.
             if (j >= 1 && __any_sync(0xffffffffu, factor != 1.f)) {
-#pragma unroll
+#pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t t[32];
                     tmem_ld32(tm_o + c * 32, t);
@@ -346,30 +378,49 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             l *= factor;
             m_run = m_use;
 
-            // pass 2: P = 2^(s*scale*log2e - m) as bf16 pairs, 64 columns at a
-            // time, written over the first half of those columns of S_k
+            // ---- pass 2: P = 2^(s*scale*log2e - m) as bf16 pairs, 64 columns at a
+            // time, written over the first half of those columns of S_k (the P
+            // columns of half h are [32h, 32h+32), all read before they are written)
             const float neg = (m_use == -INFINITY) ? 0.f : -m_use;
             float sum = 0.f;
-#pragma unroll
+#pragma unroll 1
             for (int half = 0; half < 2; ++half) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    uint32_t t[32];
-                    tmem_ld32(tm_s + half * 64 + q * 32, t);
-                    tmem_ld_wait();
+                uint32_t t0[32], t1[32], pk[32];
+                tmem_ld32(tm_s + half * 64, t0);
+                tmem_ld32(tm_s + half * 64 + 32, t1);
+                tmem_ld_wait();
+                if (full) {
+                    // Many keys: the row sum takes the fp32 weights (their bf16
+                    // rounding averages out over a whole tile).
+                    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const int c = half * 64 + q * 32 + 2 * i;
-                        const float p0 = keep(c) ? fast_exp2(fmaf(__uint_as_float(t[2 * i]), sl2, neg)) : 0.f;
-                        const float p1 = keep(c + 1) ? fast_exp2(fmaf(__uint_as_float(t[2 * i + 1]), sl2, neg)) : 0.f;
-                        sum += p0 + p1;
-                        pk[q * 16 + i] = pack_bf16x2(p0, p1);
+                        const float2 y0 = ffma2(make_float2(__uint_as_float(t0[2 * i]), __uint_as_float(t0[2 * i + 1])), sl2, neg);
+                        const float2 y1 = ffma2(make_float2(__uint_as_float(t1[2 * i]), __uint_as_float(t1[2 * i + 1])), sl2, neg);
+                        const float2 e0 = make_float2(fast_exp2(y0.x), fast_exp2(y0.y));
+                        const float2 e1 = make_float2(fast_exp2(y1.x), fast_exp2(y1.y));
+                        pk[i] = pack_bf16x2(e0.x, e0.y);
+                        pk[16 + i] = pack_bf16x2(e1.x, e1.y);
+                        acc0 = fadd2(acc0, e0);
+                        acc1 = fadd2(acc1, e1);
+                    }
+                    sum += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+                } else {
+                    // Few keys (partial or tree tile): the row sum takes exactly
+                    // the bf16 weights the P V product sees.
+                    const uint32_t m0 = half ? vm[2] : vm[0], m1 = half ? vm[3] : vm[1];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float a = ((m0 >> (2 * i)) & 1u) ? fast_exp2(fmaf(__uint_as_float(t0[2 * i]), sl2, neg)) : 0.f;
+                        const float bq = ((m0 >> (2 * i + 1)) & 1u) ? fast_exp2(fmaf(__uint_as_float(t0[2 * i + 1]), sl2, neg)) : 0.f;
+                        const float c = ((m1 >> (2 * i)) & 1u) ? fast_exp2(fmaf(__uint_as_float(t1[2 * i]), sl2, neg)) : 0.f;
+                        const float d = ((m1 >> (2 * i + 1)) & 1u) ? fast_exp2(fmaf(__uint_as_float(t1[2 * i + 1]), sl2, neg)) : 0.f;
+                        pk[i] = pack_bf16x2(a, bq);
+                        pk[16 + i] = pack_bf16x2(c, d);
+                        sum += (__uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u)) +
+                               (__uint_as_float(pk[16 + i] << 16) + __uint_as_float(pk[16 + i] & 0xffff0000u));
                     }
                 }
-                // P columns [32*half, 32*half+32) hold keys [64*half, 64*half+64);
-                // S columns read above were [64*half, 64*half+64): no overlap
-                // with what this store overwrites in the next half's reads.
                 tmem_st32(tm_s + half * 32, pk);
             }
             tmem_st_wait();
