@@ -59,7 +59,7 @@ struct Params {
     const uint32_t* anc_mask;
     uint16_t* out;
     float* lse;
-    float* part_o;   // [B*Hkv*mtiles][smax][D][128]
+    uint32_t* part_o;  // [B*Hkv*mtiles][smax][D/2][128] bf16 pairs of O / l
     float* part_ml;  // [B*Hkv*mtiles][smax][2][128]
     unsigned int* tickets;  // [B*Hkv*mpairs]
     int B, N, Hq, Hkv, G, W, mtiles, mpairs, tps, smax;
@@ -489,15 +489,19 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
         } else {
             if (have) {
+                // partial: O / l as bf16 pairs [D/2][128], plus (m, l) in fp32
                 const size_t slot = tslot + split;
-                float* po = p.part_o + slot * D * BM;
+                uint32_t* po = p.part_o + slot * (D / 2) * BM;
+                const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t t[32];
                     tmem_ld32(tm_o + c * 32, t);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) po[(c * 32 + i) * BM + r] = __uint_as_float(t[i]);
+                    for (int i = 0; i < 16; ++i)
+                        po[(c * 16 + i) * BM + r] = pack_bf16x2(__uint_as_float(t[2 * i]) * inv,
+                                                                __uint_as_float(t[2 * i + 1]) * inv);
                 }
                 p.part_ml[slot * 2 * BM + r] = m_run;
                 p.part_ml[slot * 2 * BM + BM + r] = l;
@@ -509,6 +513,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                                   (unsigned)splits);
             softmax_bar();
             if (s_last && mine) {
+                // out = sum_s w_s o_s / sum_s w_s, w_s = l_s 2^(m_s - M)
                 float M = -INFINITY;
                 for (int s2 = 0; s2 < splits; ++s2)
                     M = fmaxf(M, __ldcg(&p.part_ml[(tslot + s2) * 2 * BM + r]));
@@ -524,12 +529,20 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = 0.f;
+#pragma unroll 2
                     for (int s2 = 0; s2 < splits; ++s2) {
                         const size_t sl = tslot + s2;
-                        const float w = fast_exp2(__ldcg(&p.part_ml[sl * 2 * BM + r]) - mref);
-                        const float* q = p.part_o + sl * D * BM + (size_t)(c * 32) * BM + r;
+                        const float w = __ldcg(&p.part_ml[sl * 2 * BM + BM + r]) *
+                                        fast_exp2(__ldcg(&p.part_ml[sl * 2 * BM + r]) - mref);
+                        const uint32_t* q = p.part_o + sl * (D / 2) * BM + (size_t)(c * 16) * BM + r;
+                        uint32_t x[16];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] += __ldcg(&q[i * BM]) * w;
+                        for (int i = 0; i < 16; ++i) x[i] = __ldcg(&q[i * BM]);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            v[2 * i] += w * __uint_as_float(x[i] << 16);
+                            v[2 * i + 1] += w * __uint_as_float(x[i] & 0xffff0000u);
+                        }
                     }
                     if (row_out) store32(c, v, inv);
                 }
@@ -605,7 +618,7 @@ int num_sms() {
 
 // Split the prefix of each (sequence, KV head, pair of query tiles) unit into
 // KV splits of `tps` tiles.  Few units: split until one wave of CTAs (one per
-// SM) is full.  Many units: cap a split at a quarter of the longest prefix so
+// SM) is full, but keep at least 4 tiles in a split.  Many units: cap a split at a quarter of the longest prefix so
 // that long sequences of a ragged batch do not leave a tail of lone CTAs.
 Plan make_plan(int B, int N, int Hq, int Hkv, int64_t cache_cap) {
     Plan pl;
@@ -618,7 +631,9 @@ Plan make_plan(int B, int N, int Hq, int Hkv, int64_t cache_cap) {
     if (max_tiles <= 1) {
         pl.tps = 1;
     } else if (units < sms) {
-        const int splits = (int)std::max(1L, std::min<long>(sms / units, max_tiles));
+        // at least 4 KV tiles per split: each split's partial costs a merge
+        const long cap = std::max(1, (max_tiles + 3) / 4);
+        const int splits = (int)std::max(1L, std::min<long>(sms / units, cap));
         pl.tps = (max_tiles + splits - 1) / splits;
     } else {
         pl.tps = max_tiles > 64 ? std::max(32, (max_tiles + 3) / 4) : max_tiles;
@@ -638,7 +653,7 @@ WsLayout attn_layout(int B, int N, int Hq, int Hkv, int D, int64_t cache_cap) {
     if (pl.smax <= 1) return w;
     w.tickets = 0;  // one counter per (sequence, KV head, tile pair)
     w.part_o = align_up((size_t)B * Hkv * pl.mpairs * 4, 256);
-    w.part_ml = align_up(w.part_o + units * pl.smax * (size_t)D * BM * 4, 256);
+    w.part_ml = align_up(w.part_o + units * pl.smax * (size_t)D * BM * 2, 256);
     w.total = align_up(w.part_ml + units * pl.smax * 2 * BM * 4, 256);
     return w;
 }
@@ -673,7 +688,7 @@ cudaError_t launch_d(const AttnArgs& a, const Plan& pl, const WsLayout& wl, cuda
     p.lse = a.lse;
     char* ws = (char*)a.ws;
     p.tickets = pl.smax > 1 ? (unsigned int*)(ws + wl.tickets) : nullptr;
-    p.part_o = pl.smax > 1 ? (float*)(ws + wl.part_o) : nullptr;
+    p.part_o = pl.smax > 1 ? (uint32_t*)(ws + wl.part_o) : nullptr;
     p.part_ml = pl.smax > 1 ? (float*)(ws + wl.part_ml) : nullptr;
     p.B = a.B; p.N = a.N; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.W = (a.N + 1 + 31) / 32;
     p.mtiles = pl.mtiles; p.mpairs = pl.mpairs; p.tps = pl.tps; p.smax = pl.smax;
