@@ -185,5 +185,24 @@ DDT_DEV void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
 DDT_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 DDT_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// ---- thread-block clusters: barrier and distributed shared memory ---------------
+// Every thread of every CTA in the cluster must arrive (the non-.aligned forms
+// allow divergent warps).  release/acquire order shared-memory writes made
+// before the arrive with reads by other CTAs after their wait.
+DDT_DEV void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// Address, in the cluster's shared window, of `saddr` in the CTA of rank `rank`.
+DDT_DEV uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+DDT_DEV float ld_dsmem_f32(uint32_t caddr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
+    return v;
+}
+
 }  // namespace sm100
 }  // namespace ddt

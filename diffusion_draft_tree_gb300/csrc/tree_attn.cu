@@ -19,9 +19,11 @@
 // bf16 over the S columns it came from and feeds the P V product directly, so
 // shared memory holds only Q, K and V.  The two groups alternate on the tensor
 // core: while one exponentiates, the other's products run.  When a unit's
-// prefix is split, each split writes (O, m, l) partials and the last split's
-// CTA (atomic ticket) merges them.  Every mbarrier wait is bounded in wall
-// time; a timeout records an error and the CTA unwinds.
+// prefix is split, the splits run as one thread-block cluster: each keeps its
+// unnormalised O and (m, l) in its own shared memory, and after a cluster
+// barrier every CTA merges a slice of the head dimension for all rows, reading
+// its peers' partials through distributed shared memory.  Every mbarrier wait
+// is bounded in wall time; a timeout records an error and the CTA unwinds.
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -43,6 +45,7 @@ constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
 constexpr int kHalfBytes = 128 * 128;  // [128 rows][64 bf16], one 128B-swizzled slab
 constexpr float kRescaleLog2 = 8.f;
 constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxSplits = 8;  // KV splits of one unit = CTAs of one (portable) cluster
 
 template <int D>
 struct Cfg {
@@ -51,6 +54,8 @@ struct Cfg {
     static constexpr int KV_BYTES = NH * kHalfBytes;  // one K (or V) tile
     static constexpr int NS = (D == 128) ? 2 : 3;
     static constexpr int SMEM = 1024 + 2 * QT_BYTES + NS * 2 * KV_BYTES;
+    // a split's partial (fp32 O of both tiles, then m and l) reuses Q and K/V
+    static_assert((D + 2) * 2 * BM * 4 <= SMEM - 1024, "partial fits in shared memory");
 };
 
 struct Params {
@@ -59,9 +64,6 @@ struct Params {
     const uint32_t* anc_mask;
     uint16_t* out;
     float* lse;
-    uint32_t* part_o;  // [B*Hkv*mtiles][smax][D/2][128] bf16 pairs of O / l
-    float* part_ml;  // [B*Hkv*mtiles][smax][2][128]
-    unsigned int* tickets;  // [B*Hkv*mpairs]
     int B, N, Hq, Hkv, G, W, mtiles, mpairs, tps, smax;
     int64_t cache_cap;
     float scale_log2;
@@ -94,8 +96,7 @@ DDT_DEV float2 fadd2(float2 a, float2 b) {
     return r;
 }
 
-// Named barrier over the 256 softmax threads (both query tiles).
-DDT_DEV void softmax_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Named barrier over the 256 softmax threads (both query tiles), AND of `v`.
 DDT_DEV bool softmax_bar_and(bool v) {
     uint32_t r;
     asm volatile(
@@ -127,16 +128,15 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         bar_pfull[2], bar_odone[2];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
-    __shared__ bool s_last;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // ---- decode the unit --------------------------------------------------------
+    // ---- decode the unit (its KV splits are consecutive CTAs: one cluster) -------
     int idx = blockIdx.x;
+    const int split = idx % p.smax;  // == rank in the cluster
+    idx /= p.smax;
     const int mpair = idx % p.mpairs;
     idx /= p.mpairs;
-    const int split = idx % p.smax;
-    idx /= p.smax;
     const int g = idx % p.Hkv;
     const int b = idx / p.Hkv;
     const int R = p.N + 1, G = p.G;
@@ -151,7 +151,6 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     const int npt = (P + BN - 1) / BN;
     const int splits = npt > 0 ? (npt + p.tps - 1) / p.tps : 1;
-    if (split >= splits) return;
     const int nodes_per_tile = BM / G;
     const int mt0 = 2 * mpair, mt1 = mt0 + 1;
     const int u00 = mt0 * nodes_per_tile, u01 = mt1 * nodes_per_tile;
@@ -166,6 +165,13 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
             for (int i = 0; i < D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
             if (p.lse) p.lse[((size_t)b * R + u) * p.Hq + h] = -INFINITY;
+        }
+        return;  // (the whole cluster takes this exit: it depends on b and mpair only)
+    }
+    if (split >= splits) {  // no KV tiles here: only keep the cluster's barrier count
+        if (p.smax > 1) {
+            cluster_sync();
+            cluster_sync();
         }
         return;
     }
@@ -304,7 +310,6 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tm_s = tmem + lane_off + k * BN;
         const uint32_t tm_o = tmem + lane_off + 256 + k * D;
-        const int mt = mt0 + k;
         const bool mine = (k == 0) || has1;        // this group has work
         const int u = (k == 0 ? u00 : u01) + r / G;
         const int hh = g * G + r % G;
@@ -446,7 +451,6 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const bool all_ok = softmax_bar_and(ok);
         const bool have = all_ok && mine;          // warp-uniform
         tc_fence_after();
-        const size_t tslot = ((size_t)(b * p.Hkv + g) * p.mtiles + mt) * p.smax;
         const bool row_out = (k == 0 || tile1) && u < R;
         uint4* dst = (uint4*)(p.out + (((size_t)b * R + u) * p.Hq + hh) * D);
         // writes 32 output columns of this row, scaled by inv
@@ -487,75 +491,22 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 for (int c = 0; c < D / 32; ++c) store32(c, z, 0.f);
                 store_lse(false, 0.f, 0.f);
             }
-        } else {
-            if (have) {
-                // partial: O / l as bf16 pairs [D/2][128], plus (m, l) in fp32
-                const size_t slot = tslot + split;
-                uint32_t* po = p.part_o + slot * (D / 2) * BM;
-                const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t t[32];
-                    tmem_ld32(tm_o + c * 32, t);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        po[(c * 16 + i) * BM + r] = pack_bf16x2(__uint_as_float(t[2 * i]) * inv,
-                                                                __uint_as_float(t[2 * i + 1]) * inv);
-                }
-                p.part_ml[slot * 2 * BM + r] = m_run;
-                p.part_ml[slot * 2 * BM + BM + r] = l;
-                __threadfence();
-            }
-            softmax_bar();
-            if (tid == 64)
-                s_last = all_ok && ticket_is_last(&p.tickets[(b * p.Hkv + g) * p.mpairs + mpair],
-                                                  (unsigned)splits);
-            softmax_bar();
-            if (s_last && mine) {
-                // out = sum_s w_s o_s / sum_s w_s, w_s = l_s 2^(m_s - M)
-                float M = -INFINITY;
-                for (int s2 = 0; s2 < splits; ++s2)
-                    M = fmaxf(M, __ldcg(&p.part_ml[(tslot + s2) * 2 * BM + r]));
-                const float mref = (M == -INFINITY) ? 0.f : M;
-                float Ls = 0.f;
-                for (int s2 = 0; s2 < splits; ++s2)
-                    Ls += __ldcg(&p.part_ml[(tslot + s2) * 2 * BM + BM + r]) *
-                          fast_exp2(__ldcg(&p.part_ml[(tslot + s2) * 2 * BM + r]) - mref);
-                const bool live = row_valid && Ls > 0.f;
-                const float inv = live ? 1.f / Ls : 0.f;
+        } else if (have) {
+            // This split's partial, unnormalised, into its own shared memory (Q and
+            // K/V stages are free: every MMA has completed): O as fp32 [D][256 rows],
+            // then m and l as [2][256 rows].
+            float* part = reinterpret_cast<float*>(base);
+            const int row2 = k * BM + r;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    float v[32];
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t t[32];
+                tmem_ld32(tm_o + c * 32, t);
+                tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
-#pragma unroll 2
-                    for (int s2 = 0; s2 < splits; ++s2) {
-                        const size_t sl = tslot + s2;
-                        const float w = __ldcg(&p.part_ml[sl * 2 * BM + BM + r]) *
-                                        fast_exp2(__ldcg(&p.part_ml[sl * 2 * BM + r]) - mref);
-                        const uint32_t* q = p.part_o + sl * (D / 2) * BM + (size_t)(c * 16) * BM + r;
-                        uint32_t x[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) x[i] = __ldcg(&q[i * BM]);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            v[2 * i] += w * __uint_as_float(x[i] << 16);
-                            v[2 * i + 1] += w * __uint_as_float(x[i] & 0xffff0000u);
-                        }
-                    }
-                    if (row_out) store32(c, v, inv);
-                }
-                if (row_out) store_lse(live, M, Ls);
+                for (int i = 0; i < 32; ++i) part[(c * 32 + i) * 2 * BM + row2] = __uint_as_float(t[i]);
             }
-            if (all_ok && !mine && tile1 && row_out && split == 0) {  // padding tile: zeros
-                float z[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) z[i] = 0.f;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) store32(c, z, 0.f);
-                store_lse(false, 0.f, 0.f);
-            }
+            part[D * 2 * BM + row2] = m_run;
+            part[(D + 1) * 2 * BM + row2] = l;
         }
         tc_fence_before();
     }
@@ -563,6 +514,81 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // ---- teardown: every thread arrives here (all waits are bounded) -------------
     tc_fence_before();
     __syncthreads();
+    if (p.smax > 1) {
+        cluster_sync();  // every split's partial is in its shared memory
+        if (splits > 1 && warp >= 2) {
+            // Merge: this CTA writes head-dimension columns [8 c_lo, 8 c_hi) of all
+            // rows of both tiles.  out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+            const int k = (warp - 2) >> 2;
+            const int r = (warp & 3) * 32 + lane;
+            const int row2 = k * BM + r;
+            const int u = (k == 0 ? u00 : u01) + r / G;
+            const int hh = g * G + r % G;
+            const bool mine = (k == 0) || has1;
+            const bool row_out = (k == 0 || tile1) && u < R;
+            const bool row_valid = mine && u <= n;
+            constexpr int nch = D / 8;
+            const int c_lo = split * nch / splits, c_hi = (split + 1) * nch / splits;
+            uint4* dst = (uint4*)(p.out + (((size_t)b * R + u) * p.Hq + hh) * D);
+            float M = -INFINITY, Ls = 0.f;
+            float w[kMaxSplits];
+            uint32_t pb[kMaxSplits];
+            if (row_valid) {
+                const uint32_t own = smem_u32(base) + (uint32_t)row2 * 4u;
+                float ms[kMaxSplits];
+#pragma unroll
+                for (int s2 = 0; s2 < kMaxSplits; ++s2) {
+                    pb[s2] = own;
+                    ms[s2] = -INFINITY;
+                    if (s2 < splits) {
+                        pb[s2] = mapa_shared(own, (uint32_t)s2);
+                        ms[s2] = ld_dsmem_f32(pb[s2] + (uint32_t)(D * 2 * BM) * 4u);
+                    }
+                    M = fmaxf(M, ms[s2]);
+                }
+                const float mref = (M == -INFINITY) ? 0.f : M;
+#pragma unroll
+                for (int s2 = 0; s2 < kMaxSplits; ++s2) {
+                    w[s2] = 0.f;
+                    if (s2 < splits) {
+                        w[s2] = fast_exp2(ms[s2] - mref);
+                        Ls += w[s2] * ld_dsmem_f32(pb[s2] + (uint32_t)((D + 1) * 2 * BM) * 4u);
+                    }
+                }
+            }
+            const bool live = row_valid && Ls > 0.f;
+            const float inv = live ? 1.f / Ls : 0.f;
+            if (row_out) {
+#pragma unroll 1
+                for (int c = c_lo; c < c_hi; ++c) {
+                    float acc[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+                    if (live) {
+#pragma unroll
+                        for (int s2 = 0; s2 < kMaxSplits; ++s2) {
+                            if (s2 < splits) {
+                                float x[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    x[i] = ld_dsmem_f32(pb[s2] + (uint32_t)((c * 8 + i) * 2 * BM) * 4u);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) acc[i] = fmaf(w[s2], x[i], acc[i]);
+                            }
+                        }
+                    }
+                    dst[c] = make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                                        pack_bf16x2(acc[2] * inv, acc[3] * inv),
+                                        pack_bf16x2(acc[4] * inv, acc[5] * inv),
+                                        pack_bf16x2(acc[6] * inv, acc[7] * inv));
+                }
+                if (split == 0 && p.lse)
+                    p.lse[((size_t)b * R + u) * p.Hq + hh] =
+                        live ? (M + __log2f(Ls)) * 0.6931471805599453f : -INFINITY;
+            }
+        }
+        cluster_sync();  // peers have finished reading this CTA's shared memory
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -617,10 +643,12 @@ int num_sms() {
 }
 
 // Split the prefix of each (sequence, KV head, pair of query tiles) unit into
-// KV splits of `tps` tiles.  Few units: split until one wave of CTAs (one per
-// SM) is full, but keep at least 4 tiles in a split.  Many units: cap a split at a quarter of the longest prefix so
-// that long sequences of a ragged batch do not leave a tail of lone CTAs.
-Plan make_plan(int B, int N, int Hq, int Hkv, int64_t cache_cap) {
+// KV splits of `tps` tiles; the splits of a unit form one cluster of at most
+// kMaxSplits CTAs and merge on chip.  Few units: split until one wave of CTAs
+// (one per SM) is full, keeping at least 2 tiles in a split.  Many units: cap a
+// split at a quarter of the longest prefix so that long sequences of a ragged
+// batch do not leave a tail of lone CTAs.
+Plan make_plan(int B, int N, int Hq, int Hkv, int64_t cache_cap, int max_splits) {
     Plan pl;
     const int G = Hq / Hkv;
     pl.mtiles = ((N + 1) * G + BM - 1) / BM;
@@ -631,35 +659,53 @@ Plan make_plan(int B, int N, int Hq, int Hkv, int64_t cache_cap) {
     if (max_tiles <= 1) {
         pl.tps = 1;
     } else if (units < sms) {
-        // at least 4 KV tiles per split: each split's partial costs a merge
-        const long cap = std::max(1, (max_tiles + 3) / 4);
+        const long cap = std::min<long>(max_splits, (max_tiles + 1) / 2);
         const int splits = (int)std::max(1L, std::min<long>(sms / units, cap));
         pl.tps = (max_tiles + splits - 1) / splits;
     } else {
         pl.tps = max_tiles > 64 ? std::max(32, (max_tiles + 3) / 4) : max_tiles;
     }
+    pl.tps = std::max(pl.tps, (max_tiles + max_splits - 1) / max_splits);
     pl.smax = max_tiles > 0 ? (max_tiles + pl.tps - 1) / pl.tps : 1;
     return pl;
 }
 
-struct WsLayout {
-    size_t tickets, part_o, part_ml, total;
-};
-
-WsLayout attn_layout(int B, int N, int Hq, int Hkv, int D, int64_t cache_cap) {
-    const Plan pl = make_plan(B, N, Hq, Hkv, cache_cap);
-    WsLayout w{};
-    const size_t units = (size_t)B * Hkv * pl.mtiles;  // partials per query tile
-    if (pl.smax <= 1) return w;
-    w.tickets = 0;  // one counter per (sequence, KV head, tile pair)
-    w.part_o = align_up((size_t)B * Hkv * pl.mpairs * 4, 256);
-    w.part_ml = align_up(w.part_o + units * pl.smax * (size_t)D * BM * 2, 256);
-    w.total = align_up(w.part_ml + units * pl.smax * 2 * BM * 4, 256);
-    return w;
+// Largest cluster (<= kMaxSplits CTAs, halving) that the device can co-schedule
+// with this kernel's shared memory; 1 if none.  Needs the kernel's dynamic
+// shared-memory attribute set first.
+template <int D>
+int cluster_cap(int dev) {
+    static int cached[64];
+    int& c = cached[dev & 63];
+    if (!c) {
+        int cap = 1;
+        for (int size = kMaxSplits; size >= 2; size /= 2) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)size);
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = Cfg<D>::SMEM;
+            cudaLaunchAttribute at;
+            at.id = cudaLaunchAttributeClusterDimension;
+            at.val.clusterDim.x = (unsigned)size;
+            at.val.clusterDim.y = 1;
+            at.val.clusterDim.z = 1;
+            cfg.attrs = &at;
+            cfg.numAttrs = 1;
+            int active = 0;
+            if (cudaOccupancyMaxActiveClusters(&active, tree_attn_kernel<D>, &cfg) == cudaSuccess &&
+                active > 0) {
+                cap = size;
+                break;
+            }
+            (void)cudaGetLastError();  // a refused size is not an error of the call
+        }
+        c = cap;
+    }
+    return c;
 }
 
 template <int D>
-cudaError_t launch_d(const AttnArgs& a, const Plan& pl, const WsLayout& wl, cudaStream_t s) {
+cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
     static std::once_flag once[64];
     int dev = 0;
     cudaGetDevice(&dev);
@@ -669,6 +715,7 @@ cudaError_t launch_d(const AttnArgs& a, const Plan& pl, const WsLayout& wl, cuda
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
     });
     if (attr_err != cudaSuccess) return attr_err;
+    const Plan pl = make_plan(a.B, a.N, a.Hq, a.Hkv, a.cache_cap, cluster_cap<D>(dev));
     const int G = a.Hq / a.Hkv, R = a.N + 1;
     CUtensorMap mq, mkc, mvc, mkt, mvt;
     const uint64_t rowb = (uint64_t)D * 2;
@@ -686,31 +733,25 @@ cudaError_t launch_d(const AttnArgs& a, const Plan& pl, const WsLayout& wl, cuda
     p.anc_mask = a.anc_mask;
     p.out = (uint16_t*)a.out;
     p.lse = a.lse;
-    char* ws = (char*)a.ws;
-    p.tickets = pl.smax > 1 ? (unsigned int*)(ws + wl.tickets) : nullptr;
-    p.part_o = pl.smax > 1 ? (uint32_t*)(ws + wl.part_o) : nullptr;
-    p.part_ml = pl.smax > 1 ? (float*)(ws + wl.part_ml) : nullptr;
     p.B = a.B; p.N = a.N; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.W = (a.N + 1 + 31) / 32;
     p.mtiles = pl.mtiles; p.mpairs = pl.mpairs; p.tps = pl.tps; p.smax = pl.smax;
     p.cache_cap = a.cache_cap;
     p.scale_log2 = a.scale * kLog2e;
     p.err = a.err;
     const long grid = (long)a.B * a.Hkv * pl.mpairs * pl.smax;
-    return launch_pdl(tree_attn_kernel<D>, dim3((unsigned)grid), dim3(kThreads),
-                      (size_t)Cfg<D>::SMEM, s, mq, mkc, mvc, mkt, mvt, p);
+    return launch_pdl_cluster(tree_attn_kernel<D>, dim3((unsigned)grid), dim3(kThreads),
+                              (size_t)Cfg<D>::SMEM, s, (unsigned)pl.smax, mq, mkc, mvc, mkt, mvt,
+                              p);
 }
 
 }  // namespace
 
-size_t attn_workspace_bytes(int B, int N, int Hq, int Hkv, int D, int64_t cache_cap) {
-    return attn_layout(B, N, Hq, Hkv, D, cache_cap).total;
-}
+// The KV splits merge through distributed shared memory: no workspace.
+size_t attn_workspace_bytes(int, int, int, int, int, int64_t) { return 0; }
 
 cudaError_t launch_tree_attn(const AttnArgs& a, cudaStream_t s) {
-    const Plan pl = make_plan(a.B, a.N, a.Hq, a.Hkv, a.cache_cap);
-    const WsLayout wl = attn_layout(a.B, a.N, a.Hq, a.Hkv, a.D, a.cache_cap);
-    if (a.D == 128) return launch_d<128>(a, pl, wl, s);
-    return launch_d<64>(a, pl, wl, s);
+    if (a.D == 128) return launch_d<128>(a, s);
+    return launch_d<64>(a, s);
 }
 
 }  // namespace ddt

@@ -126,6 +126,7 @@ def _random_case(seed, B, N, Hq, Hkv, D, P, cap, L=4, K=3):
     (2, 60, 4, 2, 64, (257, 3), 260, 3, 3),      # K^L = 39 < N: padding rows
     (1, 511, 8, 1, 128, (2000,), 2048, 16, 16),  # G = 8, N + 1 = 512
     (1, 1024, 4, 2, 128, (129,), 129, 16, 16),   # largest budget
+    (3, 30, 8, 2, 64, (0, 2000, 700), 2048, 4, 3),  # 8-CTA clusters, some CTAs idle
 ])
 def test_attn_edge_cases(cuda_device, B, N, Hq, Hkv, D, P, cap, L, K):
     q, kc, vc, kt, vt, plen, t = _random_case(B * 7 + N + D + cap, B, N, Hq, Hkv, D, P, cap, L, K)
