@@ -45,7 +45,11 @@ constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
 constexpr int kHalfBytes = 128 * 128;  // [128 rows][64 bf16], one 128B-swizzled slab
 constexpr float kRescaleLog2 = 8.f;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kMaxSplits = 8;  // KV splits of one unit = CTAs of one (portable) cluster
+constexpr int kMaxSplits = 16;  // KV splits of one unit = CTAs of one cluster
+// How the KV splits of a unit combine: a single split stores directly; few
+// units run each unit's splits as one cluster and merge on chip; many units
+// (clusters would fragment the schedule) merge through a global workspace.
+constexpr int kMergeNone = 0, kMergeCluster = 1, kMergeGlobal = 2;
 
 template <int D>
 struct Cfg {
@@ -64,7 +68,11 @@ struct Params {
     const uint32_t* anc_mask;
     uint16_t* out;
     float* lse;
+    uint32_t* part_o;       // global merge: [B*Hkv*mtiles][smax][D/2][128] bf16 pairs of O / l
+    float* part_ml;         // global merge: [B*Hkv*mtiles][smax][2][128]
+    unsigned int* tickets;  // global merge: [B*Hkv*mpairs]
     int B, N, Hq, Hkv, G, W, mtiles, mpairs, tps, smax;
+    int merge;              // how the KV splits of a unit combine: kMerge*
     int64_t cache_cap;
     float scale_log2;
     uint32_t* err;
@@ -96,7 +104,9 @@ DDT_DEV float2 fadd2(float2 a, float2 b) {
     return r;
 }
 
-// Named barrier over the 256 softmax threads (both query tiles), AND of `v`.
+// Named barrier over the 256 softmax threads (both query tiles).
+DDT_DEV void softmax_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// ... and the AND of `v` over them.
 DDT_DEV bool softmax_bar_and(bool v) {
     uint32_t r;
     asm volatile(
@@ -115,6 +125,8 @@ DDT_DEV bool softmax_bar_and(bool v) {
 // group k reads S_k, writes P_k (bf16) over the first 64 of those columns, and
 // the tensor core runs O_k += P_k V_j with P_k read straight from TMEM.  While
 // one group exponentiates, the tensor core works on the other group's tile.
+// A unit's key tiles are its prefix tiles followed by its tree tiles; split s
+// takes tiles [s tps, (s+1) tps) of that list.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
@@ -128,8 +140,39 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         bar_pfull[2], bar_odone[2];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
+    __shared__ bool s_last;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // ---- set-up that reads no global memory (overlaps the previous kernel) -------
+    if (tid == 0) {
+        mbar_init(&bar_q, 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&bar_full[s], 1);
+            mbar_init(&bar_empty[s], 1);
+        }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(&bar_sfull[k], 1);
+            mbar_init(&bar_pfull[k], 128);
+            mbar_init(&bar_odone[k], 1);
+        }
+        s_abort = 0;
+        mbar_init_fence();
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_kc);
+        tma_prefetch_desc(&tm_vc);
+        tma_prefetch_desc(&tm_kt);
+        tma_prefetch_desc(&tm_vt);
+    }
+    if (warp == 1) tmem_alloc(&s_tmem, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    // S_k / P_k at columns 128k; O_k at 256 + D*k
+    auto free_tmem = [&]() {  // only on exits where no tcgen05 operation was issued
+        if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    };
 
     // ---- decode the unit (its KV splits are consecutive CTAs: one cluster) -------
     int idx = blockIdx.x;
@@ -144,43 +187,47 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     pdl_wait();
     const int P = p.prefix_len[b];
     const int n = p.n_nodes[b];
-    if (P < 0 || P > p.cache_cap || n < 0 || n > p.N) {
+    if (P < 0 || P > p.cache_cap || n < 0 || n > p.N) {  // (the whole cluster exits here)
         if (tid == 0 && split == 0 && mpair == 0 && g == 0)
             record_error(p.err, ERR_ATTN | (n < 0 || n > p.N ? ERR_BAD_N_NODES : ERR_BAD_PREFIX_LEN));
+        free_tmem();
         return;
     }
-    const int npt = (P + BN - 1) / BN;
-    const int splits = npt > 0 ? (npt + p.tps - 1) / p.tps : 1;
+    const int npt = (P + BN - 1) / BN;      // prefix tiles
+    const int ntt = (n + 1 + BN - 1) / BN;  // tree tiles
+    const int splits = (npt + ntt + p.tps - 1) / p.tps;
     const int nodes_per_tile = BM / G;
     const int mt0 = 2 * mpair, mt1 = mt0 + 1;
     const int u00 = mt0 * nodes_per_tile, u01 = mt1 * nodes_per_tile;
     const bool tile1 = mt1 < p.mtiles;          // the second tile exists
     const bool has1 = tile1 && (u01 <= n);      // ... and holds a live node
     if (u00 > n) {  // every query row of both tiles is padding: zeros, once
-        if (split != 0) return;
-        for (int r = tid; r < 2 * BM; r += kThreads) {
-            const int u = u00 + r / G, h = g * G + r % G;
-            if (u >= R || (r >= BM && !tile1)) continue;
-            uint4* o = (uint4*)(p.out + (((size_t)b * R + u) * p.Hq + h) * D);
+        if (split == 0) {
+            for (int r = tid; r < 2 * BM; r += kThreads) {
+                const int u = u00 + r / G, h = g * G + r % G;
+                if (u >= R || (r >= BM && !tile1)) continue;
+                uint4* o = (uint4*)(p.out + (((size_t)b * R + u) * p.Hq + h) * D);
 #pragma unroll
-            for (int i = 0; i < D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
-            if (p.lse) p.lse[((size_t)b * R + u) * p.Hq + h] = -INFINITY;
+                for (int i = 0; i < D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+                if (p.lse) p.lse[((size_t)b * R + u) * p.Hq + h] = -INFINITY;
+            }
         }
+        free_tmem();
         return;  // (the whole cluster takes this exit: it depends on b and mpair only)
     }
     if (split >= splits) {  // no KV tiles here: only keep the cluster's barrier count
-        if (p.smax > 1) {
+        if (p.merge == kMergeCluster) {
             cluster_sync();
             cluster_sync();
         }
+        free_tmem();
         return;
     }
     const int t_begin = split * p.tps;
-    const int t_end = min(npt, t_begin + p.tps);
-    const int nprefix = max(0, t_end - t_begin);
-    const bool last_split = (split == splits - 1);
-    const int ntree = last_split ? (n + 1 + BN - 1) / BN : 0;
-    const int nt = nprefix + ntree;
+    const int t_end = min(npt + ntt, t_begin + p.tps);
+    const int nprefix = max(0, min(npt, t_end) - t_begin);
+    const int tree_first = max(t_begin, npt) - npt;  // first tree tile of this split
+    const int nt = t_end - t_begin;                  // >= 1; tiles >= nprefix are tree tiles
 
     // ---- shared memory carve-up (1024-byte aligned for the 128B swizzle) ----------
     const uint32_t base_u32 = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -188,27 +235,6 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     uint8_t* sq = base;                          // two query tiles
     uint8_t* sk = sq + 2 * C::QT_BYTES;          // NS stages of K
     uint8_t* sv = sk + NS * C::KV_BYTES;         // NS stages of V
-
-    if (tid == 0) {
-        mbar_init(&bar_q, 1);
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&bar_full[s], 1);
-            mbar_init(&bar_empty[s], 1);
-        }
-        for (int k = 0; k < 2; ++k) {
-            mbar_init(&bar_sfull[k], 1);
-            mbar_init(&bar_pfull[k], 128);
-            mbar_init(&bar_odone[k], 1);
-        }
-        s_abort = 0;
-        mbar_init_fence();
-    }
-    if (warp == 1) tmem_alloc(&s_tmem, kTmemCols);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = s_tmem;
-    // S_k / P_k at columns 128k; O_k at 256 + D*k
 
     auto fail = [&]() {
         record_error(p.err, ERR_ATTN | ERR_WAIT_TIMEOUT);
@@ -218,11 +244,6 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (warp == 0) {
         // =========================== TMA producer ===========================
         if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_kc);
-            tma_prefetch_desc(&tm_vc);
-            tma_prefetch_desc(&tm_kt);
-            tma_prefetch_desc(&tm_vt);
             mbar_arrive_expect_tx(&bar_q, (has1 ? 2 : 1) * C::QT_BYTES);
             for (int h = 0; h < C::NH; ++h) {
                 tma_load_3d(sq + h * kHalfBytes, &tm_q, &bar_q, 64 * h, g * G, b * R + u00);
@@ -243,7 +264,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         tma_load_3d(dv + h * kHalfBytes, &tm_vc, &bar_full[s], 64 * h, p0, b * p.Hkv + g);
                     }
                 } else {
-                    const int a0 = (j - nprefix) * BN;
+                    const int a0 = (tree_first + j - nprefix) * BN;
                     for (int h = 0; h < C::NH; ++h) {
                         tma_load_3d(dk + h * kHalfBytes, &tm_kt, &bar_full[s], 64 * h, g, b * R + a0);
                         tma_load_3d(dv + h * kHalfBytes, &tm_vt, &bar_full[s], 64 * h, g, b * R + a0);
@@ -315,6 +336,17 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int hh = g * G + r % G;
         const bool row_valid = mine && (u <= n);
         const float sl2 = p.scale_log2;
+        // ancestor words of this row for the next tree tile, fetched one tile ahead
+        uint32_t am[4] = {0u, 0u, 0u, 0u};
+        auto fetch_mask = [&](int tt) {
+            const uint32_t* mrow = p.anc_mask + ((size_t)b * R + u) * p.W;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int wi = tt * (BN / 32) + c;
+                am[c] = (row_valid && wi < p.W) ? __ldg(&mrow[wi]) : 0u;
+            }
+        };
+        if (nprefix < nt) fetch_mask(tree_first);
         float m_run = -INFINITY, l = 0.f;          // running max (scaled, log2), sum
         bool ok = true;
         for (int j = 0; mine && j < nt; ++j) {
@@ -325,7 +357,8 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // (a whole prefix tile needs none; the last, partial prefix tile keys
             // below the prefix length; a tree tile the row's ancestor bits)
             const bool is_tree = (j >= nprefix);
-            const int lim = is_tree ? (n + 1 - (j - nprefix) * BN) : (P - (t_begin + j) * BN);
+            const int a0 = (tree_first + j - nprefix) * BN;
+            const int lim = is_tree ? (n + 1 - a0) : (P - (t_begin + j) * BN);
             const bool key_r_valid = r < lim;
             const bool full = !is_tree && lim >= BN;
             uint32_t vm[4];
@@ -335,14 +368,9 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 vm[c] = rem >= 32 ? ~0u : (rem <= 0 ? 0u : ((1u << rem) - 1u));
             }
             if (is_tree) {
-                const int a0 = (j - nprefix) * BN;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int wi = (a0 >> 5) + c;
-                    vm[c] &= (row_valid && wi < p.W)
-                                 ? __ldg(&p.anc_mask[((size_t)b * R + u) * p.W + wi])
-                                 : 0u;
-                }
+                for (int c = 0; c < 4; ++c) vm[c] &= am[c];
+                if (j + 1 < nt) fetch_mask(tree_first + j + 1 - nprefix);
             }
             // ---- pass 1: row max, 32 columns at a time, four independent chains ----
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -468,6 +496,14 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 p.lse[((size_t)b * R + u) * p.Hq + hh] =
                     live ? (M + __log2f(Ls)) * 0.6931471805599453f : -INFINITY;
         };
+        auto store_zero = [&]() {
+            float z[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) z[i] = 0.f;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) store32(c, z, 0.f);
+            store_lse(false, 0.f, 0.f);
+        };
         if (splits == 1) {
             if (have) {
                 const bool live = row_valid && l > 0.f;
@@ -479,34 +515,98 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     tmem_ld_wait();
                     float v[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(t[i]);
+                    for (int i = 0; i < 32; ++i) v[i] = live ? __uint_as_float(t[i]) : 0.f;
                     if (row_out) store32(c, v, inv);
                 }
                 if (row_out) store_lse(live, m_run, l);
-            } else if (all_ok && row_out && split == 0) {  // a tile of padding rows
-                float z[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) z[i] = 0.f;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) store32(c, z, 0.f);
-                store_lse(false, 0.f, 0.f);
+            } else if (all_ok && row_out) {  // a tile of padding rows
+                store_zero();
             }
-        } else if (have) {
-            // This split's partial, unnormalised, into its own shared memory (Q and
-            // K/V stages are free: every MMA has completed): O as fp32 [D][256 rows],
-            // then m and l as [2][256 rows].
-            float* part = reinterpret_cast<float*>(base);
-            const int row2 = k * BM + r;
+        } else if (p.merge == kMergeCluster) {
+            if (have) {
+                // This split's partial, unnormalised, into its own shared memory (Q
+                // and K/V stages are free: every MMA has completed): O as fp32
+                // float4 groups [D/4][256 rows], then m and l as [2][256 rows].
+                float4* part = reinterpret_cast<float4*>(base);
+                const int row2 = k * BM + r;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t t[32];
-                tmem_ld32(tm_o + c * 32, t);
-                tmem_ld_wait();
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t t[32];
+                    tmem_ld32(tm_o + c * 32, t);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) part[(c * 32 + i) * 2 * BM + row2] = __uint_as_float(t[i]);
+                    for (int i = 0; i < 8; ++i)
+                        part[(c * 8 + i) * 2 * BM + row2] =
+                            make_float4(__uint_as_float(t[4 * i]), __uint_as_float(t[4 * i + 1]),
+                                        __uint_as_float(t[4 * i + 2]), __uint_as_float(t[4 * i + 3]));
+                }
+                float* ml = reinterpret_cast<float*>(part + (D / 4) * 2 * BM);
+                ml[row2] = m_run;
+                ml[2 * BM + row2] = l;
             }
-            part[D * 2 * BM + row2] = m_run;
-            part[(D + 1) * 2 * BM + row2] = l;
+        } else {
+            // Global merge: partial O / l as bf16 pairs [D/2][128] plus (m, l) in
+            // fp32; the last split of the unit (atomic ticket) merges them.
+            const size_t tslot = ((size_t)(b * p.Hkv + g) * p.mtiles + mt0 + k) * p.smax;
+            if (have) {
+                uint32_t* po = p.part_o + (tslot + split) * (D / 2) * BM;
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t t[32];
+                    tmem_ld32(tm_o + c * 32, t);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        po[(c * 16 + i) * BM + r] = pack_bf16x2(__uint_as_float(t[2 * i]) * inv,
+                                                                __uint_as_float(t[2 * i + 1]) * inv);
+                }
+                p.part_ml[(tslot + split) * 2 * BM + r] = m_run;
+                p.part_ml[(tslot + split) * 2 * BM + BM + r] = l;
+                __threadfence();
+            }
+            softmax_bar();
+            if (tid == 64)
+                s_last = all_ok && ticket_is_last(&p.tickets[(b * p.Hkv + g) * p.mpairs + mpair],
+                                                  (unsigned)splits);
+            softmax_bar();
+            if (s_last && mine) {
+                // out = sum_s w_s o_s / sum_s w_s, w_s = l_s 2^(m_s - M)
+                float M = -INFINITY;
+                for (int s2 = 0; s2 < splits; ++s2)
+                    M = fmaxf(M, __ldcg(&p.part_ml[(tslot + s2) * 2 * BM + r]));
+                const float mref = (M == -INFINITY) ? 0.f : M;
+                float Ls = 0.f;
+                for (int s2 = 0; s2 < splits; ++s2)
+                    Ls += __ldcg(&p.part_ml[(tslot + s2) * 2 * BM + BM + r]) *
+                          fast_exp2(__ldcg(&p.part_ml[(tslot + s2) * 2 * BM + r]) - mref);
+                const bool live = row_valid && Ls > 0.f;
+                const float inv = live ? 1.f / Ls : 0.f;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+#pragma unroll 2
+                    for (int s2 = 0; live && s2 < splits; ++s2) {
+                        const size_t sl = tslot + s2;
+                        const float w = __ldcg(&p.part_ml[sl * 2 * BM + BM + r]) *
+                                        fast_exp2(__ldcg(&p.part_ml[sl * 2 * BM + r]) - mref);
+                        const uint32_t* q = p.part_o + sl * (D / 2) * BM + (size_t)(c * 16) * BM + r;
+                        uint32_t x[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) x[i] = __ldcg(&q[i * BM]);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            v[2 * i] += w * __uint_as_float(x[i] << 16);
+                            v[2 * i + 1] += w * __uint_as_float(x[i] & 0xffff0000u);
+                        }
+                    }
+                    if (row_out) store32(c, v, inv);
+                }
+                if (row_out) store_lse(live, M, Ls);
+            }
+            if (all_ok && !mine && row_out && split == 0) store_zero();  // padding tile
         }
         tc_fence_before();
     }
@@ -514,11 +614,12 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // ---- teardown: every thread arrives here (all waits are bounded) -------------
     tc_fence_before();
     __syncthreads();
-    if (p.smax > 1) {
+    if (p.merge == kMergeCluster) {
         cluster_sync();  // every split's partial is in its shared memory
         if (splits > 1 && warp >= 2) {
-            // Merge: this CTA writes head-dimension columns [8 c_lo, 8 c_hi) of all
-            // rows of both tiles.  out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+            // This CTA writes head-dimension columns [8 c_lo, 8 c_hi) of every row
+            // of both tiles: out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,
+            // reading the peers' partials through distributed shared memory.
             const int k = (warp - 2) >> 2;
             const int r = (warp & 3) * 32 + lane;
             const int row2 = k * BM + r;
@@ -529,21 +630,16 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const bool row_valid = mine && u <= n;
             constexpr int nch = D / 8;
             const int c_lo = split * nch / splits, c_hi = (split + 1) * nch / splits;
-            uint4* dst = (uint4*)(p.out + (((size_t)b * R + u) * p.Hq + hh) * D);
+            const uint32_t own_o = smem_u32(base) + (uint32_t)row2 * 16u;
+            const uint32_t own_ml = smem_u32(base) + (uint32_t)(D / 4) * 2 * BM * 16 + (uint32_t)row2 * 4u;
             float M = -INFINITY, Ls = 0.f;
             float w[kMaxSplits];
-            uint32_t pb[kMaxSplits];
             if (row_valid) {
-                const uint32_t own = smem_u32(base) + (uint32_t)row2 * 4u;
                 float ms[kMaxSplits];
 #pragma unroll
                 for (int s2 = 0; s2 < kMaxSplits; ++s2) {
-                    pb[s2] = own;
                     ms[s2] = -INFINITY;
-                    if (s2 < splits) {
-                        pb[s2] = mapa_shared(own, (uint32_t)s2);
-                        ms[s2] = ld_dsmem_f32(pb[s2] + (uint32_t)(D * 2 * BM) * 4u);
-                    }
+                    if (s2 < splits) ms[s2] = ld_dsmem_f32(mapa_shared(own_ml, (uint32_t)s2));
                     M = fmaxf(M, ms[s2]);
                 }
                 const float mref = (M == -INFINITY) ? 0.f : M;
@@ -552,13 +648,14 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     w[s2] = 0.f;
                     if (s2 < splits) {
                         w[s2] = fast_exp2(ms[s2] - mref);
-                        Ls += w[s2] * ld_dsmem_f32(pb[s2] + (uint32_t)((D + 1) * 2 * BM) * 4u);
+                        Ls += w[s2] * ld_dsmem_f32(mapa_shared(own_ml + 2 * BM * 4, (uint32_t)s2));
                     }
                 }
             }
             const bool live = row_valid && Ls > 0.f;
             const float inv = live ? 1.f / Ls : 0.f;
             if (row_out) {
+                uint4* dst = (uint4*)(p.out + (((size_t)b * R + u) * p.Hq + hh) * D);
 #pragma unroll 1
                 for (int c = c_lo; c < c_hi; ++c) {
                     float acc[8];
@@ -566,14 +663,31 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
                     if (live) {
 #pragma unroll
-                        for (int s2 = 0; s2 < kMaxSplits; ++s2) {
-                            if (s2 < splits) {
-                                float x[8];
+                        for (int s0 = 0; s0 < kMaxSplits; s0 += 4) {
+                            if (s0 < splits) {
+                                float4 x[4][2];
 #pragma unroll
-                                for (int i = 0; i < 8; ++i)
-                                    x[i] = ld_dsmem_f32(pb[s2] + (uint32_t)((c * 8 + i) * 2 * BM) * 4u);
+                                for (int i = 0; i < 4; ++i) {
+                                    x[i][0] = x[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                                    if (s0 + i < splits) {
+                                        const uint32_t a = mapa_shared(
+                                            own_o + (uint32_t)(2 * c) * 2 * BM * 16, (uint32_t)(s0 + i));
+                                        x[i][0] = ld_dsmem_f32x4(a);
+                                        x[i][1] = ld_dsmem_f32x4(a + 2 * BM * 16);
+                                    }
+                                }
 #pragma unroll
-                                for (int i = 0; i < 8; ++i) acc[i] = fmaf(w[s2], x[i], acc[i]);
+                                for (int i = 0; i < 4; ++i) {
+                                    const float ws = w[s0 + i];
+                                    acc[0] = fmaf(ws, x[i][0].x, acc[0]);
+                                    acc[1] = fmaf(ws, x[i][0].y, acc[1]);
+                                    acc[2] = fmaf(ws, x[i][0].z, acc[2]);
+                                    acc[3] = fmaf(ws, x[i][0].w, acc[3]);
+                                    acc[4] = fmaf(ws, x[i][1].x, acc[4]);
+                                    acc[5] = fmaf(ws, x[i][1].y, acc[5]);
+                                    acc[6] = fmaf(ws, x[i][1].z, acc[6]);
+                                    acc[7] = fmaf(ws, x[i][1].w, acc[7]);
+                                }
                             }
                         }
                     }
@@ -625,7 +739,7 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_
 }
 
 struct Plan {
-    int mtiles, mpairs, tps, smax;
+    int mtiles, mpairs, tps, smax, merge;
 };
 
 // Streaming multiprocessors of the current device (148 if the query fails).
@@ -642,80 +756,126 @@ int num_sms() {
     return cached[dev];
 }
 
-// Split the prefix of each (sequence, KV head, pair of query tiles) unit into
-// KV splits of `tps` tiles; the splits of a unit form one cluster of at most
-// kMaxSplits CTAs and merge on chip.  Few units: split until one wave of CTAs
-// (one per SM) is full, keeping at least 2 tiles in a split.  Many units: cap a
-// split at a quarter of the longest prefix so that long sequences of a ragged
-// batch do not leave a tail of lone CTAs.
-Plan make_plan(int B, int N, int Hq, int Hkv, int64_t cache_cap, int max_splits) {
-    Plan pl;
+// Per-unit tile counts bounding a plan: the longest prefix and the largest tree.
+struct Tiles {
+    int prefix, tree;
+};
+Tiles max_tiles(int N, int64_t cache_cap) {
+    return {(int)((cache_cap + BN - 1) / BN), (N + 1 + BN - 1) / BN};
+}
+
+Plan plan_base(int N, int Hq, int Hkv) {
+    Plan pl{};
     const int G = Hq / Hkv;
     pl.mtiles = ((N + 1) * G + BM - 1) / BM;
     pl.mpairs = (pl.mtiles + 1) / 2;
-    const int max_tiles = (int)((cache_cap + BN - 1) / BN);
-    const long units = (long)B * Hkv * pl.mpairs;
-    const int sms = num_sms();
-    if (max_tiles <= 1) {
-        pl.tps = 1;
-    } else if (units < sms) {
-        const long cap = std::min<long>(max_splits, (max_tiles + 1) / 2);
-        const int splits = (int)std::max(1L, std::min<long>(sms / units, cap));
-        pl.tps = (max_tiles + splits - 1) / splits;
-    } else {
-        pl.tps = max_tiles > 64 ? std::max(32, (max_tiles + 3) / 4) : max_tiles;
-    }
-    pl.tps = std::max(pl.tps, (max_tiles + max_splits - 1) / max_splits);
-    pl.smax = max_tiles > 0 ? (max_tiles + pl.tps - 1) / pl.tps : 1;
     return pl;
 }
 
-// Largest cluster (<= kMaxSplits CTAs, halving) that the device can co-schedule
-// with this kernel's shared memory; 1 if none.  Needs the kernel's dynamic
-// shared-memory attribute set first.
+long plan_units(const Plan& pl, int B, int Hkv) { return (long)B * Hkv * pl.mpairs; }
+
+// Many units fill the GPU without clusters: split only long tile lists, at a
+// quarter of the longest (so that long sequences of a ragged batch do not leave
+// a tail of lone CTAs), and merge through the workspace.
+Plan plan_many(const Plan& base, Tiles t) {
+    Plan pl = base;
+    const int T = t.prefix + t.tree;
+    pl.tps = T > 64 ? std::max(32, (T + 3) / 4) : T;
+    pl.smax = (T + pl.tps - 1) / pl.tps;
+    pl.merge = pl.smax > 1 ? kMergeGlobal : kMergeNone;
+    return pl;
+}
+
+// Few units: split each unit's tiles over a cluster of S CTAs, with the fewest
+// tiles per split (at least 2) for which every unit's cluster is resident at
+// once: units x S CTAs within one wave, and the device able to co-schedule that
+// many clusters of S (active(S) reports how many it can).
+template <typename Active>
+Plan plan_few(const Plan& base, Tiles t, long units, int sms, Active active) {
+    Plan pl = base;
+    const int T = t.prefix + t.tree;
+    pl.tps = T;
+    for (int tps = 2; tps < T; ++tps) {
+        const int S = (T + tps - 1) / tps;
+        if (S > kMaxSplits || units * S > sms) continue;
+        if (active(S) < units) continue;
+        pl.tps = tps;
+        break;
+    }
+    pl.smax = (T + pl.tps - 1) / pl.tps;
+    pl.merge = pl.smax > 1 ? kMergeCluster : kMergeNone;
+    return pl;
+}
+
+struct WsLayout {
+    size_t tickets, part_o, part_ml, total;
+};
+
+// Workspace of the global merge (empty for the other plans).
+WsLayout attn_layout(const Plan& pl, int B, int Hkv, int D) {
+    WsLayout w{};
+    if (pl.merge != kMergeGlobal) return w;
+    const size_t tiles = (size_t)B * Hkv * pl.mtiles;  // partials per query tile
+    w.tickets = 0;  // one counter per (sequence, KV head, tile pair)
+    w.part_o = align_up((size_t)B * Hkv * pl.mpairs * 4, 256);
+    w.part_ml = align_up(w.part_o + tiles * pl.smax * (size_t)D * BM * 2, 256);
+    w.total = align_up(w.part_ml + tiles * pl.smax * 2 * BM * 4, 256);
+    return w;
+}
+
+// Co-resident clusters of `size` CTAs of tree_attn_kernel<D> on device `dev`
+// (0 if that size cannot launch).  Needs the kernel's attributes set first.
 template <int D>
-int cluster_cap(int dev) {
-    static int cached[64];
-    int& c = cached[dev & 63];
-    if (!c) {
-        int cap = 1;
-        for (int size = kMaxSplits; size >= 2; size /= 2) {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((unsigned)size);
-            cfg.blockDim = dim3(kThreads);
-            cfg.dynamicSmemBytes = Cfg<D>::SMEM;
-            cudaLaunchAttribute at;
-            at.id = cudaLaunchAttributeClusterDimension;
-            at.val.clusterDim.x = (unsigned)size;
-            at.val.clusterDim.y = 1;
-            at.val.clusterDim.z = 1;
-            cfg.attrs = &at;
-            cfg.numAttrs = 1;
-            int active = 0;
-            if (cudaOccupancyMaxActiveClusters(&active, tree_attn_kernel<D>, &cfg) == cudaSuccess &&
-                active > 0) {
-                cap = size;
-                break;
-            }
+int active_clusters(int dev, int size) {
+    static int cached[64][kMaxSplits + 1];
+    static bool done[64][kMaxSplits + 1];
+    if (size < 1 || size > kMaxSplits) return 0;
+    if (!done[dev & 63][size]) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)size);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = Cfg<D>::SMEM;
+        cudaLaunchAttribute at;
+        at.id = cudaLaunchAttributeClusterDimension;
+        at.val.clusterDim.x = (unsigned)size;
+        at.val.clusterDim.y = 1;
+        at.val.clusterDim.z = 1;
+        cfg.attrs = &at;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, tree_attn_kernel<D>, &cfg) != cudaSuccess) {
+            n = 0;
             (void)cudaGetLastError();  // a refused size is not an error of the call
         }
-        c = cap;
+        cached[dev & 63][size] = n;
+        done[dev & 63][size] = true;
     }
-    return c;
+    return cached[dev & 63][size];
 }
 
 template <int D>
 cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
     static std::once_flag once[64];
+    static cudaError_t attr_err[64];
     int dev = 0;
     cudaGetDevice(&dev);
-    cudaError_t attr_err = cudaSuccess;
     std::call_once(once[dev & 63], [&] {
-        attr_err = cudaFuncSetAttribute(tree_attn_kernel<D>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(tree_attn_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(tree_attn_kernel<D>,
+                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        attr_err[dev & 63] = e;
     });
-    if (attr_err != cudaSuccess) return attr_err;
-    const Plan pl = make_plan(a.B, a.N, a.Hq, a.Hkv, a.cache_cap, cluster_cap<D>(dev));
+    if (attr_err[dev & 63] != cudaSuccess) return attr_err[dev & 63];
+    const Plan base = plan_base(a.N, a.Hq, a.Hkv);
+    const Tiles t = max_tiles(a.N, a.cache_cap);
+    const long units = plan_units(base, a.B, a.Hkv);
+    const int sms = num_sms();
+    const Plan pl = units >= sms ? plan_many(base, t)
+                                 : plan_few(base, t, units, sms,
+                                            [&](int S) { return active_clusters<D>(dev, S); });
+    const WsLayout wl = attn_layout(pl, a.B, a.Hkv, D);
     const int G = a.Hq / a.Hkv, R = a.N + 1;
     CUtensorMap mq, mkc, mvc, mkt, mvt;
     const uint64_t rowb = (uint64_t)D * 2;
@@ -733,21 +893,32 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
     p.anc_mask = a.anc_mask;
     p.out = (uint16_t*)a.out;
     p.lse = a.lse;
+    char* ws = (char*)a.ws;
+    const bool glob = pl.merge == kMergeGlobal;
+    p.tickets = glob ? (unsigned int*)(ws + wl.tickets) : nullptr;
+    p.part_o = glob ? (uint32_t*)(ws + wl.part_o) : nullptr;
+    p.part_ml = glob ? (float*)(ws + wl.part_ml) : nullptr;
     p.B = a.B; p.N = a.N; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.W = (a.N + 1 + 31) / 32;
     p.mtiles = pl.mtiles; p.mpairs = pl.mpairs; p.tps = pl.tps; p.smax = pl.smax;
+    p.merge = pl.merge;
     p.cache_cap = a.cache_cap;
     p.scale_log2 = a.scale * kLog2e;
     p.err = a.err;
-    const long grid = (long)a.B * a.Hkv * pl.mpairs * pl.smax;
+    const long grid = units * pl.smax;
     return launch_pdl_cluster(tree_attn_kernel<D>, dim3((unsigned)grid), dim3(kThreads),
-                              (size_t)Cfg<D>::SMEM, s, (unsigned)pl.smax, mq, mkc, mvc, mkt, mvt,
-                              p);
+                              (size_t)Cfg<D>::SMEM, s,
+                              pl.merge == kMergeCluster ? (unsigned)pl.smax : 1u, mq, mkc, mvc,
+                              mkt, mvt, p);
 }
 
 }  // namespace
 
-// The KV splits merge through distributed shared memory: no workspace.
-size_t attn_workspace_bytes(int, int, int, int, int, int64_t) { return 0; }
+// Only plans for many units (no clusters) merge their KV splits in a workspace.
+size_t attn_workspace_bytes(int B, int N, int Hq, int Hkv, int D, int64_t cache_cap) {
+    const Plan base = plan_base(N, Hq, Hkv);
+    if (plan_units(base, B, Hkv) < num_sms()) return 0;
+    return attn_layout(plan_many(base, max_tiles(N, cache_cap)), B, Hkv, D).total;
+}
 
 cudaError_t launch_tree_attn(const AttnArgs& a, cudaStream_t s) {
     if (a.D == 128) return launch_d<128>(a, s);

@@ -172,11 +172,11 @@ ddtree_status ddtree_build_heap(const float* topk_logp, const int32_t* topk_idx,
  *   every device pointer 16-byte aligned.
  * Outputs: out bf16 [B][N+1][Hq][D] (rows past n_nodes are zero);
  *          lse fp32 [B][N+1][Hq] (nullable; natural-log sum of exps, -inf past n).
- * Workspace: none at present -- the KV splits of a (sequence, KV head) unit run
- * as one thread-block cluster and merge their partial results in on-chip
- * shared memory; ddtree_workspace_size(DDTREE_OP_TREE_ATTN, ...) returns 0 and
- * `workspace` may be NULL.  The arguments stay so that a future layout may use
- * one. */
+ * Workspace: ddtree_workspace_size(DDTREE_OP_TREE_ATTN, ...), which is 0 (and
+ * `workspace` may be NULL) when the problem has fewer (sequence, KV head,
+ * query-tile pair) units than the GPU has SMs: the KV splits of a unit then run
+ * as one thread-block cluster and merge in on-chip shared memory.  Larger
+ * batches merge their splits through the workspace. */
 ddtree_status ddtree_tree_attn(const void* q, const void* k_cache, const void* v_cache,
                                int64_t cache_cap, const void* k_tree, const void* v_tree,
                                const int32_t* prefix_len, const int32_t* n_nodes,
