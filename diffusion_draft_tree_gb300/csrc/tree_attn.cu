@@ -58,8 +58,8 @@ struct Cfg {
     static constexpr int KV_BYTES = NH * kHalfBytes;  // one K (or V) tile
     static constexpr int NS = (D == 128) ? 2 : 3;
     static constexpr int SMEM = 1024 + 2 * QT_BYTES + NS * 2 * KV_BYTES;
-    // a split's partial (fp32 O of both tiles, then m and l) reuses Q and K/V
-    static_assert((D + 2) * 2 * BM * 4 <= SMEM - 1024, "partial fits in shared memory");
+    // a split's partial (bf16 O / l of both tiles, then m and l) reuses Q and K/V
+    static_assert((D * 2 + 8) * 2 * BM <= SMEM - 1024, "partial fits in shared memory");
 };
 
 struct Params {
@@ -524,25 +524,26 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
         } else if (p.merge == kMergeCluster) {
             if (have) {
-                // This split's partial, unnormalised, into its own shared memory (Q
-                // and K/V stages are free: every MMA has completed): O as fp32
-                // float4 groups [D/4][256 rows], then m and l as [2][256 rows].
-                float4* part = reinterpret_cast<float4*>(base);
+                // This split's partial into its own shared memory (Q and K/V stages
+                // are free: every MMA has completed): O / l as bf16, 8 columns per
+                // 16-byte group, [D/8][256 rows]; then (m, l) as float2 [256 rows].
+                uint4* part = reinterpret_cast<uint4*>(base);
                 const int row2 = k * BM + r;
+                const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t t[32];
                     tmem_ld32(tm_o + c * 32, t);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        part[(c * 8 + i) * 2 * BM + row2] =
-                            make_float4(__uint_as_float(t[4 * i]), __uint_as_float(t[4 * i + 1]),
-                                        __uint_as_float(t[4 * i + 2]), __uint_as_float(t[4 * i + 3]));
+                    for (int i = 0; i < 4; ++i)
+                        part[(c * 4 + i) * 2 * BM + row2] = make_uint4(
+                            pack_bf16x2(__uint_as_float(t[8 * i]) * inv, __uint_as_float(t[8 * i + 1]) * inv),
+                            pack_bf16x2(__uint_as_float(t[8 * i + 2]) * inv, __uint_as_float(t[8 * i + 3]) * inv),
+                            pack_bf16x2(__uint_as_float(t[8 * i + 4]) * inv, __uint_as_float(t[8 * i + 5]) * inv),
+                            pack_bf16x2(__uint_as_float(t[8 * i + 6]) * inv, __uint_as_float(t[8 * i + 7]) * inv));
                 }
-                float* ml = reinterpret_cast<float*>(part + (D / 4) * 2 * BM);
-                ml[row2] = m_run;
-                ml[2 * BM + row2] = l;
+                reinterpret_cast<float2*>(part + (D / 8) * 2 * BM)[row2] = make_float2(m_run, l);
             }
         } else {
             // Global merge: partial O / l as bf16 pairs [D/2][128] plus (m, l) in
@@ -618,8 +619,9 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         cluster_sync();  // every split's partial is in its shared memory
         if (splits > 1 && warp >= 2) {
             // This CTA writes head-dimension columns [8 c_lo, 8 c_hi) of every row
-            // of both tiles: out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,
-            // reading the peers' partials through distributed shared memory.
+            // of both tiles: out = sum_s w_s o_s / sum_s w_s with o_s = O_s / l_s
+            // and w_s = l_s 2^(m_s - M), reading the peers' partials through
+            // distributed shared memory.
             const int k = (warp - 2) >> 2;
             const int r = (warp & 3) * 32 + lane;
             const int row2 = k * BM + r;
@@ -631,25 +633,23 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             constexpr int nch = D / 8;
             const int c_lo = split * nch / splits, c_hi = (split + 1) * nch / splits;
             const uint32_t own_o = smem_u32(base) + (uint32_t)row2 * 16u;
-            const uint32_t own_ml = smem_u32(base) + (uint32_t)(D / 4) * 2 * BM * 16 + (uint32_t)row2 * 4u;
+            const uint32_t own_ml = smem_u32(base) + (uint32_t)nch * 2 * BM * 16 + (uint32_t)row2 * 8u;
+            // Peer loads are unconditional (ranks past the last split re-read it
+            // with weight 0) so that each group of them is in flight together.
             float M = -INFINITY, Ls = 0.f;
             float w[kMaxSplits];
             if (row_valid) {
-                float ms[kMaxSplits];
+                float2 ml[kMaxSplits];
 #pragma unroll
-                for (int s2 = 0; s2 < kMaxSplits; ++s2) {
-                    ms[s2] = -INFINITY;
-                    if (s2 < splits) ms[s2] = ld_dsmem_f32(mapa_shared(own_ml, (uint32_t)s2));
-                    M = fmaxf(M, ms[s2]);
-                }
+                for (int s2 = 0; s2 < kMaxSplits; ++s2)
+                    ml[s2] = ld_dsmem_f32x2(mapa_shared(own_ml, (uint32_t)min(s2, splits - 1)));
+#pragma unroll
+                for (int s2 = 0; s2 < kMaxSplits; ++s2) M = fmaxf(M, ml[s2].x);
                 const float mref = (M == -INFINITY) ? 0.f : M;
 #pragma unroll
                 for (int s2 = 0; s2 < kMaxSplits; ++s2) {
-                    w[s2] = 0.f;
-                    if (s2 < splits) {
-                        w[s2] = fast_exp2(ms[s2] - mref);
-                        Ls += w[s2] * ld_dsmem_f32(mapa_shared(own_ml + 2 * BM * 4, (uint32_t)s2));
-                    }
+                    w[s2] = s2 < splits ? ml[s2].y * fast_exp2(ml[s2].x - mref) : 0.f;
+                    Ls += w[s2];
                 }
             }
             const bool live = row_valid && Ls > 0.f;
@@ -662,31 +662,23 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
                     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
                     if (live) {
+                        const uint32_t oc = own_o + (uint32_t)c * 2 * BM * 16;
 #pragma unroll
-                        for (int s0 = 0; s0 < kMaxSplits; s0 += 4) {
+                        for (int s0 = 0; s0 < kMaxSplits; s0 += 8) {
                             if (s0 < splits) {
-                                float4 x[4][2];
+                                uint4 x[8];
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    x[i][0] = x[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-                                    if (s0 + i < splits) {
-                                        const uint32_t a = mapa_shared(
-                                            own_o + (uint32_t)(2 * c) * 2 * BM * 16, (uint32_t)(s0 + i));
-                                        x[i][0] = ld_dsmem_f32x4(a);
-                                        x[i][1] = ld_dsmem_f32x4(a + 2 * BM * 16);
-                                    }
-                                }
+                                for (int i = 0; i < 8; ++i)
+                                    x[i] = ld_dsmem_u32x4(mapa_shared(oc, (uint32_t)min(s0 + i, splits - 1)));
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
+                                for (int i = 0; i < 8; ++i) {
                                     const float ws = w[s0 + i];
-                                    acc[0] = fmaf(ws, x[i][0].x, acc[0]);
-                                    acc[1] = fmaf(ws, x[i][0].y, acc[1]);
-                                    acc[2] = fmaf(ws, x[i][0].z, acc[2]);
-                                    acc[3] = fmaf(ws, x[i][0].w, acc[3]);
-                                    acc[4] = fmaf(ws, x[i][1].x, acc[4]);
-                                    acc[5] = fmaf(ws, x[i][1].y, acc[5]);
-                                    acc[6] = fmaf(ws, x[i][1].z, acc[6]);
-                                    acc[7] = fmaf(ws, x[i][1].w, acc[7]);
+                                    const uint32_t q[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        acc[2 * e] = fmaf(ws, __uint_as_float(q[e] << 16), acc[2 * e]);
+                                        acc[2 * e + 1] = fmaf(ws, __uint_as_float(q[e] & 0xffff0000u), acc[2 * e + 1]);
+                                    }
                                 }
                             }
                         }
