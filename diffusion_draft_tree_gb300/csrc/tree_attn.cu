@@ -634,22 +634,27 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int c_lo = split * nch / splits, c_hi = (split + 1) * nch / splits;
             const uint32_t own_o = smem_u32(base) + (uint32_t)row2 * 16u;
             const uint32_t own_ml = smem_u32(base) + (uint32_t)nch * 2 * BM * 16 + (uint32_t)row2 * 8u;
-            // Peer loads are unconditional (ranks past the last split re-read it
-            // with weight 0) so that each group of them is in flight together.
+            // Peers are visited starting at this CTA's own rank, so that at any
+            // moment each CTA's shared memory serves one reader.
             float M = -INFINITY, Ls = 0.f;
             float w[kMaxSplits];
             if (row_valid) {
                 float2 ml[kMaxSplits];
 #pragma unroll
-                for (int s2 = 0; s2 < kMaxSplits; ++s2)
-                    ml[s2] = ld_dsmem_f32x2(mapa_shared(own_ml, (uint32_t)min(s2, splits - 1)));
+                for (int i = 0; i < kMaxSplits; ++i) {
+                    ml[i] = make_float2(-INFINITY, 0.f);
+                    if (i < splits) {
+                        const int s2 = (split + i) % splits;
+                        ml[i] = ld_dsmem_f32x2(mapa_shared(own_ml, (uint32_t)s2));
+                    }
+                }
 #pragma unroll
-                for (int s2 = 0; s2 < kMaxSplits; ++s2) M = fmaxf(M, ml[s2].x);
+                for (int i = 0; i < kMaxSplits; ++i) M = fmaxf(M, ml[i].x);
                 const float mref = (M == -INFINITY) ? 0.f : M;
 #pragma unroll
-                for (int s2 = 0; s2 < kMaxSplits; ++s2) {
-                    w[s2] = s2 < splits ? ml[s2].y * fast_exp2(ml[s2].x - mref) : 0.f;
-                    Ls += w[s2];
+                for (int i = 0; i < kMaxSplits; ++i) {
+                    w[i] = i < splits ? ml[i].y * fast_exp2(ml[i].x - mref) : 0.f;
+                    Ls += w[i];
                 }
             }
             const bool live = row_valid && Ls > 0.f;
@@ -668,8 +673,12 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             if (s0 < splits) {
                                 uint4 x[8];
 #pragma unroll
-                                for (int i = 0; i < 8; ++i)
-                                    x[i] = ld_dsmem_u32x4(mapa_shared(oc, (uint32_t)min(s0 + i, splits - 1)));
+                                for (int i = 0; i < 8; ++i) {
+                                    x[i] = make_uint4(0u, 0u, 0u, 0u);
+                                    if (s0 + i < splits)
+                                        x[i] = ld_dsmem_u32x4(
+                                            mapa_shared(oc, (uint32_t)((split + s0 + i) % splits)));
+                                }
 #pragma unroll
                                 for (int i = 0; i < 8; ++i) {
                                     const float ws = w[s0 + i];
