@@ -25,6 +25,7 @@ enum : uint32_t {
     ERR_BAD_TREE = 0x3,
     ERR_WAIT_TIMEOUT = 0x4,
     ERR_BAD_INPUT = 0x5,
+    ERR_PLAN = 0x6,  // a launch plan the kernel cannot carry out (a library bug)
 };
 
 DDT_DEV void record_error(uint32_t* err, uint32_t code) {

@@ -192,6 +192,16 @@ DDT_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: 
 DDT_DEV void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
+// Copy engine: `bytes` (a multiple of 16, both addresses 16-byte aligned) from
+// this CTA's shared memory to a peer's (dst and the peer's mbarrier given as
+// cluster-window addresses); completes as transaction bytes on that mbarrier.
+DDT_DEV void bulk_copy_s2s(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                           uint32_t mbar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst_cluster), "r"(src_cta), "r"(bytes), "r"(mbar_cluster)
+        : "memory");
+}
 // Address, in the cluster's shared window, of `saddr` in the CTA of rank `rank`.
 DDT_DEV uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
     uint32_t r;

@@ -58,8 +58,22 @@ struct Cfg {
     static constexpr int KV_BYTES = NH * kHalfBytes;  // one K (or V) tile
     static constexpr int NS = (D == 128) ? 2 : 3;
     static constexpr int SMEM = 1024 + 2 * QT_BYTES + NS * 2 * KV_BYTES;
-    // a split's partial (bf16 O / l of both tiles, then m and l) reuses Q and K/V
-    static_assert((D * 2 + 8) * 2 * BM <= SMEM - 1024, "partial fits in shared memory");
+    // Cluster merge: a split's partial O / l (bf16, both tiles) fills the Q
+    // region; its (m, l) rows take the last ML_BYTES of the K/V region, the rest
+    // of which receives the peers' slices.
+    static constexpr int ML_BYTES = 2 * BM * 8;
+    static constexpr int RECV_BYTES = NS * 2 * KV_BYTES - ML_BYTES;
+    static_assert(D * 2 * 2 * BM == 2 * QT_BYTES, "partial O fills the Q region");
+    // Whether a unit of S splits can receive its slices ...
+    static constexpr bool recv_fits(int S) {
+        return S * (((D / 8 + S - 1) / S) * 2 * BM * 16 + ML_BYTES) <= RECV_BYTES;
+    }
+    // ... and every unit of a cluster of S (a short sequence uses fewer splits).
+    static constexpr bool recv_fits_upto(int S) {
+        for (int s = 2; s <= S; ++s)
+            if (!recv_fits(s)) return false;
+        return true;
+    }
 };
 
 struct Params {
@@ -137,7 +151,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     constexpr int NS = C::NS;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_q, bar_full[NS], bar_empty[NS], bar_sfull[2],
-        bar_pfull[2], bar_odone[2];
+        bar_pfull[2], bar_odone[2], bar_recv;
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
     __shared__ bool s_last;
@@ -156,6 +170,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             mbar_init(&bar_pfull[k], 128);
             mbar_init(&bar_odone[k], 1);
         }
+        mbar_init(&bar_recv, 1);
         s_abort = 0;
         mbar_init_fence();
         tma_prefetch_desc(&tm_q);
@@ -372,21 +387,27 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 for (int c = 0; c < 4; ++c) vm[c] &= am[c];
                 if (j + 1 < nt) fetch_mask(tree_first + j + 1 - nprefix);
             }
-            // ---- pass 1: row max, 32 columns at a time, four independent chains ----
+            // ---- pass 1: row max, 64 columns per TMEM wait, four independent chains ----
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c0 = 0; c0 < 4; ++c0) {
-                uint32_t t[32];
+            for (int c0 = 0; c0 < 4; c0 += 2) {
+                uint32_t t[32], t2[32];
                 tmem_ld32(tm_s + 32 * c0, t);
+                tmem_ld32(tm_s + 32 * c0 + 32, t2);
                 tmem_ld_wait();
                 if (full) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(t[i]));
+                    for (int i = 0; i < 32; ++i) {
+                        mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(t[i]));
+                        mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(t2[i]));
+                    }
                 } else {
-                    const uint32_t m = vm[c0];
+                    const uint32_t m = vm[c0], m2 = vm[c0 + 1];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
+                    for (int i = 0; i < 32; ++i) {
                         mx[i & 3] = fmaxf(mx[i & 3], ((m >> i) & 1u) ? __uint_as_float(t[i]) : -INFINITY);
+                        mx[i & 3] = fmaxf(mx[i & 3], ((m2 >> i) & 1u) ? __uint_as_float(t2[i]) : -INFINITY);
+                    }
                 }
             }
             const float mt_raw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
@@ -543,8 +564,9 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             pack_bf16x2(__uint_as_float(t[8 * i + 4]) * inv, __uint_as_float(t[8 * i + 5]) * inv),
                             pack_bf16x2(__uint_as_float(t[8 * i + 6]) * inv, __uint_as_float(t[8 * i + 7]) * inv));
                 }
-                reinterpret_cast<float2*>(part + (D / 8) * 2 * BM)[row2] = make_float2(m_run, l);
+                reinterpret_cast<float2*>(sk + C::RECV_BYTES)[row2] = make_float2(m_run, l);
             }
+            fence_proxy_async_smem();  // the partial leaves by bulk copy (async proxy)
         } else {
             // Global merge: partial O / l as bf16 pairs [D/2][128] plus (m, l) in
             // fp32; the last split of the unit (atomic ticket) merges them.
@@ -616,93 +638,108 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     tc_fence_before();
     __syncthreads();
     if (p.merge == kMergeCluster) {
-        cluster_sync();  // every split's partial is in its shared memory
-        if (splits > 1 && warp >= 2) {
-            // This CTA writes head-dimension columns [8 c_lo, 8 c_hi) of every row
-            // of both tiles: out = sum_s w_s o_s / sum_s w_s with o_s = O_s / l_s
-            // and w_s = l_s 2^(m_s - M), reading the peers' partials through
-            // distributed shared memory.
-            const int k = (warp - 2) >> 2;
-            const int r = (warp & 3) * 32 + lane;
-            const int row2 = k * BM + r;
-            const int u = (k == 0 ? u00 : u01) + r / G;
-            const int hh = g * G + r % G;
-            const bool mine = (k == 0) || has1;
-            const bool row_out = (k == 0 || tile1) && u < R;
-            const bool row_valid = mine && u <= n;
-            constexpr int nch = D / 8;
+        cluster_sync();  // every split's partial is written; every K/V stage is free
+        if (splits > 1 && !C::recv_fits(splits)) {  // the plan rules this out
+            if (tid == 0 && split == 0) record_error(p.err, ERR_ATTN | ERR_PLAN);
+        } else if (splits > 1) {
+            // Split o owns head-dimension columns [8 lo(o), 8 hi(o)).  Each CTA's
+            // copy engine sends every owner its slice of this CTA's partial and its
+            // (m, l) rows, into the owner's (now idle) K/V stages, completing on the
+            // owner's bar_recv; the owner then merges from its own shared memory:
+            // out = sum_s w_s o_s / sum_s w_s, o_s = O_s / l_s, w_s = l_s 2^(m_s - M).
+            constexpr int nch = D / 8;             // 8-column chunks of 256 rows x 16 B
+            constexpr uint32_t kChunk = 2 * BM * 16;
+            constexpr uint32_t kMl = 2 * BM * 8;
             const int c_lo = split * nch / splits, c_hi = (split + 1) * nch / splits;
-            const uint32_t own_o = smem_u32(base) + (uint32_t)row2 * 16u;
-            const uint32_t own_ml = smem_u32(base) + (uint32_t)nch * 2 * BM * 16 + (uint32_t)row2 * 8u;
-            // Peers are visited starting at this CTA's own rank, so that at any
-            // moment each CTA's shared memory serves one reader.
-            float M = -INFINITY, Ls = 0.f;
-            float w[kMaxSplits];
-            if (row_valid) {
-                float2 ml[kMaxSplits];
-#pragma unroll
-                for (int i = 0; i < kMaxSplits; ++i) {
-                    ml[i] = make_float2(-INFINITY, 0.f);
-                    if (i < splits) {
-                        const int s2 = (split + i) % splits;
-                        ml[i] = ld_dsmem_f32x2(mapa_shared(own_ml, (uint32_t)s2));
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < kMaxSplits; ++i) M = fmaxf(M, ml[i].x);
-                const float mref = (M == -INFINITY) ? 0.f : M;
-#pragma unroll
-                for (int i = 0; i < kMaxSplits; ++i) {
-                    w[i] = i < splits ? ml[i].y * fast_exp2(ml[i].x - mref) : 0.f;
-                    Ls += w[i];
+            const uint32_t slot = (uint32_t)((nch + splits - 1) / splits) * kChunk;
+            const uint32_t part_s = smem_u32(base);
+            const uint32_t ml_s = smem_u32(sk + C::RECV_BYTES);
+            const uint32_t recv_s = smem_u32(sk);
+            const uint32_t recv_ml_s = recv_s + (uint32_t)splits * slot;
+            if (tid == 0) {
+                mbar_arrive_expect_tx(&bar_recv, (uint32_t)(splits - 1) *
+                                                     ((uint32_t)(c_hi - c_lo) * kChunk + kMl));
+                for (int i = 1; i < splits; ++i) {
+                    const uint32_t o = (uint32_t)((split + i) % splits);
+                    const int lo = (int)o * nch / splits, hi = ((int)o + 1) * nch / splits;
+                    const uint32_t rbar = mapa_shared(smem_u32(&bar_recv), o);
+                    bulk_copy_s2s(mapa_shared(recv_s + (uint32_t)split * slot, o),
+                                  part_s + (uint32_t)lo * kChunk, (uint32_t)(hi - lo) * kChunk, rbar);
+                    bulk_copy_s2s(mapa_shared(recv_ml_s + (uint32_t)split * kMl, o), ml_s, kMl, rbar);
                 }
             }
-            const bool live = row_valid && Ls > 0.f;
-            const float inv = live ? 1.f / Ls : 0.f;
-            if (row_out) {
-                uint4* dst = (uint4*)(p.out + (((size_t)b * R + u) * p.Hq + hh) * D);
+            if (warp >= 2) {
+                const int k = (warp - 2) >> 2;
+                const int r = (warp & 3) * 32 + lane;
+                const int row2 = k * BM + r;
+                const int u = (k == 0 ? u00 : u01) + r / G;
+                const int hh = g * G + r % G;
+                const bool mine = (k == 0) || has1;
+                const bool row_out = (k == 0 || tile1) && u < R;
+                const bool row_valid = mine && u <= n;
+                if (!mbar_wait(&bar_recv, 0, nullptr) && lane == 0)
+                    record_error(p.err, ERR_ATTN | ERR_WAIT_TIMEOUT);
+                const float2* mls[kMaxSplits];
+                const uint4* prt[kMaxSplits];  // chunk c_lo of each split's slice
+#pragma unroll
+                for (int s2 = 0; s2 < kMaxSplits; ++s2) {
+                    const bool self = s2 == split;
+                    mls[s2] = reinterpret_cast<const float2*>(
+                        self ? sk + C::RECV_BYTES : sk + splits * slot + s2 * kMl);
+                    prt[s2] = reinterpret_cast<const uint4*>(self ? base + c_lo * kChunk
+                                                                  : sk + s2 * slot);
+                }
+                float M = -INFINITY, Ls = 0.f;
+                float w[kMaxSplits];
+                if (row_valid) {
+                    float2 ml[kMaxSplits];
+#pragma unroll
+                    for (int s2 = 0; s2 < kMaxSplits; ++s2) {
+                        ml[s2] = s2 < splits ? mls[s2][row2] : make_float2(-INFINITY, 0.f);
+                        M = fmaxf(M, ml[s2].x);
+                    }
+                    const float mref = (M == -INFINITY) ? 0.f : M;
+#pragma unroll
+                    for (int s2 = 0; s2 < kMaxSplits; ++s2) {
+                        w[s2] = s2 < splits ? ml[s2].y * fast_exp2(ml[s2].x - mref) : 0.f;
+                        Ls += w[s2];
+                    }
+                }
+                const bool live = row_valid && Ls > 0.f;
+                const float inv = live ? 1.f / Ls : 0.f;
+                if (row_out) {
+                    uint4* dst = (uint4*)(p.out + (((size_t)b * R + u) * p.Hq + hh) * D);
 #pragma unroll 1
-                for (int c = c_lo; c < c_hi; ++c) {
-                    float acc[8];
+                    for (int c = c_lo; c < c_hi; ++c) {
+                        float acc[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-                    if (live) {
-                        const uint32_t oc = own_o + (uint32_t)c * 2 * BM * 16;
+                        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+                        if (live) {
 #pragma unroll
-                        for (int s0 = 0; s0 < kMaxSplits; s0 += 8) {
-                            if (s0 < splits) {
-                                uint4 x[8];
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) {
-                                    x[i] = make_uint4(0u, 0u, 0u, 0u);
-                                    if (s0 + i < splits)
-                                        x[i] = ld_dsmem_u32x4(
-                                            mapa_shared(oc, (uint32_t)((split + s0 + i) % splits)));
-                                }
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) {
-                                    const float ws = w[s0 + i];
-                                    const uint32_t q[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+                            for (int s2 = 0; s2 < kMaxSplits; ++s2) {
+                                if (s2 < splits) {
+                                    const uint4 x = prt[s2][(c - c_lo) * 2 * BM + row2];
+                                    const uint32_t q[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
                                     for (int e = 0; e < 4; ++e) {
-                                        acc[2 * e] = fmaf(ws, __uint_as_float(q[e] << 16), acc[2 * e]);
-                                        acc[2 * e + 1] = fmaf(ws, __uint_as_float(q[e] & 0xffff0000u), acc[2 * e + 1]);
+                                        acc[2 * e] = fmaf(w[s2], __uint_as_float(q[e] << 16), acc[2 * e]);
+                                        acc[2 * e + 1] = fmaf(w[s2], __uint_as_float(q[e] & 0xffff0000u), acc[2 * e + 1]);
                                     }
                                 }
                             }
                         }
+                        dst[c] = make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                                            pack_bf16x2(acc[2] * inv, acc[3] * inv),
+                                            pack_bf16x2(acc[4] * inv, acc[5] * inv),
+                                            pack_bf16x2(acc[6] * inv, acc[7] * inv));
                     }
-                    dst[c] = make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv),
-                                        pack_bf16x2(acc[2] * inv, acc[3] * inv),
-                                        pack_bf16x2(acc[4] * inv, acc[5] * inv),
-                                        pack_bf16x2(acc[6] * inv, acc[7] * inv));
+                    if (split == 0 && p.lse)
+                        p.lse[((size_t)b * R + u) * p.Hq + hh] =
+                            live ? (M + __log2f(Ls)) * 0.6931471805599453f : -INFINITY;
                 }
-                if (split == 0 && p.lse)
-                    p.lse[((size_t)b * R + u) * p.Hq + hh] =
-                        live ? (M + __log2f(Ls)) * 0.6931471805599453f : -INFINITY;
             }
         }
-        cluster_sync();  // peers have finished reading this CTA's shared memory
+        cluster_sync();  // every copy out of this CTA's shared memory has landed
     }
     if (warp == 1) {
         tc_fence_after();
@@ -875,7 +912,9 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
     const int sms = num_sms();
     const Plan pl = units >= sms ? plan_many(base, t)
                                  : plan_few(base, t, units, sms,
-                                            [&](int S) { return active_clusters<D>(dev, S); });
+                                            [&](int S) {
+                                                return Cfg<D>::recv_fits_upto(S) ? active_clusters<D>(dev, S) : 0;
+                                            });
     const WsLayout wl = attn_layout(pl, a.B, a.Hkv, D);
     const int G = a.Hq / a.Hkv, R = a.N + 1;
     CUtensorMap mq, mkc, mvc, mkt, mvt;
