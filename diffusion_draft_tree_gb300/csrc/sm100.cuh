@@ -192,6 +192,12 @@ DDT_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: 
 DDT_DEV void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
+// The same barrier for execution order only: the arrive does not wait for this
+// thread's earlier memory operations to become visible (mbarrier initialisation
+// is published separately by fence.mbarrier_init.release.cluster).
+DDT_DEV void cluster_sync_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
 // Copy engine: `bytes` (a multiple of 16, both addresses 16-byte aligned) from
 // this CTA's shared memory to a peer's (dst and the peer's mbarrier given as
 // cluster-window addresses); completes as transaction bytes on that mbarrier.

@@ -232,8 +232,8 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     if (split >= splits) {  // no KV tiles here: only keep the cluster's barrier count
         if (p.merge == kMergeCluster) {
-            cluster_sync();
-            cluster_sync();
+            cluster_sync_relaxed();
+            cluster_sync_relaxed();
         }
         free_tmem();
         return;
@@ -638,7 +638,9 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     tc_fence_before();
     __syncthreads();
     if (p.merge == kMergeCluster) {
-        cluster_sync();  // every split's partial is written; every K/V stage is free
+        // Execution order is all that is needed: every split's partial is written
+        // and read only by its own copy engine; every K/V stage is idle.
+        cluster_sync_relaxed();
         if (splits > 1 && !C::recv_fits(splits)) {  // the plan rules this out
             if (tid == 0 && split == 0) record_error(p.err, ERR_ATTN | ERR_PLAN);
         } else if (splits > 1) {
@@ -739,7 +741,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
             }
         }
-        cluster_sync();  // every copy out of this CTA's shared memory has landed
+        cluster_sync_relaxed();  // every copy out of this CTA's shared memory has landed
     }
     if (warp == 1) {
         tc_fence_after();
