@@ -158,7 +158,9 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
             int cnt = 0;
 #pragma unroll
             for (int j = 0; j < kPairsPerThread; ++j) {
-                const int q = base + tid * kPairsPerThread + j;
+                // strided, so that a small batch spreads over all threads (the
+                // batch is sorted below, so the order of the keys is free)
+                const int q = base + j * kThreads + tid;
                 key[j] = 0ull;
                 if (q < pairs) {
                     const int pi = q / K, r = q - pi * K;

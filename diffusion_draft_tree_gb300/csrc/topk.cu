@@ -11,10 +11,11 @@
 // Top-K selection avoids per-element insertion: every warp finds tau_w, the
 // K-th largest of its 32 lane maxima (a warp bitonic sort), the CTA takes
 // tau = max_w tau_w -- a lower bound on the chunk's K-th largest value -- and
-// only elements >= tau (typically ~2K of 8K) are appended to a shared buffer.
-// Each candidate's rank is then counted by its own thread (no sort).  The last
-// CTA of a row (atomic ticket, no spinning) loads every chunk partial in
-// parallel and ranks them the same way.
+// only elements >= tau (typically ~2K of 8K) are appended to a shared buffer
+// (one shared atomic per warp), then sorted by one warp (or ranked by
+// counting when there are more than 32).  A second, PDL-chained kernel merges
+// each row's chunk partials: the K largest of the nchunks sorted lists, each
+// key ranked by binary searches in all of them, and the row's logsumexp.
 #include <mutex>
 
 #include "chunk.cuh"
@@ -63,12 +64,37 @@ DDT_DEV void cta_rank_select(const uint64_t* cand, int cnt, int K, uint64_t* sel
     }
 }
 
+// Warp-wide bitonic sort of one uint64 per lane, descending (lane 0 largest).
+DDT_DEV uint64_t warp_sort_desc_u64(uint64_t v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const uint64_t o = __shfl_xor_sync(0xffffffffu, v, j);
+            const bool keep_max = (((lane & k) == 0) == ((lane & j) == 0));
+            v = keep_max ? (v > o ? v : o) : (v < o ? v : o);
+        }
+    }
+    return v;
+}
+
+// Keys of the descending list a[0..n) that are larger than x.
+DDT_DEV int count_greater_desc(const uint64_t* a, int n, uint64_t x) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (a[mid] > x) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads)
 topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, int nchunks,
             bool aligned, int32_t* __restrict__ topk_idx, float* __restrict__ topk_logp,
-            float* __restrict__ lse, TopkPartial* __restrict__ parts,
-            unsigned int* __restrict__ tickets) {
+            float* __restrict__ lse, TopkPartial* __restrict__ parts) {
     using Chunk = SmemChunk<BF16, kChunkBytes / (BF16 ? 2 : 4)>;
     constexpr int VEC = Chunk::VEC;
     constexpr int PER = Chunk::NVEC / kThreads;  // vectors per thread
@@ -78,9 +104,7 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     __shared__ uint64_t s_sel[DDTREE_MAX_K];
     __shared__ float s_wmax[kThreads / 32], s_wsum[kThreads / 32];
     __shared__ uint32_t s_wtau[kThreads / 32];
-    __shared__ float s_m[kMaxChunks], s_s[kMaxChunks];
     __shared__ int s_cnt;
-    __shared__ bool s_last;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int chunk = blockIdx.x, row = blockIdx.y;
@@ -121,6 +145,7 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     const float off = -ref * kLog2e;
     const float tv = (tau == 0u) ? -INFINITY : float_from_ord(tau);
     float ssum = 0.f;
+    int mine = 0;  // this thread's candidates
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
         const int v = tid + i * kThreads;
@@ -131,11 +156,35 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
         for (int k = 0; k < VEC; ++k) ssum += fast_exp2(fmaf(x[k], kLog2e, off));
         if (Chunk::vmax(w) >= tv) {
 #pragma unroll
-            for (int k = 0; k < VEC; ++k) {
-                const int e = c0 + v * VEC + k;
-                if (x[k] >= tv && e < V) {
-                    const int pos = atomicAdd(&s_cnt, 1);
-                    if (pos < kCandCap) s_cand[pos] = value_index_key(x[k], (uint32_t)e);
+            for (int k = 0; k < VEC; ++k) mine += (x[k] >= tv && c0 + v * VEC + k < V) ? 1 : 0;
+        }
+    }
+    // one shared atomic per warp reserves the warp's slots
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    int wbase = 0;
+    if (lane == 31 && incl > 0) wbase = atomicAdd(&s_cnt, incl);
+    wbase = __shfl_sync(0xffffffffu, wbase, 31);
+    if (mine) {
+        int pos = wbase + incl - mine;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int v = tid + i * kThreads;
+            const uint4 w = vec[v];
+            if (Chunk::vmax(w) >= tv) {
+                float x[VEC];
+                Chunk::unpack(w, x);
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) {
+                    const int e = c0 + v * VEC + k;
+                    if (x[k] >= tv && e < V) {
+                        if (pos < kCandCap) s_cand[pos] = value_index_key(x[k], (uint32_t)e);
+                        ++pos;
+                    }
                 }
             }
         }
@@ -145,7 +194,12 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     __syncthreads();
     const int cnt = s_cnt;
 
-    if (cnt <= kCandCap) {
+    if (cnt <= 32) {
+        if (warp == 0) {
+            const uint64_t key = warp_sort_desc_u64(lane < cnt ? s_cand[lane] : 0ull);
+            if (lane < K) s_sel[lane] = key;
+        }
+    } else if (cnt <= kCandCap) {
         cta_rank_select(s_cand, cnt, K, s_sel);
     } else {
         // Degenerate ties overflowed the buffer: exact K-round selection
@@ -183,7 +237,7 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     for (int i = 0; i < kThreads / 32; ++i) S += s_wsum[i];
     float M = ref;
 
-    if (nchunks > 1) {
+    if (nchunks > 1) {  // the merge kernel finishes the row
         if (warp == 0) {
             TopkPartial* p = parts + (size_t)row * nchunks + chunk;
             if (lane < K) p->keys[lane] = s_sel[lane];
@@ -191,44 +245,69 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
                 p->m = m;
                 p->s = S;
             }
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) s_last = ticket_is_last(&tickets[row], (unsigned)nchunks);
         }
-        __syncthreads();
-        if (!s_last) return;
-        // ---- last CTA of the row: merge the chunk partials (loads in parallel) ----
-        const TopkPartial* rp = parts + (size_t)row * nchunks;
-        const int nk = nchunks * K;
-        for (int t = tid; t < nk; t += kThreads) {
-            const int c = t / K, k = t - c * K;
-            s_cand[t] = __ldcg((const unsigned long long*)&rp[c].keys[k]);
-        }
-        for (int c = tid; c < nchunks; c += kThreads) {
-            s_m[c] = __ldcg(&rp[c].m);
-            s_s[c] = __ldcg(&rp[c].s);
-        }
-        if (tid < K) s_sel[tid] = 0ull;
-        __syncthreads();
-        cta_rank_select(s_cand, nk, K, s_sel);  // zero keys (short lists) rank last
-        __syncthreads();
-        if (warp != 0) return;
-        float mm = -INFINITY;
-        for (int c = lane; c < nchunks; c += 32) mm = fmaxf(mm, s_m[c]);
-        mm = warp_max(mm);
-        M = (mm == -INFINITY) ? 0.f : mm;
-        float ss = 0.f;
-        for (int c = lane; c < nchunks; c += 32) ss += s_s[c] * fast_exp2((s_m[c] - M) * kLog2e);
-        S = warp_sum(ss);
-    } else if (warp != 0) {
         return;
     }
+    if (warp != 0) return;
     const float logS = logf(S);
     if (lane < K) {
         const uint64_t key = s_sel[lane];
         const float v = key_value(key);
         topk_idx[(size_t)row * K + lane] = (int32_t)key_index(key);
         topk_logp[(size_t)row * K + lane] = (v - M) - logS;
+    }
+    if (lane == 0 && lse) lse[row] = M + logS;
+}
+
+// One CTA per row: the row's K best keys among its chunks' sorted K-lists (a
+// key's rank = the keys above it, counted by binary search in every list) and
+// its logsumexp from the chunks' (max, sum) pairs, combined in fp64.
+__global__ void __launch_bounds__(kThreads)
+topk_merge_kernel(const TopkPartial* __restrict__ parts, int nchunks, int K,
+                  int32_t* __restrict__ topk_idx, float* __restrict__ topk_logp,
+                  float* __restrict__ lse) {
+    __shared__ uint64_t s_keys[kCandCap];
+    __shared__ float s_m[kMaxChunks], s_s[kMaxChunks];
+    __shared__ uint64_t s_sel[DDTREE_MAX_K];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int row = blockIdx.x;
+    if (tid < K) s_sel[tid] = 0ull;
+    pdl_trigger();
+    pdl_wait();
+    const TopkPartial* rp = parts + (size_t)row * nchunks;
+    const int nk = nchunks * K;
+    for (int t = tid; t < nk; t += kThreads) {
+        const int c = t / K, k = t - c * K;
+        s_keys[t] = __ldcg((const unsigned long long*)&rp[c].keys[k]);
+    }
+    for (int c = tid; c < nchunks; c += kThreads) {
+        s_m[c] = __ldcg(&rp[c].m);
+        s_s[c] = __ldcg(&rp[c].s);
+    }
+    __syncthreads();
+    for (int t = tid; t < nk; t += kThreads) {
+        const uint64_t key = s_keys[t];
+        if (key == 0ull) continue;  // a short chunk's empty slot
+        int rank = 0;
+        for (int c = 0; c < nchunks && rank < K; ++c)
+            rank += count_greater_desc(s_keys + c * K, K, key);
+        if (rank < K) s_sel[rank] = key;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    float mm = -INFINITY;
+    for (int c = lane; c < nchunks; c += 32) mm = fmaxf(mm, s_m[c]);
+    mm = warp_max(mm);
+    const float M = (mm == -INFINITY) ? 0.f : mm;
+    double ss = 0.0;
+    for (int c = lane; c < nchunks; c += 32) ss += (double)s_s[c] * (double)fast_exp2((s_m[c] - M) * kLog2e);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float logS = (float)log(ss);
+    if (lane < K) {
+        const uint64_t key = s_sel[lane];
+        topk_idx[(size_t)row * K + lane] = (int32_t)key_index(key);
+        topk_logp[(size_t)row * K + lane] = (key_value(key) - M) - logS;
     }
     if (lane == 0 && lse) lse[row] = M + logS;
 }
@@ -250,24 +329,21 @@ int topk_chunks(int V, int dtype) {
 size_t topk_workspace_bytes(int rows, int V, int dtype) {
     const int nch = topk_chunks(V, dtype);
     if (nch <= 1) return 0;
-    return align_up((size_t)rows * sizeof(unsigned int), 256) +
-           (size_t)rows * nch * sizeof(TopkPartial);
+    return (size_t)rows * nch * sizeof(TopkPartial);
 }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
     const int nch = topk_chunks(a.V, a.dtype);
     const int es = a.dtype == DDTREE_BF16 ? 2 : 4;
     const bool aligned = ((uintptr_t)a.logits % 16 == 0) && ((a.row_stride * es) % 16 == 0);
-    unsigned int* tickets = nullptr;
-    TopkPartial* parts = nullptr;
-    if (nch > 1) {
-        tickets = (unsigned int*)a.ws;
-        parts = (TopkPartial*)((char*)a.ws + align_up((size_t)a.rows * sizeof(unsigned int), 256));
-    }
+    TopkPartial* parts = nch > 1 ? (TopkPartial*)a.ws : nullptr;
     dim3 grid(nch, a.rows);
     auto kern = (a.dtype == DDTREE_BF16) ? topk_kernel<true> : topk_kernel<false>;
-    return launch_pdl(kern, grid, dim3(kThreads), 0, s, a.logits, a.V, a.row_stride, a.K, nch,
-                      aligned, a.topk_idx, a.topk_logp, a.lse, parts, tickets);
+    cudaError_t e = launch_pdl(kern, grid, dim3(kThreads), 0, s, a.logits, a.V, a.row_stride,
+                               a.K, nch, aligned, a.topk_idx, a.topk_logp, a.lse, parts);
+    if (e != cudaSuccess || nch <= 1) return e;
+    return launch_pdl(topk_merge_kernel, dim3(a.rows), dim3(kThreads), 0, s,
+                      (const TopkPartial*)parts, nch, a.K, a.topk_idx, a.topk_logp, a.lse);
 }
 
 }  // namespace ddt
@@ -319,14 +395,8 @@ extern "C" ddtree_status ddtree_topk_noalloc(const void* draft_logits, int dtype
     const size_t need = ddt::topk_workspace_bytes(rows, V, dtype);
     if (need > DDTREE_NOALLOC_SCRATCH_BYTES) return DDTREE_ERR_UNSUPPORTED;
     void* scratch = nullptr;
-    if (need) {
-        if (noalloc_scratch(&scratch) != cudaSuccess) return DDTREE_ERR_CUDA;
-        // The array keeps whatever the previous call left in it; the row
-        // counters must start at zero.
-        const size_t counters = ddt::align_up((size_t)rows * sizeof(unsigned int), 256);
-        if (cudaMemsetAsync(scratch, 0, counters, (cudaStream_t)stream) != cudaSuccess)
-            return DDTREE_ERR_CUDA;
-    }
+    // (every partial the merge reads is written by the same call: no clearing)
+    if (need && noalloc_scratch(&scratch) != cudaSuccess) return DDTREE_ERR_CUDA;
     ddt::TopkArgs a{draft_logits, dtype, rows, V, row_stride, K, topk_idx, topk_logp, lse,
                     scratch, nullptr};
     return ddt::launch_topk(a, (cudaStream_t)stream) == cudaSuccess ? DDTREE_OK : DDTREE_ERR_CUDA;
