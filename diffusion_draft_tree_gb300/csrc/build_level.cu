@@ -190,9 +190,7 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
                 __syncthreads();  // the batch's keys are in place
                 for (int i = tid; i < c; i += kThreads) {
                     const uint64_t k = s_cand[i];
-                    int r = 0;
-                    for (int j = 0; j < c; ++j) r += (s_cand[j] > k) ? 1 : 0;
-                    s_cand[kCandCap / 2 + r] = k;
+                    s_cand[kCandCap / 2 + count_larger(s_cand, c, k)] = k;
                 }
                 sorted = s_cand + kCandCap / 2;
                 __syncthreads();

@@ -128,6 +128,22 @@ DDT_DEV bool ticket_is_last(unsigned int* counter, unsigned int expected) {
     return last;
 }
 
+// Number of a[0..n) larger than x, for a rank by counting.  a is 16-byte
+// aligned shared memory read by every thread of a warp at once (broadcast),
+// two keys per load, eight loads in flight.
+DDT_DEV int count_larger(const uint64_t* a, int n, uint64_t x) {
+    const ulonglong2* a2 = reinterpret_cast<const ulonglong2*>(a);
+    const int n2 = n >> 1;
+    int r = 0;
+#pragma unroll 8
+    for (int j = 0; j < n2; ++j) {
+        const ulonglong2 v = a2[j];
+        r += (v.x > x ? 1 : 0) + (v.y > x ? 1 : 0);
+    }
+    if (n & 1) r += a[n - 1] > x ? 1 : 0;
+    return r;
+}
+
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch.  Kernels are launched so that they may start
 // while the previous kernel on the stream is finishing: each one first lets its

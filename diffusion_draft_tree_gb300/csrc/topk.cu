@@ -13,9 +13,9 @@
 // tau = max_w tau_w -- a lower bound on the chunk's K-th largest value -- and
 // only elements >= tau (typically ~2K of 8K) are appended to a shared buffer
 // (one shared atomic per warp), then sorted by one warp (or ranked by
-// counting when there are more than 32).  A second, PDL-chained kernel merges
-// each row's chunk partials: the K largest of the nchunks sorted lists, each
-// key ranked by binary searches in all of them, and the row's logsumexp.
+// counting when there are more than 32).  A second, PDL-chained kernel (one
+// warp per row) merges each row's chunk partials the same way -- the keys at
+// or above the largest chunk-K-th key, sorted -- and forms the logsumexp.
 #include <mutex>
 
 #include "chunk.cuh"
@@ -58,8 +58,7 @@ DDT_DEV uint32_t warp_sort_desc_u32(uint32_t v) {
 DDT_DEV void cta_rank_select(const uint64_t* cand, int cnt, int K, uint64_t* sel) {
     for (int i = threadIdx.x; i < cnt; i += kThreads) {
         const uint64_t ki = cand[i];
-        int rank = 0;
-        for (int j = 0; j < cnt; ++j) rank += (cand[j] > ki) ? 1 : 0;
+        const int rank = count_larger(cand, cnt, ki);
         if (rank < K) sel[rank] = ki;
     }
 }
@@ -79,17 +78,6 @@ DDT_DEV uint64_t warp_sort_desc_u64(uint64_t v) {
     return v;
 }
 
-// Keys of the descending list a[0..n) that are larger than x.
-DDT_DEV int count_greater_desc(const uint64_t* a, int n, uint64_t x) {
-    int lo = 0, hi = n;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (a[mid] > x) lo = mid + 1;
-        else hi = mid;
-    }
-    return lo;
-}
-
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads)
 topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, int nchunks,
@@ -100,7 +88,7 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     constexpr int PER = Chunk::NVEC / kThreads;  // vectors per thread
     __shared__ __align__(128) uint8_t s_buf[Chunk::BYTES];
     __shared__ __align__(8) uint64_t s_bar;
-    __shared__ uint64_t s_cand[kCandCap];
+    __shared__ __align__(16) uint64_t s_cand[kCandCap];
     __shared__ uint64_t s_sel[DDTREE_MAX_K];
     __shared__ float s_wmax[kThreads / 32], s_wsum[kThreads / 32];
     __shared__ uint32_t s_wtau[kThreads / 32];
@@ -259,51 +247,69 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     if (lane == 0 && lse) lse[row] = M + logS;
 }
 
-// One CTA per row: the row's K best keys among its chunks' sorted K-lists (a
-// key's rank = the keys above it, counted by binary search in every list) and
-// its logsumexp from the chunks' (max, sum) pairs, combined in fp64.
-__global__ void __launch_bounds__(kThreads)
+// One warp per row merges its chunk partials.  The row's K best keys are >=
+// tau2 = the largest K-th key of any chunk (that chunk alone holds K keys >=
+// tau2), so only the keys >= tau2 -- usually K to 2K of them -- are sorted
+// (one warp bitonic sort, or ranked by counting when more than 32).  The
+// logsumexp combines the chunks' (max, sum) pairs.
+constexpr int kMergeThreads = 32;
+__global__ void __launch_bounds__(kMergeThreads)
 topk_merge_kernel(const TopkPartial* __restrict__ parts, int nchunks, int K,
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_logp,
                   float* __restrict__ lse) {
-    __shared__ uint64_t s_keys[kCandCap];
-    __shared__ float s_m[kMaxChunks], s_s[kMaxChunks];
+    __shared__ __align__(16) uint64_t s_keys[kCandCap];
+    __shared__ __align__(16) uint64_t s_c[kCandCap];
     __shared__ uint64_t s_sel[DDTREE_MAX_K];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lane = threadIdx.x;
     const int row = blockIdx.x;
-    if (tid < K) s_sel[tid] = 0ull;
     pdl_trigger();
     pdl_wait();
     const TopkPartial* rp = parts + (size_t)row * nchunks;
     const int nk = nchunks * K;
-    for (int t = tid; t < nk; t += kThreads) {
+    uint64_t tau2 = 0ull;
+    float mm = -INFINITY;
+    for (int c = lane; c < nchunks; c += 32) {
+        tau2 = umax64(tau2, __ldcg((const unsigned long long*)&rp[c].keys[K - 1]));
+        mm = fmaxf(mm, __ldcg(&rp[c].m));
+    }
+    for (int t = lane; t < nk; t += 32) {
         const int c = t / K, k = t - c * K;
         s_keys[t] = __ldcg((const unsigned long long*)&rp[c].keys[k]);
     }
-    for (int c = tid; c < nchunks; c += kThreads) {
-        s_m[c] = __ldcg(&rp[c].m);
-        s_s[c] = __ldcg(&rp[c].s);
-    }
-    __syncthreads();
-    for (int t = tid; t < nk; t += kThreads) {
-        const uint64_t key = s_keys[t];
-        if (key == 0ull) continue;  // a short chunk's empty slot
-        int rank = 0;
-        for (int c = 0; c < nchunks && rank < K; ++c)
-            rank += count_greater_desc(s_keys + c * K, K, key);
-        if (rank < K) s_sel[rank] = key;
-    }
-    __syncthreads();
-    if (warp != 0) return;
-    float mm = -INFINITY;
-    for (int c = lane; c < nchunks; c += 32) mm = fmaxf(mm, s_m[c]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tau2 = umax64(tau2, shfl_xor_u64(tau2, o));
     mm = warp_max(mm);
     const float M = (mm == -INFINITY) ? 0.f : mm;
-    double ss = 0.0;
-    for (int c = lane; c < nchunks; c += 32) ss += (double)s_s[c] * (double)fast_exp2((s_m[c] - M) * kLog2e);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float logS = (float)log(ss);
+    float ss = 0.f;
+    for (int c = lane; c < nchunks; c += 32)
+        ss += __ldcg(&rp[c].s) * fast_exp2((__ldcg(&rp[c].m) - M) * kLog2e);
+    ss = warp_sum(ss);
+    __syncwarp();
+    // keys >= tau2, compacted in list order
+    int cnt = 0;
+    for (int t0 = 0; t0 < nk; t0 += 32) {
+        const int t = t0 + lane;
+        const uint64_t key = t < nk ? s_keys[t] : 0ull;
+        const bool in = key >= tau2 && key != 0ull;
+        const unsigned bal = __ballot_sync(0xffffffffu, in);
+        if (in) s_c[cnt + __popc(bal & ((1u << lane) - 1u))] = key;
+        cnt += __popc(bal);
+    }
+    __syncwarp();
+    if (cnt <= 32) {
+        const uint64_t key = warp_sort_desc_u64(lane < cnt ? s_c[lane] : 0ull);
+        if (lane < K) s_sel[lane] = key;
+    } else {
+        if (lane < K) s_sel[lane] = 0ull;
+        __syncwarp();
+        for (int i = lane; i < cnt; i += 32) {
+            const uint64_t key = s_c[i];
+            const int rank = count_larger(s_c, cnt, key);
+            if (rank < K) s_sel[rank] = key;
+        }
+    }
+    __syncwarp();
+    const float logS = logf(ss);
     if (lane < K) {
         const uint64_t key = s_sel[lane];
         topk_idx[(size_t)row * K + lane] = (int32_t)key_index(key);
@@ -342,7 +348,7 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
     cudaError_t e = launch_pdl(kern, grid, dim3(kThreads), 0, s, a.logits, a.V, a.row_stride,
                                a.K, nch, aligned, a.topk_idx, a.topk_logp, a.lse, parts);
     if (e != cudaSuccess || nch <= 1) return e;
-    return launch_pdl(topk_merge_kernel, dim3(a.rows), dim3(kThreads), 0, s,
+    return launch_pdl(topk_merge_kernel, dim3(a.rows), dim3(kMergeThreads), 0, s,
                       (const TopkPartial*)parts, nch, a.K, a.topk_idx, a.topk_logp, a.lse);
 }
 
