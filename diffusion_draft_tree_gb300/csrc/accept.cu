@@ -105,7 +105,6 @@ accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nc
     const size_t row = (size_t)b * R + u;
     const char* rowp = (const char*)logits + row * (size_t)row_stride * Chunk::ES;
     const int c0 = chunk * Chunk::SIZE;
-    pdl_trigger();
     pdl_wait();
     // Start the row's bulk copy before the tree size arrives; rows past the
     // tree wait for their copy and leave.
@@ -181,6 +180,7 @@ accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nc
     }
 
     __shared__ int s_tok[DDTREE_MAX_N + 1];
+    pdl_trigger();
     if (!sample) {
         // greedy: one 64-bit atomicMax per CTA resolves the row; the last CTA of
         // the whole sequence (all rows, all chunks) walks the tree.

@@ -51,7 +51,6 @@ build_kernel(const float* __restrict__ topk_logp, const int32_t* __restrict__ to
 
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
     const int LK = L * K;
-    pdl_trigger();
     pdl_wait();
     for (int i = tid; i < LK; i += kThreads) {
         s_lp[i] = topk_logp[(size_t)b * LK + i];
@@ -122,6 +121,7 @@ build_kernel(const float* __restrict__ topk_logp, const int32_t* __restrict__ to
     for (int c = 1 + tid; c <= n; c += kThreads) atomicAdd(&s_cc[s_par[c]], 1);
     __syncthreads();
 
+    pdl_trigger();
     const int R = N + 1, W = (N + 1 + 31) / 32;
     const int P = prefix_len[b];
     for (int u = tid; u < R; u += kThreads) {

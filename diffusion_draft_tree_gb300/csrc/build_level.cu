@@ -107,7 +107,6 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
 
     const int b = blockIdx.x, tid = threadIdx.x;
     const int LK = L * K;
-    pdl_trigger();
     pdl_wait();
     for (int i = tid; i < LK; i += kThreads) s_lp[i] = topk_logp[(size_t)b * LK + i];
     __syncthreads();
@@ -258,6 +257,7 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
         if (!s_flag) break;
     }
 
+    pdl_trigger();
     // ---- outputs: node u = position u-1 of T ------------------------------------------
     const int n = t;
     int16_t* s_par = (int16_t*)s_cand;                    // [N+1]

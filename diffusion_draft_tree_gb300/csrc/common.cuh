@@ -146,11 +146,12 @@ DDT_DEV int count_larger(const uint64_t* a, int n, uint64_t x) {
 
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch.  Kernels are launched so that they may start
-// while the previous kernel on the stream is finishing: each one first lets its
-// own successor start (pdl_trigger) and then waits (pdl_wait) until every
-// earlier kernel on the stream has completed and its writes are visible, before
-// it reads or writes any global memory.  What overlaps is launch latency and
-// CTA start-up, never data.
+// while the previous kernel on the stream is finishing: each one waits
+// (pdl_wait) until every earlier kernel on the stream has completed and its
+// writes are visible before it reads or writes any global memory, and lets its
+// own successor be scheduled (pdl_trigger) only once its main work is done --
+// a successor's CTAs waiting on an SM slow the kernel still running there.
+// What overlaps is launch latency and CTA start-up, never data.
 // ---------------------------------------------------------------------------
 DDT_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 DDT_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

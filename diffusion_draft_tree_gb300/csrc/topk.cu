@@ -100,7 +100,6 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     const char* rowp = (const char*)logits + (size_t)row * (size_t)row_stride * Chunk::ES;
     if (tid == 0) s_cnt = 0;
     if (tid < K) s_sel[tid] = 0ull;
-    pdl_trigger();
     pdl_wait();
     if (!Chunk::load(s_buf, &s_bar, rowp, c0, V, aligned)) return;  // copy never landed
     const uint4* vec = reinterpret_cast<const uint4*>(s_buf);
@@ -181,6 +180,7 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     if (lane == 0) s_wsum[warp] = ssum;
     __syncthreads();
     const int cnt = s_cnt;
+    pdl_trigger();
 
     if (cnt <= 32) {
         if (warp == 0) {
@@ -262,7 +262,6 @@ topk_merge_kernel(const TopkPartial* __restrict__ parts, int nchunks, int K,
     __shared__ uint64_t s_sel[DDTREE_MAX_K];
     const int lane = threadIdx.x;
     const int row = blockIdx.x;
-    pdl_trigger();
     pdl_wait();
     const TopkPartial* rp = parts + (size_t)row * nchunks;
     const int nk = nchunks * K;
@@ -285,6 +284,7 @@ topk_merge_kernel(const TopkPartial* __restrict__ parts, int nchunks, int K,
         ss += __ldcg(&rp[c].s) * fast_exp2((__ldcg(&rp[c].m) - M) * kLog2e);
     ss = warp_sum(ss);
     __syncwarp();
+    pdl_trigger();
     // keys >= tau2, compacted in list order
     int cnt = 0;
     for (int t0 = 0; t0 < nk; t0 += 32) {

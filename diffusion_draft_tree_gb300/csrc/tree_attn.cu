@@ -198,7 +198,6 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int g = idx % p.Hkv;
     const int b = idx / p.Hkv;
     const int R = p.N + 1, G = p.G;
-    pdl_trigger();
     pdl_wait();
     const int P = p.prefix_len[b];
     const int n = p.n_nodes[b];
@@ -637,6 +636,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // ---- teardown: every thread arrives here (all waits are bounded) -------------
     tc_fence_before();
     __syncthreads();
+    pdl_trigger();
     if (p.merge == kMergeCluster) {
         // Execution order is all that is needed: every split's partial is written
         // and read only by its own copy engine; every K/V stage is idle.
