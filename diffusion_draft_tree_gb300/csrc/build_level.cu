@@ -155,20 +155,28 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
             const float theta = full ? lk_score(s_T[cur][t - 1]) : 0.f;
             uint64_t key[kPairsPerThread];
             int cnt = 0;
+            // pair q = (parent q / K, rank q % K); strided over the threads so that
+            // a small batch spreads over all of them (the batch is sorted below,
+            // so the order of the keys is free); one division, then increments
+            const int step_pi = kThreads / K, step_r = kThreads - step_pi * K;
+            int pi = (base + tid) / K, r = base + tid - pi * K;
 #pragma unroll
             for (int j = 0; j < kPairsPerThread; ++j) {
-                // strided, so that a small batch spreads over all threads (the
-                // batch is sorted below, so the order of the keys is free)
                 const int q = base + j * kThreads + tid;
                 key[j] = 0ull;
                 if (q < pairs) {
-                    const int pi = q / K, r = q - pi * K;
                     const int pp = s_plist[pi];
                     const float sc = __fadd_rn(s_pscore[pi], lp[r]);
                     if (!full || sc > theta) {
                         key[j] = lkey(sc, d, pp, r);
                         ++cnt;
                     }
+                }
+                pi += step_pi;
+                r += step_r;
+                if (r >= K) {
+                    r -= K;
+                    ++pi;
                 }
             }
             int c;

@@ -265,11 +265,20 @@ topk_merge_kernel(const TopkPartial* __restrict__ parts, int nchunks, int K,
     pdl_wait();
     const TopkPartial* rp = parts + (size_t)row * nchunks;
     const int nk = nchunks * K;
+    // every load of the row in one round trip
+    constexpr int kPerLane = kMaxChunks / 32;
     uint64_t tau2 = 0ull;
-    float mm = -INFINITY;
-    for (int c = lane; c < nchunks; c += 32) {
-        tau2 = umax64(tau2, __ldcg((const unsigned long long*)&rp[c].keys[K - 1]));
-        mm = fmaxf(mm, __ldcg(&rp[c].m));
+    float cm[kPerLane], cs[kPerLane];
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        const int c = lane + 32 * i;
+        cm[i] = -INFINITY;
+        cs[i] = 0.f;
+        if (c < nchunks) {
+            tau2 = umax64(tau2, __ldcg((const unsigned long long*)&rp[c].keys[K - 1]));
+            cm[i] = __ldcg(&rp[c].m);
+            cs[i] = __ldcg(&rp[c].s);
+        }
     }
     for (int t = lane; t < nk; t += 32) {
         const int c = t / K, k = t - c * K;
@@ -277,11 +286,15 @@ topk_merge_kernel(const TopkPartial* __restrict__ parts, int nchunks, int K,
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) tau2 = umax64(tau2, shfl_xor_u64(tau2, o));
+    float mm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) mm = fmaxf(mm, cm[i]);
     mm = warp_max(mm);
     const float M = (mm == -INFINITY) ? 0.f : mm;
     float ss = 0.f;
-    for (int c = lane; c < nchunks; c += 32)
-        ss += __ldcg(&rp[c].s) * fast_exp2((__ldcg(&rp[c].m) - M) * kLog2e);
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i)
+        ss += (cm[i] == -INFINITY) ? 0.f : cs[i] * fast_exp2((cm[i] - M) * kLog2e);
     ss = warp_sum(ss);
     __syncwarp();
     pdl_trigger();
