@@ -68,6 +68,47 @@ struct SmemChunk {
         return __syncthreads_and(ok) != 0;
     }
 
+    // For a ring of stages whose mbarriers (count 1) were initialised once:
+    // starts staging the chunk into `buf`, completing on `bar`'s next phase.
+    // All threads call it; they fill the unaligned tail themselves, so the
+    // stage may be read only after wait() and a CTA barrier.
+    DDT_DEV static void issue_ring(uint8_t* buf, uint64_t* bar, const char* rowp, int c0, int V,
+                                   bool aligned) {
+        const int n_in = max(0, min(SIZE, V - c0));
+        const int n_bulk = aligned ? (n_in / VEC) * VEC : 0;
+        if (threadIdx.x == 0) {
+            sm100::fence_proxy_async_smem();  // earlier generic reads of the stage
+            if (n_bulk > 0) {
+                sm100::mbar_arrive_expect_tx(bar, (uint32_t)(n_bulk * ES));
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+                    " [%0], [%1], %2, [%3];" ::"r"(sm100::smem_u32(buf)),
+                    "l"(rowp + (size_t)c0 * ES), "r"((uint32_t)(n_bulk * ES)),
+                    "r"(sm100::smem_u32(bar))
+                    : "memory");
+            } else {
+                sm100::mbar_arrive(bar);
+            }
+        }
+        for (int i = n_bulk + (int)threadIdx.x; i < SIZE; i += THREADS) {
+            if (BF16) {
+                const unsigned short v =
+                    (i < n_in) ? __ldg((const unsigned short*)rowp + c0 + i) : (unsigned short)0xff80u;
+                ((unsigned short*)buf)[i] = v;
+            } else {
+                const unsigned int v = (i < n_in) ? __ldg((const unsigned int*)rowp + c0 + i)
+                                                  : 0xff800000u;
+                ((unsigned int*)buf)[i] = v;
+            }
+        }
+    }
+
+    // Waits (bounded) for the given phase of a ring stage; CTA-uniform result.
+    DDT_DEV static bool wait_ring(uint64_t* bar, uint32_t parity) {
+        const bool ok = sm100::mbar_wait(bar, parity, nullptr);
+        return __syncthreads_and(ok) != 0;
+    }
+
     DDT_DEV static bool load(uint8_t* buf, uint64_t* bar, const char* rowp, int c0, int V,
                              bool aligned) {
         issue(buf, bar, rowp, c0, V, aligned);

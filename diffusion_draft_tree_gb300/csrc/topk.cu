@@ -31,6 +31,8 @@ constexpr int kThreads = 256;
 constexpr int kChunkBytes = 16384;
 constexpr int kCandCap = 1024;
 constexpr int kMaxChunks = 128;
+constexpr int kStages = 4;       // chunks in flight per CTA
+constexpr int kCtasPerSm = 2;
 
 struct TopkPartial {
     float m;   // chunk max
@@ -78,16 +80,20 @@ DDT_DEV uint64_t warp_sort_desc_u64(uint64_t v) {
     return v;
 }
 
+// Persistent: CTA i handles chunks [i per, (i+1) per) of the flattened
+// (row, chunk) list, streaming them through a ring of kStages shared-memory
+// stages (bulk copies issued kStages-1 chunks ahead).
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads)
 topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, int nchunks,
-            bool aligned, int32_t* __restrict__ topk_idx, float* __restrict__ topk_logp,
-            float* __restrict__ lse, TopkPartial* __restrict__ parts) {
+            bool aligned, int total, int per, int32_t* __restrict__ topk_idx,
+            float* __restrict__ topk_logp, float* __restrict__ lse,
+            TopkPartial* __restrict__ parts, uint32_t* err) {
     using Chunk = SmemChunk<BF16, kChunkBytes / (BF16 ? 2 : 4)>;
     constexpr int VEC = Chunk::VEC;
     constexpr int PER = Chunk::NVEC / kThreads;  // vectors per thread
-    __shared__ __align__(128) uint8_t s_buf[Chunk::BYTES];
-    __shared__ __align__(8) uint64_t s_bar;
+    extern __shared__ __align__(128) uint8_t s_ring[];  // kStages x Chunk::BYTES
+    __shared__ __align__(8) uint64_t s_bar[kStages];
     __shared__ __align__(16) uint64_t s_cand[kCandCap];
     __shared__ uint64_t s_sel[DDTREE_MAX_K];
     __shared__ float s_wmax[kThreads / 32], s_wsum[kThreads / 32];
@@ -95,156 +101,174 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     __shared__ int s_cnt;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int chunk = blockIdx.x, row = blockIdx.y;
-    const int c0 = chunk * Chunk::SIZE;
-    const char* rowp = (const char*)logits + (size_t)row * (size_t)row_stride * Chunk::ES;
-    if (tid == 0) s_cnt = 0;
-    if (tid < K) s_sel[tid] = 0ull;
-    pdl_wait();
-    if (!Chunk::load(s_buf, &s_bar, rowp, c0, V, aligned)) return;  // copy never landed
-    const uint4* vec = reinterpret_cast<const uint4*>(s_buf);
-
-    // ---- pass 1: lane maxima; tau_w = K-th largest lane maximum of the warp ------
-    float tmax = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) tmax = fmaxf(tmax, Chunk::vmax(vec[tid + i * kThreads]));
-    const bool has = c0 + tid * VEC < V;
-    const uint32_t lane_ord = has ? ord_from_float(tmax) : 0u;
-    const uint32_t tau_w = __shfl_sync(0xffffffffu, warp_sort_desc_u32(lane_ord), K - 1);
-    const float wmax = warp_max(tmax);
-    if (lane == 0) {
-        s_wmax[warp] = wmax;
-        s_wtau[warp] = tau_w;
+    const int w0 = blockIdx.x * per;
+    const int nmine = min(total, w0 + per) - w0;
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) sm100::mbar_init(&s_bar[s], 1);
+        sm100::mbar_init_fence();
     }
     __syncthreads();
-    // The chunk has >= K elements >= the value with order tau (K lane maxima of
-    // one warp), so its top K are among the elements >= that value.
-    float m = s_wmax[0];
-    uint32_t tau = s_wtau[0];
-#pragma unroll
-    for (int i = 1; i < kThreads / 32; ++i) {
-        m = fmaxf(m, s_wmax[i]);
-        tau = max(tau, s_wtau[i]);
-    }
-
-    // ---- pass 2: sum of exponentials; candidates -----------------------------------
-    const float ref = (m == -INFINITY) ? 0.f : m;
-    const float off = -ref * kLog2e;
-    const float tv = (tau == 0u) ? -INFINITY : float_from_ord(tau);
-    float ssum = 0.f;
-    int mine = 0;  // this thread's candidates
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        const int v = tid + i * kThreads;
-        const uint4 w = vec[v];
-        float x[VEC];
-        Chunk::unpack(w, x);
-#pragma unroll
-        for (int k = 0; k < VEC; ++k) ssum += fast_exp2(fmaf(x[k], kLog2e, off));
-        if (Chunk::vmax(w) >= tv) {
-#pragma unroll
-            for (int k = 0; k < VEC; ++k) mine += (x[k] >= tv && c0 + v * VEC + k < V) ? 1 : 0;
+    pdl_wait();
+    auto issue = [&](int j) {  // chunk j of this CTA into stage j % kStages
+        const int w = w0 + j, row = w / nchunks, chunk = w - row * nchunks;
+        Chunk::issue_ring(s_ring + (j % kStages) * Chunk::BYTES, &s_bar[j % kStages],
+                          (const char*)logits + (size_t)row * (size_t)row_stride * Chunk::ES,
+                          chunk * Chunk::SIZE, V, aligned);
+    };
+    for (int j = 0; j < kStages - 1 && j < nmine; ++j) issue(j);
+    for (int j = 0; j < nmine; ++j) {
+        if (j + kStages - 1 < nmine) issue(j + kStages - 1);  // into the stage freed last step
+        if (j == nmine - 1) pdl_trigger();
+        const int w = w0 + j, row = w / nchunks, chunk = w - row * nchunks;
+        const int c0 = chunk * Chunk::SIZE;
+        if (tid == 0) s_cnt = 0;
+        if (tid < K) s_sel[tid] = 0ull;
+        if (!Chunk::wait_ring(&s_bar[j % kStages], (uint32_t)((j / kStages) & 1))) {
+            if (tid == 0) record_error(err, ERR_TOPK | ERR_WAIT_TIMEOUT);
+            return;  // a copy never landed
         }
-    }
-    // one shared atomic per warp reserves the warp's slots
-    int incl = mine;
+        const uint4* vec = reinterpret_cast<const uint4*>(s_ring + (j % kStages) * Chunk::BYTES);
+
+        // ---- pass 1: lane maxima; tau_w = K-th largest lane maximum of the warp ------
+        float tmax = -INFINITY;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-    }
-    int wbase = 0;
-    if (lane == 31 && incl > 0) wbase = atomicAdd(&s_cnt, incl);
-    wbase = __shfl_sync(0xffffffffu, wbase, 31);
-    if (mine) {
-        int pos = wbase + incl - mine;
+        for (int i = 0; i < PER; ++i) tmax = fmaxf(tmax, Chunk::vmax(vec[tid + i * kThreads]));
+        const bool has = c0 + tid * VEC < V;
+        const uint32_t lane_ord = has ? ord_from_float(tmax) : 0u;
+        const uint32_t tau_w = __shfl_sync(0xffffffffu, warp_sort_desc_u32(lane_ord), K - 1);
+        const float wmax = warp_max(tmax);
+        if (lane == 0) {
+            s_wmax[warp] = wmax;
+            s_wtau[warp] = tau_w;
+        }
+        __syncthreads();
+        // The chunk has >= K elements >= the value with order tau (K lane maxima of
+        // one warp), so its top K are among the elements >= that value.
+        float m = s_wmax[0];
+        uint32_t tau = s_wtau[0];
+#pragma unroll
+        for (int i = 1; i < kThreads / 32; ++i) {
+            m = fmaxf(m, s_wmax[i]);
+            tau = max(tau, s_wtau[i]);
+        }
+
+        // ---- pass 2: sum of exponentials; candidates -----------------------------------
+        const float ref = (m == -INFINITY) ? 0.f : m;
+        const float off = -ref * kLog2e;
+        const float tv = (tau == 0u) ? -INFINITY : float_from_ord(tau);
+        float ssum = 0.f;
+        int mine = 0;  // this thread's candidates
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
             const int v = tid + i * kThreads;
             const uint4 w = vec[v];
-            if (Chunk::vmax(w) >= tv) {
-                float x[VEC];
-                Chunk::unpack(w, x);
+            float x[VEC];
+            Chunk::unpack(w, x);
 #pragma unroll
-                for (int k = 0; k < VEC; ++k) {
-                    const int e = c0 + v * VEC + k;
-                    if (x[k] >= tv && e < V) {
-                        if (pos < kCandCap) s_cand[pos] = value_index_key(x[k], (uint32_t)e);
-                        ++pos;
-                    }
-                }
+            for (int k = 0; k < VEC; ++k) ssum += fast_exp2(fmaf(x[k], kLog2e, off));
+            if (Chunk::vmax(w) >= tv) {
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) mine += (x[k] >= tv && c0 + v * VEC + k < V) ? 1 : 0;
             }
         }
-    }
-    ssum = warp_sum(ssum);
-    if (lane == 0) s_wsum[warp] = ssum;
-    __syncthreads();
-    const int cnt = s_cnt;
-    pdl_trigger();
-
-    if (cnt <= 32) {
-        if (warp == 0) {
-            const uint64_t key = warp_sort_desc_u64(lane < cnt ? s_cand[lane] : 0ull);
-            if (lane < K) s_sel[lane] = key;
+        // one shared atomic per warp reserves the warp's slots
+        int incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
         }
-    } else if (cnt <= kCandCap) {
-        cta_rank_select(s_cand, cnt, K, s_sel);
-    } else {
-        // Degenerate ties overflowed the buffer: exact K-round selection
-        // (rare path; correctness only).
-        uint64_t prev = ~0ull;
-        for (int r = 0; r < K; ++r) {
-            uint64_t tb = 0ull;
+        int wbase = 0;
+        if (lane == 31 && incl > 0) wbase = atomicAdd(&s_cnt, incl);
+        wbase = __shfl_sync(0xffffffffu, wbase, 31);
+        if (mine) {
+            int pos = wbase + incl - mine;
+#pragma unroll
             for (int i = 0; i < PER; ++i) {
                 const int v = tid + i * kThreads;
-                float x[VEC];
-                Chunk::unpack(vec[v], x);
-                for (int k = 0; k < VEC; ++k) {
-                    const int e = c0 + v * VEC + k;
-                    if (e < V) {
-                        const uint64_t key = value_index_key(x[k], (uint32_t)e);
-                        if (key < prev && key > tb) tb = key;
+                const uint4 w = vec[v];
+                if (Chunk::vmax(w) >= tv) {
+                    float x[VEC];
+                    Chunk::unpack(w, x);
+#pragma unroll
+                    for (int k = 0; k < VEC; ++k) {
+                        const int e = c0 + v * VEC + k;
+                        if (x[k] >= tv && e < V) {
+                            if (pos < kCandCap) s_cand[pos] = value_index_key(x[k], (uint32_t)e);
+                            ++pos;
+                        }
                     }
                 }
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) tb = umax64(tb, shfl_xor_u64(tb, o));
-            if (lane == 0) s_cand[warp] = tb;
-            __syncthreads();
-            uint64_t cb = s_cand[0];
-            for (int i = 1; i < kThreads / 32; ++i) cb = umax64(cb, s_cand[i]);
-            if (tid == 0) s_sel[r] = cb;
-            prev = cb;
-            __syncthreads();
         }
-    }
-    __syncthreads();
+        ssum = warp_sum(ssum);
+        if (lane == 0) s_wsum[warp] = ssum;
+        __syncthreads();
+        const int cnt = s_cnt;
 
-    float S = 0.f;
+        if (cnt <= 32) {
+            if (warp == 0) {
+                const uint64_t key = warp_sort_desc_u64(lane < cnt ? s_cand[lane] : 0ull);
+                if (lane < K) s_sel[lane] = key;
+            }
+        } else if (cnt <= kCandCap) {
+            cta_rank_select(s_cand, cnt, K, s_sel);
+        } else {
+            // Degenerate ties overflowed the buffer: exact K-round selection
+            // (rare path; correctness only).
+            uint64_t prev = ~0ull;
+            for (int r = 0; r < K; ++r) {
+                uint64_t tb = 0ull;
+                for (int i = 0; i < PER; ++i) {
+                    const int v = tid + i * kThreads;
+                    float x[VEC];
+                    Chunk::unpack(vec[v], x);
+                    for (int k = 0; k < VEC; ++k) {
+                        const int e = c0 + v * VEC + k;
+                        if (e < V) {
+                            const uint64_t key = value_index_key(x[k], (uint32_t)e);
+                            if (key < prev && key > tb) tb = key;
+                        }
+                    }
+                }
 #pragma unroll
-    for (int i = 0; i < kThreads / 32; ++i) S += s_wsum[i];
-    float M = ref;
-
-    if (nchunks > 1) {  // the merge kernel finishes the row
-        if (warp == 0) {
-            TopkPartial* p = parts + (size_t)row * nchunks + chunk;
-            if (lane < K) p->keys[lane] = s_sel[lane];
-            if (lane == 0) {
-                p->m = m;
-                p->s = S;
+                for (int o = 16; o > 0; o >>= 1) tb = umax64(tb, shfl_xor_u64(tb, o));
+                if (lane == 0) s_cand[warp] = tb;
+                __syncthreads();
+                uint64_t cb = s_cand[0];
+                for (int i = 1; i < kThreads / 32; ++i) cb = umax64(cb, s_cand[i]);
+                if (tid == 0) s_sel[r] = cb;
+                prev = cb;
+                __syncthreads();
             }
         }
-        return;
+        __syncthreads();
+
+        float S = 0.f;
+#pragma unroll
+        for (int i = 0; i < kThreads / 32; ++i) S += s_wsum[i];
+        float M = ref;
+
+        if (nchunks > 1) {  // the merge kernel finishes the row
+            if (warp == 0) {
+                TopkPartial* p = parts + (size_t)row * nchunks + chunk;
+                if (lane < K) p->keys[lane] = s_sel[lane];
+                if (lane == 0) {
+                    p->m = m;
+                    p->s = S;
+                }
+            }
+        } else if (warp == 0) {
+            const float logS = logf(S);
+            if (lane < K) {
+                const uint64_t key = s_sel[lane];
+                topk_idx[(size_t)row * K + lane] = (int32_t)key_index(key);
+                topk_logp[(size_t)row * K + lane] = (key_value(key) - M) - logS;
+            }
+            if (lane == 0 && lse) lse[row] = M + logS;
+        }
+        __syncthreads();  // the stage, the candidates and the selection are free again
     }
-    if (warp != 0) return;
-    const float logS = logf(S);
-    if (lane < K) {
-        const uint64_t key = s_sel[lane];
-        const float v = key_value(key);
-        topk_idx[(size_t)row * K + lane] = (int32_t)key_index(key);
-        topk_logp[(size_t)row * K + lane] = (v - M) - logS;
-    }
-    if (lane == 0 && lse) lse[row] = M + logS;
 }
 
 // One warp per row merges its chunk partials.  The row's K best keys are >=
@@ -333,6 +357,20 @@ topk_merge_kernel(const TopkPartial* __restrict__ parts, int nchunks, int K,
 
 int chunk_elems(int dtype) { return kChunkBytes / (dtype == DDTREE_BF16 ? 2 : 4); }
 
+// Streaming multiprocessors of the current device (148 if the query fails).
+int num_sms_topk() {
+    static int cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
 }  // namespace
 
 bool topk_supported(int V, int dtype, int K) {
@@ -356,10 +394,29 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
     const int es = a.dtype == DDTREE_BF16 ? 2 : 4;
     const bool aligned = ((uintptr_t)a.logits % 16 == 0) && ((a.row_stride * es) % 16 == 0);
     TopkPartial* parts = nch > 1 ? (TopkPartial*)a.ws : nullptr;
-    dim3 grid(nch, a.rows);
+    static std::once_flag once[64];
+    static cudaError_t attr_err[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const size_t ring = (size_t)kStages * kChunkBytes;
+    std::call_once(once[dev & 63], [&] {
+        cudaError_t e = cudaFuncSetAttribute(topk_kernel<true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(topk_kernel<false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring);
+        attr_err[dev & 63] = e;
+    });
+    if (attr_err[dev & 63] != cudaSuccess) return attr_err[dev & 63];
+    // one wave of persistent CTAs, each streaming a contiguous run of chunks
+    const long total = (long)nch * a.rows;
+    const long slots = (long)num_sms_topk() * kCtasPerSm;
+    const int per = (int)((total + slots - 1) / slots);
+    const int grid = (int)((total + per - 1) / per);
     auto kern = (a.dtype == DDTREE_BF16) ? topk_kernel<true> : topk_kernel<false>;
-    cudaError_t e = launch_pdl(kern, grid, dim3(kThreads), 0, s, a.logits, a.V, a.row_stride,
-                               a.K, nch, aligned, a.topk_idx, a.topk_logp, a.lse, parts);
+    cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kThreads), ring, s, a.logits, a.V,
+                               a.row_stride, a.K, nch, aligned, (int)total, per, a.topk_idx,
+                               a.topk_logp, a.lse, parts, a.err);
     if (e != cudaSuccess || nch <= 1) return e;
     return launch_pdl(topk_merge_kernel, dim3(a.rows), dim3(kMergeThreads), 0, s,
                       (const TopkPartial*)parts, nch, a.K, a.topk_idx, a.topk_logp, a.lse);
