@@ -132,6 +132,24 @@ struct SmemChunk {
         }
     }
 
+    // acc += 2^(x c + off) over the vector's elements, two per packed op.
+    DDT_DEV static void exp_sum(const uint4& w, float c, float off, float2& acc) {
+        const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+        if (BF16) {
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const float2 y = ffma2(make_float2(bf16lo(a[p]), bf16hi(a[p])), c, off);
+                acc = fadd2(acc, make_float2(fast_exp2(y.x), fast_exp2(y.y)));
+            }
+        } else {
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                const float2 y = ffma2(make_float2(__uint_as_float(a[2 * p]), __uint_as_float(a[2 * p + 1])), c, off);
+                acc = fadd2(acc, make_float2(fast_exp2(y.x), fast_exp2(y.y)));
+            }
+        }
+    }
+
     // Largest element of a vector (bf16: packed max, two elements per op).
     DDT_DEV static float vmax(const uint4& w) {
         if (BF16) {

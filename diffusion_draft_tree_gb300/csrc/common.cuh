@@ -128,6 +128,58 @@ DDT_DEV bool ticket_is_last(unsigned int* counter, unsigned int expected) {
     return last;
 }
 
+// Two floats rounded to a bf16 pair (lo in the low half).
+DDT_DEV uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// Packed fp32x2 arithmetic (two lanes per instruction on sm_100-class GPUs).
+DDT_DEV float2 ffma2(float2 a, float b, float c) {
+    unsigned long long A, B, C, R;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(B) : "f"(b));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(C) : "f"(c));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(R) : "l"(A), "l"(B), "l"(C));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(R));
+    return r;
+}
+DDT_DEV float2 fadd2(float2 a, float2 b) {
+    unsigned long long A, B, R;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b.x), "f"(b.y));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(R) : "l"(A), "l"(B));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(R));
+    return r;
+}
+
+// K-th largest (with multiplicity) of one uint32 per lane, K in [1, 32];
+// warp-collective.  Small K: remove the maximum K-1 times (one reduction, one
+// ballot each); larger K: a bitonic sort.
+DDT_DEV uint32_t warp_kth_largest(uint32_t v, int K) {
+    const int lane = threadIdx.x & 31;
+    if (K <= 12) {
+        for (int r = 1; r < K; ++r) {
+            const uint32_t mx = __reduce_max_sync(0xffffffffu, v);
+            const unsigned holders = __ballot_sync(0xffffffffu, v == mx);
+            if (lane == __ffs(holders) - 1) v = 0u;
+        }
+        return __reduce_max_sync(0xffffffffu, v);
+    }
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const uint32_t o = __shfl_xor_sync(0xffffffffu, v, j);
+            const bool keep_max = (((lane & k) == 0) == ((lane & j) == 0));
+            v = keep_max ? max(v, o) : min(v, o);
+        }
+    }
+    return __shfl_sync(0xffffffffu, v, K - 1);
+}
+
 // Number of a[0..n) larger than x, for a rank by counting.  a is 16-byte
 // aligned shared memory read by every thread of a warp at once (broadcast),
 // two keys per load, eight loads in flight.

@@ -3,19 +3,21 @@
 // Draft Trees", §3 marginals q_i; §4.3 log-probabilities; App. A restricted
 // prefix set).
 //
-// One row = one (sequence, draft position), V logits.  A row is split into
-// chunks of 16 KB (8192 bf16 or 4096 fp32 logits), one CTA per (chunk, row),
-// so even a single sequence fills the GPU.  A CTA brings its chunk into shared
-// memory with one bulk copy and computes from there, touching HBM once:
-//   m_c = max, s_c = sum exp(x - m_c), and its K best (value, index) keys.
-// Top-K selection avoids per-element insertion: every warp finds tau_w, the
-// K-th largest of its 32 lane maxima (a warp bitonic sort), the CTA takes
+// One row = one (sequence, draft position), V logits, split into chunks of
+// 32 KB (16384 bf16 or 8192 fp32 logits).  A persistent wave of CTAs streams
+// the (row, chunk) list, each CTA a contiguous run of chunks through a ring of
+// shared-memory stages filled by bulk copies a few chunks ahead, so HBM is
+// read once and stays busy.  Per chunk, one pass over shared memory gives
+// every vector's maximum and each thread's online (max, sum of exponentials);
+// from those come the chunk's m_c = max, s_c = sum exp(x - m_c), and its K
+// best (value, index) keys.  Top-K selection avoids per-element insertion:
+// every warp finds tau_w, the K-th largest of its 32 lane maxima, the CTA takes
 // tau = max_w tau_w -- a lower bound on the chunk's K-th largest value -- and
-// only elements >= tau (typically ~2K of 8K) are appended to a shared buffer
-// (one shared atomic per warp), then sorted by one warp (or ranked by
-// counting when there are more than 32).  A second, PDL-chained kernel (one
-// warp per row) merges each row's chunk partials the same way -- the keys at
-// or above the largest chunk-K-th key, sorted -- and forms the logsumexp.
+// only elements >= tau (typically ~2K) are appended to a shared buffer (one
+// shared atomic per warp), then sorted by one warp (or ranked by counting when
+// there are more than 32).  A second, PDL-chained kernel (one warp per row)
+// merges each row's chunk partials the same way -- the keys at or above the
+// largest chunk-K-th key, sorted -- and forms the logsumexp.
 #include <mutex>
 
 #include "chunk.cuh"
@@ -28,10 +30,10 @@ namespace ddt {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kChunkBytes = 16384;
+constexpr int kChunkBytes = 32768;
 constexpr int kCandCap = 1024;
 constexpr int kMaxChunks = 128;
-constexpr int kStages = 4;       // chunks in flight per CTA
+constexpr int kStages = 3;       // chunks in flight per CTA
 constexpr int kCtasPerSm = 2;
 
 struct TopkPartial {
@@ -39,21 +41,6 @@ struct TopkPartial {
     float s;   // sum exp(x - m) over the chunk
     uint64_t keys[DDTREE_MAX_K];
 };
-
-// Warp-wide bitonic sort of one uint32 per lane, descending.
-DDT_DEV uint32_t warp_sort_desc_u32(uint32_t v) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            const uint32_t o = __shfl_xor_sync(0xffffffffu, v, j);
-            const bool keep_max = (((lane & k) == 0) == ((lane & j) == 0));
-            v = keep_max ? max(v, o) : min(v, o);
-        }
-    }
-    return v;
-}
 
 // Rank of every key of cand[0..cnt) (keys are distinct) by counting the larger
 // ones; keys of rank < K land in sel[rank].  Whole CTA; sel must be zeroed.
@@ -129,21 +116,45 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
         }
         const uint4* vec = reinterpret_cast<const uint4*>(s_ring + (j % kStages) * Chunk::BYTES);
 
-        // ---- pass 1: lane maxima; tau_w = K-th largest lane maximum of the warp ------
-        float tmax = -INFINITY;
+        // ---- one pass over the chunk: every vector's maximum, and per thread an
+        // online (max, sum of exponentials), rescaled when its maximum grows ----
+        float vmx[PER];
+        float mt = -INFINITY;
+        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < PER; ++i) tmax = fmaxf(tmax, Chunk::vmax(vec[tid + i * kThreads]));
+        for (int i = 0; i < PER; ++i) {
+            const uint4 w = vec[tid + i * kThreads];
+            const float vm = Chunk::vmax(w);
+            vmx[i] = vm;
+            if (vm > mt) {
+                const float f = fast_exp2((mt - vm) * kLog2e);  // 0 while mt = -inf
+                acc.x *= f;
+                acc.y *= f;
+                mt = vm;
+            }
+            if (mt != -INFINITY) Chunk::exp_sum(w, kLog2e, -mt * kLog2e, acc);
+        }
+        float st = acc.x + acc.y;
+        // tau_w = the K-th largest lane maximum of the warp: the chunk has >= K
+        // elements >= it, so its top K are among the elements >= tau = max_w tau_w.
         const bool has = c0 + tid * VEC < V;
-        const uint32_t lane_ord = has ? ord_from_float(tmax) : 0u;
-        const uint32_t tau_w = __shfl_sync(0xffffffffu, warp_sort_desc_u32(lane_ord), K - 1);
-        const float wmax = warp_max(tmax);
+        const uint32_t tau_w = warp_kth_largest(has ? ord_from_float(mt) : 0u, K);
+        // the warp's (max, sum), each lane's sum rescaled to the warp maximum
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float mo = __shfl_xor_sync(0xffffffffu, mt, o);
+            const float so = __shfl_xor_sync(0xffffffffu, st, o);
+            const float mx = fmaxf(mt, mo);
+            st = (mt == -INFINITY ? 0.f : st * fast_exp2((mt - mx) * kLog2e)) +
+                 (mo == -INFINITY ? 0.f : so * fast_exp2((mo - mx) * kLog2e));
+            mt = mx;
+        }
         if (lane == 0) {
-            s_wmax[warp] = wmax;
+            s_wmax[warp] = mt;
+            s_wsum[warp] = st;
             s_wtau[warp] = tau_w;
         }
         __syncthreads();
-        // The chunk has >= K elements >= the value with order tau (K lane maxima of
-        // one warp), so its top K are among the elements >= that value.
         float m = s_wmax[0];
         uint32_t tau = s_wtau[0];
 #pragma unroll
@@ -151,22 +162,21 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
             m = fmaxf(m, s_wmax[i]);
             tau = max(tau, s_wtau[i]);
         }
-
-        // ---- pass 2: sum of exponentials; candidates -----------------------------------
         const float ref = (m == -INFINITY) ? 0.f : m;
-        const float off = -ref * kLog2e;
+        float S = 0.f;
+#pragma unroll
+        for (int i = 0; i < kThreads / 32; ++i)
+            S += s_wmax[i] == -INFINITY ? 0.f : s_wsum[i] * fast_exp2((s_wmax[i] - ref) * kLog2e);
+
+        // ---- candidates: elements >= tau, from the vectors whose maximum reaches it ----
         const float tv = (tau == 0u) ? -INFINITY : float_from_ord(tau);
-        float ssum = 0.f;
         int mine = 0;  // this thread's candidates
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
-            const int v = tid + i * kThreads;
-            const uint4 w = vec[v];
-            float x[VEC];
-            Chunk::unpack(w, x);
-#pragma unroll
-            for (int k = 0; k < VEC; ++k) ssum += fast_exp2(fmaf(x[k], kLog2e, off));
-            if (Chunk::vmax(w) >= tv) {
+            if (vmx[i] >= tv) {
+                const int v = tid + i * kThreads;
+                float x[VEC];
+                Chunk::unpack(vec[v], x);
 #pragma unroll
                 for (int k = 0; k < VEC; ++k) mine += (x[k] >= tv && c0 + v * VEC + k < V) ? 1 : 0;
             }
@@ -186,10 +196,9 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
 #pragma unroll
             for (int i = 0; i < PER; ++i) {
                 const int v = tid + i * kThreads;
-                const uint4 w = vec[v];
-                if (Chunk::vmax(w) >= tv) {
+                if (vmx[i] >= tv) {
                     float x[VEC];
-                    Chunk::unpack(w, x);
+                    Chunk::unpack(vec[v], x);
 #pragma unroll
                     for (int k = 0; k < VEC; ++k) {
                         const int e = c0 + v * VEC + k;
@@ -201,8 +210,6 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
                 }
             }
         }
-        ssum = warp_sum(ssum);
-        if (lane == 0) s_wsum[warp] = ssum;
         __syncthreads();
         const int cnt = s_cnt;
 
@@ -244,10 +251,7 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
         }
         __syncthreads();
 
-        float S = 0.f;
-#pragma unroll
-        for (int i = 0; i < kThreads / 32; ++i) S += s_wsum[i];
-        float M = ref;
+        const float M = ref;
 
         if (nchunks > 1) {  // the merge kernel finishes the row
             if (warp == 0) {

@@ -92,32 +92,6 @@ struct Params {
     uint32_t* err;
 };
 
-DDT_DEV uint32_t pack_bf16x2(float lo, float hi) {
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-// Packed fp32x2 arithmetic (two lanes per instruction on sm_100-class GPUs).
-DDT_DEV float2 ffma2(float2 a, float b, float c) {
-    unsigned long long A, B, C, R;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a.x), "f"(a.y));
-    asm("mov.b64 %0, {%1, %1};" : "=l"(B) : "f"(b));
-    asm("mov.b64 %0, {%1, %1};" : "=l"(C) : "f"(c));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(R) : "l"(A), "l"(B), "l"(C));
-    float2 r;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(R));
-    return r;
-}
-DDT_DEV float2 fadd2(float2 a, float2 b) {
-    unsigned long long A, B, R;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a.x), "f"(a.y));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b.x), "f"(b.y));
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(R) : "l"(A), "l"(B));
-    float2 r;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(R));
-    return r;
-}
-
 // Named barrier over the 256 softmax threads (both query tiles).
 DDT_DEV void softmax_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 // ... and the AND of `v` over them.

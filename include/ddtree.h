@@ -106,10 +106,10 @@ ddtree_status ddtree_topk(const void* draft_logits, int dtype, int rows, int V,
  * process exits); the call allocates nothing.  It needs
  * ddtree_workspace_size(DDTREE_OP_TOPK, ...) bytes of it; a larger problem is
  * rejected with DDTREE_ERR_UNSUPPORTED before anything is enqueued (for
- * V = 151936 bf16 that is about 200 rows).
+ * V = 151936 bf16 that is about 390 rows).
  * The first call made on a device looks up the array's device address on that
- * device (make it with the device current, before any stream capture).  Each
- * call zeroes the counters it needs with cudaMemsetAsync on `stream`.  All
+ * device (make it with the device current, before any stream capture).  Every
+ * partial a call reads is written by that call, so nothing is cleared.  All
  * calls share the one array: calls whose kernels can overlap on the GPU (other
  * streams, other threads) race and give wrong results; serialise them. */
 ddtree_status ddtree_topk_noalloc(const void* draft_logits, int dtype, int rows, int V,
