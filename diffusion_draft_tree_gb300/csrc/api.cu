@@ -62,11 +62,10 @@ const char* ddtree_status_str(ddtree_status s) {
 
 size_t ddtree_workspace_size(ddtree_op op, int B, int L, int N, int V, int K, int dtype, int Hq,
                              int Hkv, int D, int64_t cache_cap) {
-    (void)K;
     switch (op) {
         case DDTREE_OP_TOPK:
             if (B <= 0 || V <= 0 || (dtype != DDTREE_BF16 && dtype != DDTREE_FP32)) return 0;
-            return ddt::topk_workspace_bytes(B * (L > 0 ? L : 1), V, dtype);
+            return ddt::topk_workspace_bytes(B * (L > 0 ? L : 1), V, dtype, K);
         case DDTREE_OP_TREE_ATTN:
             if (B <= 0 || N < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || cache_cap < 0) return 0;
             return ddt::attn_workspace_bytes(B, N, Hq, Hkv, D, cache_cap);
@@ -87,7 +86,7 @@ ddtree_status ddtree_topk(const void* draft_logits, int dtype, int rows, int V,
         return DDTREE_ERR_INVALID_ARG;
     if (K > DDTREE_MAX_K || !ddt::topk_supported(V, dtype, K)) return DDTREE_ERR_UNSUPPORTED;
     if (!aligned(draft_logits, dtype == DDTREE_BF16 ? 2 : 4)) return DDTREE_ERR_INVALID_ARG;
-    const size_t need = ddt::topk_workspace_bytes(rows, V, dtype);
+    const size_t need = ddt::topk_workspace_bytes(rows, V, dtype, K);
     if (need && (!workspace || ws_bytes < need || !aligned(workspace, 256)))
         return DDTREE_ERR_INVALID_ARG;
     ddt::TopkArgs a{draft_logits, dtype, rows, V, row_stride, K, topk_idx, topk_logp, lse,

@@ -132,20 +132,21 @@ struct SmemChunk {
         }
     }
 
-    // acc += 2^(x c + off) over the vector's elements, two per packed op.
-    DDT_DEV static void exp_sum(const uint4& w, float c, float off, float2& acc) {
+    // a0 + a1 += 2^(x c + off) over the vector's elements (two sums, so that
+    // the additions form two independent chains).
+    DDT_DEV static void exp_sum(const uint4& w, float c, float off, float& a0, float& a1) {
         const uint32_t a[4] = {w.x, w.y, w.z, w.w};
         if (BF16) {
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
-                const float2 y = ffma2(make_float2(bf16lo(a[p]), bf16hi(a[p])), c, off);
-                acc = fadd2(acc, make_float2(fast_exp2(y.x), fast_exp2(y.y)));
+                a0 += fast_exp2(fmaf(bf16lo(a[p]), c, off));
+                a1 += fast_exp2(fmaf(bf16hi(a[p]), c, off));
             }
         } else {
 #pragma unroll
             for (int p = 0; p < 2; ++p) {
-                const float2 y = ffma2(make_float2(__uint_as_float(a[2 * p]), __uint_as_float(a[2 * p + 1])), c, off);
-                acc = fadd2(acc, make_float2(fast_exp2(y.x), fast_exp2(y.y)));
+                a0 += fast_exp2(fmaf(__uint_as_float(a[2 * p]), c, off));
+                a1 += fast_exp2(fmaf(__uint_as_float(a[2 * p + 1]), c, off));
             }
         }
     }
