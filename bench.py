@@ -214,7 +214,7 @@ def gpu_arm(args, rank, world, dev):
         torch.bfloat16)
     i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
     ws = {"topk": ops.alloc_workspace(ops.workspace_size(ops.OP_TOPK, B=w.B, L=w.L, V=w.V,
-                                                         dtype=w.dtype), dev),
+                                                         K=w.K, dtype=w.dtype), dev),
           "attn": ops.alloc_workspace(ops.workspace_size(ops.OP_TREE_ATTN, B=w.B, N=w.N,
                                                          Hq=w.Hq, Hkv=w.Hkv, D=w.D,
                                                          cache_cap=w.P_cap), dev),

@@ -187,7 +187,7 @@ def topk(draft_logits: torch.Tensor, K: int, workspace=None, stream=None):
     lse = torch.empty((x.shape[0],), dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = alloc_workspace(workspace_size(OP_TOPK, B=x.shape[0], L=1, V=x.shape[1],
-                                                   dtype=_dtype_code(x)), dev)
+                                                   K=K, dtype=_dtype_code(x)), dev)
     ddtree_topk(x, K, idx, lp, lse, workspace, stream)
     return idx.reshape(*lead, K), lp.reshape(*lead, K), lse.reshape(lead)
 

@@ -52,7 +52,8 @@ def test_noalloc_topk_matches_workspace_topk_twice(cuda_device):
              (wl.draft_logits(second).reshape(second.B * second.L, second.V), second.dtype, 16)]
     for raw, dtype, K in cases:
         x = dev_logits(raw, dtype, cuda_device)
-        need = ops.workspace_size(ops.OP_TOPK, B=x.shape[0], L=1, V=x.shape[1], dtype=dtype)
+        need = ops.workspace_size(ops.OP_TOPK, B=x.shape[0], L=1, V=x.shape[1], K=K,
+                                  dtype=dtype)
         assert 0 < need <= SCRATCH_BYTES
         ref_idx, ref_lp, ref_lse = ops.topk(x, K)
         idx, lp, lse = _call_noalloc(x, K)
@@ -67,6 +68,7 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     """Sizes are checked on the host before anything is enqueued: no GPU needed."""
     f = _noalloc()
     fake = ctypes.c_void_p(0x1000)
-    rows = 2000  # 2000 rows of a 151936-token bf16 vocabulary need ~5 MB of partials
-    assert ops.workspace_size(ops.OP_TOPK, B=rows, L=1, V=151936, dtype=ops.BF16) > SCRATCH_BYTES
+    rows = 2000  # 2000 rows of a 151936-token bf16 vocabulary need ~11 MB of partials
+    assert ops.workspace_size(ops.OP_TOPK, B=rows, L=1, V=151936, K=8,
+                              dtype=ops.BF16) > SCRATCH_BYTES
     assert f(fake, ops.BF16, rows, 151936, 151936, 8, fake, fake, None, None) == 2
