@@ -31,8 +31,10 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kChunkBytes = 32768;
-constexpr int kMaxChunks = 128;
+// Chunks are 32 KB when there are enough to keep every CTA streaming, else
+// 16 KB (twice the CTAs, half the work per warp: lower latency).
+constexpr int kChunkBig = 32768, kChunkSmall = 16384;
+constexpr int kMaxChunks = 128;  // per row, at the small size
 constexpr int kStages = 3;       // chunks in flight per CTA
 constexpr int kCtasPerSm = 2;
 constexpr int kWarpCand = 64;    // candidates a warp gathers before its slow path
@@ -88,12 +90,12 @@ DDT_DEV uint64_t warp_top_k(uint64_t* buf, int count, int cap, int K, uint64_t* 
 // (row, chunk) list, streaming them through a ring of kStages shared-memory
 // stages (bulk copies issued kStages-1 chunks ahead).  Warp w of a chunk writes
 // list (row, chunk, w): K keys to keys[list * K], (m, s) to ms[list].
-template <bool BF16>
+template <bool BF16, int CHUNK_BYTES>
 __global__ void __launch_bounds__(kThreads)
 topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, int nchunks,
             bool aligned, int total, int per, float2* __restrict__ ms,
             uint64_t* __restrict__ keys, uint32_t* err) {
-    using Chunk = SmemChunk<BF16, kChunkBytes / (BF16 ? 2 : 4)>;
+    using Chunk = SmemChunk<BF16, CHUNK_BYTES / (BF16 ? 2 : 4)>;
     constexpr int VEC = Chunk::VEC;
     constexpr int VPW = Chunk::NVEC / kWarps;  // vectors per warp
     constexpr int PL = VPW / 32;               // vectors per lane
@@ -225,28 +227,40 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     }
 }
 
-// One warp per row merges the row's nchunks x kWarps lists.  The row's K best
+// One CTA per row merges the row's nchunks x kWarps lists.  The row's K best
 // keys are >= tau2 = the largest K-th key of any list (that list alone holds K
 // keys >= tau2), so only the keys >= tau2 -- usually K to 2K of them -- are
-// sorted (one warp bitonic sort, or ranked by counting when more than 32).
-// The logsumexp combines the lists' (max, sum) pairs.
-constexpr int kMergeThreads = 32;
+// gathered and sorted by one warp (bitonic, or ranked by counting when more
+// than 32).  The logsumexp combines the lists' (max, sum) pairs.  Each thread
+// issues all of its loads before using any, so the row costs one round trip.
+constexpr int kMergeThreads = 128;
+constexpr int kMergeLoads = 8;  // keys per thread per batch of loads
 __global__ void __launch_bounds__(kMergeThreads)
 topk_merge_kernel(const float2* __restrict__ ms, const uint64_t* __restrict__ keys, int nlists,
                   int K, int32_t* __restrict__ topk_idx, float* __restrict__ topk_logp,
                   float* __restrict__ lse) {
     __shared__ __align__(16) uint64_t s_c[kMergeCand];
     __shared__ uint64_t s_sel[DDTREE_MAX_K];
-    const int lane = threadIdx.x;
+    __shared__ uint64_t s_tau[kMergeThreads / 32];
+    __shared__ float s_m[kMergeThreads / 32], s_s[kMergeThreads / 32];
+    __shared__ int s_cnt;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int row = blockIdx.x;
+    if (tid == 0) s_cnt = 0;
     pdl_wait();
     const float2* rms = ms + (size_t)row * nlists;
     const uint64_t* rk = keys + (size_t)row * nlists * K;
     const int nk = nlists * K;
+    // this thread's first batch of keys, in flight with the list loads below
+    uint64_t kv[kMergeLoads];
+#pragma unroll
+    for (int u = 0; u < kMergeLoads; ++u) {
+        const int t = tid + u * kMergeThreads;
+        kv[u] = t < nk ? __ldcg((const unsigned long long*)&rk[t]) : 0ull;
+    }
     uint64_t tau2 = 0ull;
     float mt = -INFINITY, st = 0.f;
-#pragma unroll 4
-    for (int l = lane; l < nlists; l += 32) {
+    for (int l = tid; l < nlists; l += kMergeThreads) {
         tau2 = umax64(tau2, __ldcg((const unsigned long long*)&rk[(size_t)l * K + K - 1]));
         const float2 p = __ldcg(&rms[l]);
         ms_combine(mt, st, p.x, p.y, kLog2e);
@@ -258,21 +272,41 @@ topk_merge_kernel(const float2* __restrict__ ms, const uint64_t* __restrict__ ke
         const float so = __shfl_xor_sync(0xffffffffu, st, o);
         ms_combine(mt, st, mo, so, kLog2e);
     }
-    pdl_trigger();
-    const float M = (mt == -INFINITY) ? 0.f : mt;
-    // keys >= tau2, compacted
-    int cnt = 0;
-#pragma unroll 4
-    for (int t0 = 0; t0 < nk; t0 += 32) {
-        const int t = t0 + lane;
-        const uint64_t key = t < nk ? __ldcg((const unsigned long long*)&rk[t]) : 0ull;
-        const bool in = key >= tau2 && key != 0ull;
-        const unsigned bal = __ballot_sync(0xffffffffu, in);
-        const int at = cnt + __popc(bal & ((1u << lane) - 1u));
-        if (in && at < kMergeCand) s_c[at] = key;
-        cnt += __popc(bal);
+    if (lane == 0) {
+        s_tau[warp] = tau2;
+        s_m[warp] = mt;
+        s_s[warp] = st;
     }
-    __syncwarp();
+    __syncthreads();
+    tau2 = s_tau[0];
+    mt = s_m[0];
+    st = s_s[0];
+#pragma unroll
+    for (int i = 1; i < kMergeThreads / 32; ++i) {
+        tau2 = umax64(tau2, s_tau[i]);
+        ms_combine(mt, st, s_m[i], s_s[i], kLog2e);
+    }
+    pdl_trigger();
+    // gather the keys >= tau2
+    for (int t0 = 0; t0 < nk; t0 += kMergeLoads * kMergeThreads) {
+        if (t0 > 0) {
+#pragma unroll
+            for (int u = 0; u < kMergeLoads; ++u) {
+                const int t = t0 + tid + u * kMergeThreads;
+                kv[u] = t < nk ? __ldcg((const unsigned long long*)&rk[t]) : 0ull;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kMergeLoads; ++u) {
+            if (kv[u] >= tau2 && kv[u] != 0ull) {
+                const int at = atomicAdd(&s_cnt, 1);
+                if (at < kMergeCand) s_c[at] = kv[u];
+            }
+        }
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    const int cnt = s_cnt;
     uint64_t sel;
     if (cnt <= kMergeCand) {
         sel = warp_top_k(s_c, cnt, kMergeCand, K, s_sel);
@@ -292,6 +326,7 @@ topk_merge_kernel(const float2* __restrict__ ms, const uint64_t* __restrict__ ke
             prev = tb;
         }
     }
+    const float M = (mt == -INFINITY) ? 0.f : mt;
     const float logS = logf(st);
     if (lane < K) {
         topk_idx[(size_t)row * K + lane] = (int32_t)key_index(sel);
@@ -300,7 +335,10 @@ topk_merge_kernel(const float2* __restrict__ ms, const uint64_t* __restrict__ ke
     if (lane == 0 && lse) lse[row] = M + logS;
 }
 
-int chunk_elems(int dtype) { return kChunkBytes / (dtype == DDTREE_BF16 ? 2 : 4); }
+int chunks_at(int V, int dtype, int bytes) {
+    const int size = bytes / (dtype == DDTREE_BF16 ? 2 : 4);
+    return (V + size - 1) / size;
+}
 
 // Streaming multiprocessors of the current device (148 if the query fails).
 int num_sms_topk() {
@@ -336,44 +374,49 @@ bool topk_supported(int V, int dtype, int K) {
     return topk_chunks(V, dtype) <= kMaxChunks && K >= 1 && K <= DDTREE_MAX_K;
 }
 
-int topk_chunks(int V, int dtype) {
-    const int size = chunk_elems(dtype);
-    return (V + size - 1) / size;
-}
+int topk_chunks(int V, int dtype) { return chunks_at(V, dtype, kChunkSmall); }
 
 size_t topk_workspace_bytes(int rows, int V, int dtype, int K) {
     return topk_layout(rows, V, dtype, K).total;
 }
 
+template <bool BF16, int BYTES>
+cudaError_t launch_partials(const TopkArgs& a, int nch, bool aligned, int total, int per,
+                            float2* ms, uint64_t* keys, cudaStream_t s) {
+    static std::once_flag once[64];
+    static cudaError_t attr_err[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const size_t ring = (size_t)kStages * BYTES;
+    std::call_once(once[dev & 63], [&] {
+        attr_err[dev & 63] = cudaFuncSetAttribute(
+            topk_kernel<BF16, BYTES>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring);
+    });
+    if (attr_err[dev & 63] != cudaSuccess) return attr_err[dev & 63];
+    const int grid = (total + per - 1) / per;
+    return launch_pdl(topk_kernel<BF16, BYTES>, dim3(grid), dim3(kThreads), ring, s, a.logits,
+                      a.V, a.row_stride, a.K, nch, aligned, total, per, ms, keys, a.err);
+}
+
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
-    const int nch = topk_chunks(a.V, a.dtype);
     const int es = a.dtype == DDTREE_BF16 ? 2 : 4;
     const bool aligned = ((uintptr_t)a.logits % 16 == 0) && ((a.row_stride * es) % 16 == 0);
     const TopkWs wl = topk_layout(a.rows, a.V, a.dtype, a.K);
     float2* ms = (float2*)((char*)a.ws + wl.ms);
     uint64_t* keys = (uint64_t*)((char*)a.ws + wl.keys);
-    static std::once_flag once[64];
-    static cudaError_t attr_err[64];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const size_t ring = (size_t)kStages * kChunkBytes;
-    std::call_once(once[dev & 63], [&] {
-        cudaError_t e = cudaFuncSetAttribute(topk_kernel<true>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(topk_kernel<false>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring);
-        attr_err[dev & 63] = e;
-    });
-    if (attr_err[dev & 63] != cudaSuccess) return attr_err[dev & 63];
     // one wave of persistent CTAs, each streaming a contiguous run of chunks
-    const long total = (long)nch * a.rows;
     const long slots = (long)num_sms_topk() * kCtasPerSm;
+    const bool small = (long)chunks_at(a.V, a.dtype, kChunkSmall) * a.rows <= slots;
+    const int nch = chunks_at(a.V, a.dtype, small ? kChunkSmall : kChunkBig);
+    const long total = (long)nch * a.rows;
     const int per = (int)((total + slots - 1) / slots);
-    const int grid = (int)((total + per - 1) / per);
-    auto kern = (a.dtype == DDTREE_BF16) ? topk_kernel<true> : topk_kernel<false>;
-    cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kThreads), ring, s, a.logits, a.V,
-                               a.row_stride, a.K, nch, aligned, (int)total, per, ms, keys, a.err);
+    cudaError_t e;
+    if (a.dtype == DDTREE_BF16)
+        e = small ? launch_partials<true, kChunkSmall>(a, nch, aligned, (int)total, per, ms, keys, s)
+                  : launch_partials<true, kChunkBig>(a, nch, aligned, (int)total, per, ms, keys, s);
+    else
+        e = small ? launch_partials<false, kChunkSmall>(a, nch, aligned, (int)total, per, ms, keys, s)
+                  : launch_partials<false, kChunkBig>(a, nch, aligned, (int)total, per, ms, keys, s);
     if (e != cudaSuccess) return e;
     return launch_pdl(topk_merge_kernel, dim3(a.rows), dim3(kMergeThreads), 0, s,
                       (const float2*)ms, (const uint64_t*)keys, nch * kWarps, a.K, a.topk_idx,
