@@ -354,12 +354,23 @@ int num_sms_topk() {
     return cached[dev];
 }
 
+// Chunks per row: small ones when even those fit in one wave of CTAs.
+struct ChunkPlan {
+    bool small;
+    int nch;
+};
+ChunkPlan chunk_plan(int rows, int V, int dtype) {
+    const long slots = (long)num_sms_topk() * kCtasPerSm;
+    const bool small = (long)chunks_at(V, dtype, kChunkSmall) * rows <= slots;
+    return {small, chunks_at(V, dtype, small ? kChunkSmall : kChunkBig)};
+}
+
 struct TopkWs {
     size_t ms, keys, total;
 };
 // Workspace: (m, s) of every list, then its K keys (K <= 0: room for any K).
 TopkWs topk_layout(int rows, int V, int dtype, int K) {
-    const size_t lists = (size_t)rows * topk_chunks(V, dtype) * kWarps;
+    const size_t lists = (size_t)rows * chunk_plan(rows, V, dtype).nch * kWarps;
     const size_t kk = (K > 0 && K <= DDTREE_MAX_K) ? (size_t)K : (size_t)DDTREE_MAX_K;
     TopkWs w;
     w.ms = 0;
@@ -406,8 +417,9 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
     uint64_t* keys = (uint64_t*)((char*)a.ws + wl.keys);
     // one wave of persistent CTAs, each streaming a contiguous run of chunks
     const long slots = (long)num_sms_topk() * kCtasPerSm;
-    const bool small = (long)chunks_at(a.V, a.dtype, kChunkSmall) * a.rows <= slots;
-    const int nch = chunks_at(a.V, a.dtype, small ? kChunkSmall : kChunkBig);
+    const ChunkPlan cp = chunk_plan(a.rows, a.V, a.dtype);
+    const bool small = cp.small;
+    const int nch = cp.nch;
     const long total = (long)nch * a.rows;
     const int per = (int)((total + slots - 1) / slots);
     cudaError_t e;
