@@ -88,8 +88,10 @@ DDT_DEV uint64_t warp_top_k(uint64_t* buf, int count, int cap, int K, uint64_t* 
 
 // Persistent: CTA i handles chunks [i per, (i+1) per) of the flattened
 // (row, chunk) list, streaming them through a ring of kStages shared-memory
-// stages (bulk copies issued kStages-1 chunks ahead).  Warp w of a chunk writes
-// list (row, chunk, w): K keys to keys[list * K], (m, s) to ms[list].
+// stages (bulk copies issued kStages-1 chunks ahead).  Every warp selects the
+// K best keys and the (m, s) of its eighth of the chunk; warp 0 merges the
+// eight into the chunk's list (row, chunk): K keys to keys[list * K], (m, s)
+// to ms[list].
 template <bool BF16, int CHUNK_BYTES>
 __global__ void __launch_bounds__(kThreads)
 topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, int nchunks,
@@ -103,6 +105,8 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     __shared__ __align__(8) uint64_t s_bar[kStages];
     __shared__ __align__(16) uint64_t s_wc[kWarps][kWarpCand];
     __shared__ uint64_t s_wsel[kWarps][DDTREE_MAX_K];
+    __shared__ __align__(16) uint64_t s_cc[kWarps * DDTREE_MAX_K];
+    __shared__ float2 s_wms[kWarps];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int w0 = blockIdx.x * per;
@@ -220,47 +224,68 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
                 prev = tb;
             }
         }
-        const size_t list = (size_t)w * kWarps + warp;
-        if (lane < K) keys[list * K + lane] = sel;
-        if (lane == 0) ms[list] = make_float2(m_w, s_w);
+        if (lane < K) s_wsel[warp][lane] = sel;
+        if (lane == 0) s_wms[warp] = make_float2(m_w, s_w);
+        __syncthreads();
+        if (warp == 0) {
+            // the chunk's list: the K best of the warps' lists, keys >= the
+            // largest warp-K-th key (that warp alone holds K keys >= it)
+            uint64_t tau = lane < kWarps ? s_wsel[lane][K - 1] : 0ull;
+            float2 p = lane < kWarps ? s_wms[lane] : make_float2(-INFINITY, 0.f);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                tau = umax64(tau, shfl_xor_u64(tau, o));
+                const float mo = __shfl_xor_sync(0xffffffffu, p.x, o);
+                const float so = __shfl_xor_sync(0xffffffffu, p.y, o);
+                ms_combine(p.x, p.y, mo, so, kLog2e);
+            }
+            int cnt = 0;
+            for (int t0 = 0; t0 < kWarps * K; t0 += 32) {
+                const int t = t0 + lane, wv = t / K;
+                const uint64_t key = t < kWarps * K ? s_wsel[wv][t - wv * K] : 0ull;
+                const bool in = key >= tau && key != 0ull;
+                const unsigned bal = __ballot_sync(0xffffffffu, in);
+                if (in) s_cc[cnt + __popc(bal & ((1u << lane) - 1u))] = key;
+                cnt += __popc(bal);
+            }
+            __syncwarp();
+            const uint64_t best = warp_top_k(s_cc, cnt, kWarps * DDTREE_MAX_K, K, s_wsel[0]);
+            if (lane < K) keys[(size_t)w * K + lane] = best;
+            if (lane == 0) ms[w] = p;
+        }
         __syncthreads();  // the stage and the candidate buffers are free again
     }
 }
 
-// One CTA per row merges the row's nchunks x kWarps lists.  The row's K best
-// keys are >= tau2 = the largest K-th key of any list (that list alone holds K
-// keys >= tau2), so only the keys >= tau2 -- usually K to 2K of them -- are
-// gathered and sorted by one warp (bitonic, or ranked by counting when more
-// than 32).  The logsumexp combines the lists' (max, sum) pairs.  Each thread
-// issues all of its loads before using any, so the row costs one round trip.
-constexpr int kMergeThreads = 128;
-constexpr int kMergeLoads = 8;  // keys per thread per batch of loads
+// One warp per row merges the row's nchunks lists.  The row's K best keys are
+// >= tau2 = the largest K-th key of any list (that list alone holds K keys >=
+// tau2), so only the keys >= tau2 -- usually K to 2K of them -- are gathered
+// and sorted (bitonic, or ranked by counting when more than 32).  The
+// logsumexp combines the lists' (max, sum) pairs.  Each lane issues its loads
+// in batches before using any.
+constexpr int kMergeThreads = 32;
+constexpr int kMergeLoads = 8;
 __global__ void __launch_bounds__(kMergeThreads)
 topk_merge_kernel(const float2* __restrict__ ms, const uint64_t* __restrict__ keys, int nlists,
                   int K, int32_t* __restrict__ topk_idx, float* __restrict__ topk_logp,
                   float* __restrict__ lse) {
     __shared__ __align__(16) uint64_t s_c[kMergeCand];
     __shared__ uint64_t s_sel[DDTREE_MAX_K];
-    __shared__ uint64_t s_tau[kMergeThreads / 32];
-    __shared__ float s_m[kMergeThreads / 32], s_s[kMergeThreads / 32];
-    __shared__ int s_cnt;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lane = threadIdx.x;
     const int row = blockIdx.x;
-    if (tid == 0) s_cnt = 0;
     pdl_wait();
     const float2* rms = ms + (size_t)row * nlists;
     const uint64_t* rk = keys + (size_t)row * nlists * K;
     const int nk = nlists * K;
-    // this thread's first batch of keys, in flight with the list loads below
     uint64_t kv[kMergeLoads];
 #pragma unroll
     for (int u = 0; u < kMergeLoads; ++u) {
-        const int t = tid + u * kMergeThreads;
+        const int t = lane + 32 * u;
         kv[u] = t < nk ? __ldcg((const unsigned long long*)&rk[t]) : 0ull;
     }
     uint64_t tau2 = 0ull;
     float mt = -INFINITY, st = 0.f;
-    for (int l = tid; l < nlists; l += kMergeThreads) {
+    for (int l = lane; l < nlists; l += 32) {
         tau2 = umax64(tau2, __ldcg((const unsigned long long*)&rk[(size_t)l * K + K - 1]));
         const float2 p = __ldcg(&rms[l]);
         ms_combine(mt, st, p.x, p.y, kLog2e);
@@ -272,41 +297,26 @@ topk_merge_kernel(const float2* __restrict__ ms, const uint64_t* __restrict__ ke
         const float so = __shfl_xor_sync(0xffffffffu, st, o);
         ms_combine(mt, st, mo, so, kLog2e);
     }
-    if (lane == 0) {
-        s_tau[warp] = tau2;
-        s_m[warp] = mt;
-        s_s[warp] = st;
-    }
-    __syncthreads();
-    tau2 = s_tau[0];
-    mt = s_m[0];
-    st = s_s[0];
-#pragma unroll
-    for (int i = 1; i < kMergeThreads / 32; ++i) {
-        tau2 = umax64(tau2, s_tau[i]);
-        ms_combine(mt, st, s_m[i], s_s[i], kLog2e);
-    }
     pdl_trigger();
-    // gather the keys >= tau2
-    for (int t0 = 0; t0 < nk; t0 += kMergeLoads * kMergeThreads) {
+    int cnt = 0;
+    for (int t0 = 0; t0 < nk; t0 += 32 * kMergeLoads) {
         if (t0 > 0) {
 #pragma unroll
             for (int u = 0; u < kMergeLoads; ++u) {
-                const int t = t0 + tid + u * kMergeThreads;
+                const int t = t0 + lane + 32 * u;
                 kv[u] = t < nk ? __ldcg((const unsigned long long*)&rk[t]) : 0ull;
             }
         }
 #pragma unroll
         for (int u = 0; u < kMergeLoads; ++u) {
-            if (kv[u] >= tau2 && kv[u] != 0ull) {
-                const int at = atomicAdd(&s_cnt, 1);
-                if (at < kMergeCand) s_c[at] = kv[u];
-            }
+            const bool in = kv[u] >= tau2 && kv[u] != 0ull;
+            const unsigned bal = __ballot_sync(0xffffffffu, in);
+            const int at = cnt + __popc(bal & ((1u << lane) - 1u));
+            if (in && at < kMergeCand) s_c[at] = kv[u];
+            cnt += __popc(bal);
         }
     }
-    __syncthreads();
-    if (warp != 0) return;
-    const int cnt = s_cnt;
+    __syncwarp();
     uint64_t sel;
     if (cnt <= kMergeCand) {
         sel = warp_top_k(s_c, cnt, kMergeCand, K, s_sel);
@@ -370,7 +380,7 @@ struct TopkWs {
 };
 // Workspace: (m, s) of every list, then its K keys (K <= 0: room for any K).
 TopkWs topk_layout(int rows, int V, int dtype, int K) {
-    const size_t lists = (size_t)rows * chunk_plan(rows, V, dtype).nch * kWarps;
+    const size_t lists = (size_t)rows * chunk_plan(rows, V, dtype).nch;
     const size_t kk = (K > 0 && K <= DDTREE_MAX_K) ? (size_t)K : (size_t)DDTREE_MAX_K;
     TopkWs w;
     w.ms = 0;
@@ -431,7 +441,7 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
                   : launch_partials<false, kChunkBig>(a, nch, aligned, (int)total, per, ms, keys, s);
     if (e != cudaSuccess) return e;
     return launch_pdl(topk_merge_kernel, dim3(a.rows), dim3(kMergeThreads), 0, s,
-                      (const float2*)ms, (const uint64_t*)keys, nch * kWarps, a.K, a.topk_idx,
+                      (const float2*)ms, (const uint64_t*)keys, nch, a.K, a.topk_idx,
                       a.topk_logp, a.lse);
 }
 
