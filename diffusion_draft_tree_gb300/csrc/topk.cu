@@ -37,7 +37,6 @@ constexpr int kChunkBig = 32768, kChunkSmall = 16384;
 constexpr int kMaxChunks = 128;  // per row, at the small size
 constexpr int kStages = 3;       // chunks in flight per CTA
 constexpr int kCtasPerSm = 2;
-constexpr int kWarpCand = 64;    // candidates a warp gathers before its slow path
 constexpr int kMergeCand = 1024; // candidates the merge gathers before its slow path
 
 // Warp-wide bitonic sort of one uint64 per lane, descending (lane 0 largest).
@@ -63,10 +62,12 @@ DDT_DEV void ms_combine(float& m, float& s, float m2, float s2, float c) {
     m = mx;
 }
 
-// The K largest of up to kWarpCand (or any number, on the slow path) candidate
-// keys: lanes < K return them in descending order, the others 0.
-// `count` keys are in buf (when count <= cap).
-DDT_DEV uint64_t warp_top_k(uint64_t* buf, int count, int cap, int K, uint64_t* sel) {
+// The K largest of the `count` candidate keys in buf: lanes < K return them in
+// descending order, the others 0.  Not inlined: it is called at two places of
+// the streaming loop, whose code must stay small enough for the instruction
+// cache.
+__device__ __noinline__ uint64_t warp_top_k(uint64_t* buf, int count, int cap, int K,
+                                            uint64_t* sel) {
     const int lane = threadIdx.x & 31;
     if (count <= 32) {
         const uint64_t key = warp_sort_desc_u64(lane < count ? buf[lane] : 0ull);
@@ -86,27 +87,75 @@ DDT_DEV uint64_t warp_top_k(uint64_t* buf, int count, int cap, int K, uint64_t* 
     return key;
 }
 
+// Per chunk, the streaming kernel leaves its (m, s), a bound tau on its K-th
+// largest value (as an order key) and every key >= tau -- usually K to 2K of
+// them, at most kChunkCand; a chunk with more (degenerate ties) keeps exactly
+// its K best, sorted, and sets tau to the K-th.
+constexpr int kChunkCand = 64;
+struct ChunkOut {
+    float m, s;       // max, sum exp(x - m)
+    uint32_t tau;     // ord key: the chunk has >= K elements >= it
+    int count;        // keys below
+    uint64_t keys[kChunkCand];
+};
+
+// Exact K best keys of a chunk by K rounds of a CTA-wide maximum below the
+// previous one (all threads call it; correctness only, kept out of line).
+// Thread 0 writes them to out->keys.
+template <typename Chunk>
+__device__ __noinline__ void cta_exact_top_k(const uint4* vec, int c0, int V, int K,
+                                             uint64_t* s_red, ChunkOut* out) {
+    constexpr int VEC = Chunk::VEC;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint64_t prev = ~0ull;
+    for (int r = 0; r < K; ++r) {
+        uint64_t tb = 0ull;
+#pragma unroll 1
+        for (int v = tid; v < Chunk::NVEC; v += kThreads) {
+            float x[VEC];
+            Chunk::unpack(vec[v], x);
+            for (int k = 0; k < VEC; ++k) {
+                const int e = c0 + v * VEC + k;
+                if (e < V) {
+                    const uint64_t key = value_index_key(x[k], (uint32_t)e);
+                    if (key < prev && key > tb) tb = key;
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tb = umax64(tb, shfl_xor_u64(tb, o));
+        if (lane == 0) s_red[warp] = tb;
+        __syncthreads();
+        tb = s_red[0];
+        for (int i = 1; i < kWarps; ++i) tb = umax64(tb, s_red[i]);
+        if (tid == 0) out->keys[r] = tb;
+        prev = tb;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        out->count = K;
+        out->tau = (uint32_t)(prev >> 32);
+    }
+}
+
 // Persistent: CTA i handles chunks [i per, (i+1) per) of the flattened
 // (row, chunk) list, streaming them through a ring of kStages shared-memory
-// stages (bulk copies issued kStages-1 chunks ahead).  Every warp selects the
-// K best keys and the (m, s) of its eighth of the chunk; warp 0 merges the
-// eight into the chunk's list (row, chunk): K keys to keys[list * K], (m, s)
-// to ms[list].
+// stages (bulk copies issued kStages-1 chunks ahead), and writes one ChunkOut
+// per chunk.  Warps own eighths of the chunk until the chunk's tau is known.
 template <bool BF16, int CHUNK_BYTES>
 __global__ void __launch_bounds__(kThreads)
 topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, int nchunks,
-            bool aligned, int total, int per, float2* __restrict__ ms,
-            uint64_t* __restrict__ keys, uint32_t* err) {
+            bool aligned, int total, int per, ChunkOut* __restrict__ outs, uint32_t* err) {
     using Chunk = SmemChunk<BF16, CHUNK_BYTES / (BF16 ? 2 : 4)>;
     constexpr int VEC = Chunk::VEC;
     constexpr int VPW = Chunk::NVEC / kWarps;  // vectors per warp
     constexpr int PL = VPW / 32;               // vectors per lane
     extern __shared__ __align__(128) uint8_t s_ring[];  // kStages x Chunk::BYTES
     __shared__ __align__(8) uint64_t s_bar[kStages];
-    __shared__ __align__(16) uint64_t s_wc[kWarps][kWarpCand];
-    __shared__ uint64_t s_wsel[kWarps][DDTREE_MAX_K];
-    __shared__ __align__(16) uint64_t s_cc[kWarps * DDTREE_MAX_K];
+    __shared__ uint32_t s_wtau[kWarps];
     __shared__ float2 s_wms[kWarps];
+    __shared__ uint64_t s_red[kWarps];
+    __shared__ int s_cnt;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int w0 = blockIdx.x * per;
@@ -129,12 +178,14 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
         if (j == nmine - 1) pdl_trigger();
         const int w = w0 + j;
         const int c0 = (w % nchunks) * Chunk::SIZE;
+        ChunkOut* out = outs + w;
+        if (tid == 0) s_cnt = 0;
         if (!Chunk::wait_ring(&s_bar[j % kStages], (uint32_t)((j / kStages) & 1))) {
             if (tid == 0) record_error(err, ERR_TOPK | ERR_WAIT_TIMEOUT);
             return;  // a copy never landed
         }
-        const uint4* vw = reinterpret_cast<const uint4*>(s_ring + (j % kStages) * Chunk::BYTES) +
-                          warp * VPW;
+        const uint4* vec = reinterpret_cast<const uint4*>(s_ring + (j % kStages) * Chunk::BYTES);
+        const uint4* vw = vec + warp * VPW;
         const int e_lane = c0 + (warp * VPW + lane) * VEC;  // first element of the lane
 
         // ---- one pass: vector maxima, and the lane's online (max, sum of exps) ----
@@ -153,9 +204,8 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
             }
             if (mt != -INFINITY) Chunk::exp_sum(v, kLog2e, -mt * kLog2e, a0, a1);
         }
-        // tau_w: the warp has >= K elements >= it (K lanes' maxima)
+        // tau_w: the warp's slice has >= K elements >= it (K lanes' maxima)
         const uint32_t tau_w = warp_kth_largest(e_lane < V ? ord_from_float(mt) : 0u, K);
-        const float tv = (tau_w == 0u) ? -INFINITY : float_from_ord(tau_w);
         float m_w = mt, s_w = a0 + a1;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -163,8 +213,17 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
             const float so = __shfl_xor_sync(0xffffffffu, s_w, o);
             ms_combine(m_w, s_w, mo, so, kLog2e);
         }
+        if (lane == 0) {
+            s_wtau[warp] = tau_w;
+            s_wms[warp] = make_float2(m_w, s_w);
+        }
+        __syncthreads();
+        uint32_t tau = s_wtau[0];
+#pragma unroll
+        for (int i = 1; i < kWarps; ++i) tau = max(tau, s_wtau[i]);
+        const float tv = (tau == 0u) ? -INFINITY : float_from_ord(tau);
 
-        // ---- candidates: elements >= tau_w of the vectors whose maximum reaches it ----
+        // ---- the chunk's keys >= tau, from the vectors whose maximum reaches it ----
         int mine = 0;
 #pragma unroll
         for (int i = 0; i < PL; ++i) {
@@ -182,153 +241,137 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
             const int t = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += t;
         }
-        const int count = __shfl_sync(0xffffffffu, incl, 31);
-        uint64_t sel;
-        if (count <= kWarpCand) {
-            int pos = incl - mine;
+        int wbase = 0;
+        if (lane == 31 && incl > 0) wbase = atomicAdd(&s_cnt, incl);
+        wbase = __shfl_sync(0xffffffffu, wbase, 31);
+        if (mine) {
+            int pos = wbase + incl - mine;
 #pragma unroll
             for (int i = 0; i < PL; ++i) {
-                if (mine && vmx[i] >= tv) {
+                if (vmx[i] >= tv) {
                     float x[VEC];
                     Chunk::unpack(vw[lane + 32 * i], x);
                     const int e = e_lane + 32 * i * VEC;
 #pragma unroll
-                    for (int k = 0; k < VEC; ++k)
-                        if (x[k] >= tv && e + k < V)
-                            s_wc[warp][pos++] = value_index_key(x[k], (uint32_t)(e + k));
-                }
-            }
-            __syncwarp();
-            sel = warp_top_k(s_wc[warp], count, kWarpCand, K, s_wsel[warp]);
-        } else {
-            // Degenerate ties: exact selection, K rounds of a warp maximum below
-            // the previous one (rare path; correctness only).
-            uint64_t prev = ~0ull;
-            sel = 0ull;
-            for (int r = 0; r < K; ++r) {
-                uint64_t tb = 0ull;
-                for (int i = 0; i < PL; ++i) {
-                    float x[VEC];
-                    Chunk::unpack(vw[lane + 32 * i], x);
-                    const int e = e_lane + 32 * i * VEC;
                     for (int k = 0; k < VEC; ++k) {
-                        if (e + k < V) {
-                            const uint64_t key = value_index_key(x[k], (uint32_t)(e + k));
-                            if (key < prev && key > tb) tb = key;
+                        if (x[k] >= tv && e + k < V) {
+                            if (pos < kChunkCand)
+                                out->keys[pos] = value_index_key(x[k], (uint32_t)(e + k));
+                            ++pos;
                         }
                     }
                 }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) tb = umax64(tb, shfl_xor_u64(tb, o));
-                if (lane == r) sel = tb;
-                prev = tb;
             }
         }
-        if (lane < K) s_wsel[warp][lane] = sel;
-        if (lane == 0) s_wms[warp] = make_float2(m_w, s_w);
         __syncthreads();
-        if (warp == 0) {
-            // the chunk's list: the K best of the warps' lists, keys >= the
-            // largest warp-K-th key (that warp alone holds K keys >= it)
-            uint64_t tau = lane < kWarps ? s_wsel[lane][K - 1] : 0ull;
-            float2 p = lane < kWarps ? s_wms[lane] : make_float2(-INFINITY, 0.f);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                tau = umax64(tau, shfl_xor_u64(tau, o));
-                const float mo = __shfl_xor_sync(0xffffffffu, p.x, o);
-                const float so = __shfl_xor_sync(0xffffffffu, p.y, o);
-                ms_combine(p.x, p.y, mo, so, kLog2e);
-            }
-            int cnt = 0;
-            for (int t0 = 0; t0 < kWarps * K; t0 += 32) {
-                const int t = t0 + lane, wv = t / K;
-                const uint64_t key = t < kWarps * K ? s_wsel[wv][t - wv * K] : 0ull;
-                const bool in = key >= tau && key != 0ull;
-                const unsigned bal = __ballot_sync(0xffffffffu, in);
-                if (in) s_cc[cnt + __popc(bal & ((1u << lane) - 1u))] = key;
-                cnt += __popc(bal);
-            }
-            __syncwarp();
-            const uint64_t best = warp_top_k(s_cc, cnt, kWarps * DDTREE_MAX_K, K, s_wsel[0]);
-            if (lane < K) keys[(size_t)w * K + lane] = best;
-            if (lane == 0) ms[w] = p;
+        const int cnt = s_cnt;
+        if (cnt > kChunkCand) {
+            cta_exact_top_k<Chunk>(vec, c0, V, K, s_red, out);  // degenerate ties
+        } else if (tid == 0) {
+            out->count = cnt;
+            out->tau = tau;
         }
-        __syncthreads();  // the stage and the candidate buffers are free again
+        if (tid == 0) {
+            float m = s_wms[0].x, sm = s_wms[0].y;
+#pragma unroll
+            for (int i = 1; i < kWarps; ++i) ms_combine(m, sm, s_wms[i].x, s_wms[i].y, kLog2e);
+            out->m = m;
+            out->s = sm;
+        }
+        __syncthreads();  // the stage and the shared counters are free again
     }
 }
 
-// One warp per row merges the row's nchunks lists.  The row's K best keys are
-// >= tau2 = the largest K-th key of any list (that list alone holds K keys >=
-// tau2), so only the keys >= tau2 -- usually K to 2K of them -- are gathered
+// One warp per row merges the row's chunk outputs.  Every chunk holds >= K
+// elements >= its tau, so the row's K best keys are >= tau2 = max over chunks
+// of tau; only the kept keys >= tau2 -- usually K to 2K of them -- are gathered
 // and sorted (bitonic, or ranked by counting when more than 32).  The
-// logsumexp combines the lists' (max, sum) pairs.  Each lane issues its loads
-// in batches before using any.
+// logsumexp combines the chunks' (max, sum) pairs.  Loads are issued in
+// batches of kMergeBatch chunks before any is used.
 constexpr int kMergeThreads = 32;
-constexpr int kMergeLoads = 8;
+constexpr int kMergeBatch = 8;
 __global__ void __launch_bounds__(kMergeThreads)
-topk_merge_kernel(const float2* __restrict__ ms, const uint64_t* __restrict__ keys, int nlists,
-                  int K, int32_t* __restrict__ topk_idx, float* __restrict__ topk_logp,
+topk_merge_kernel(const ChunkOut* __restrict__ outs, int nchunks, int K,
+                  int32_t* __restrict__ topk_idx, float* __restrict__ topk_logp,
                   float* __restrict__ lse) {
     __shared__ __align__(16) uint64_t s_c[kMergeCand];
     __shared__ uint64_t s_sel[DDTREE_MAX_K];
     const int lane = threadIdx.x;
     const int row = blockIdx.x;
     pdl_wait();
-    const float2* rms = ms + (size_t)row * nlists;
-    const uint64_t* rk = keys + (size_t)row * nlists * K;
-    const int nk = nlists * K;
-    uint64_t kv[kMergeLoads];
-#pragma unroll
-    for (int u = 0; u < kMergeLoads; ++u) {
-        const int t = lane + 32 * u;
-        kv[u] = t < nk ? __ldcg((const unsigned long long*)&rk[t]) : 0ull;
-    }
-    uint64_t tau2 = 0ull;
+    const ChunkOut* ro = outs + (size_t)row * nchunks;
+    // per chunk (lane c, c + 32, ...): tau, (m, s), count
+    constexpr int kPerLane = kMaxChunks / 32;
+    int cnt_l[kPerLane];
+    uint32_t tau2 = 0u;
     float mt = -INFINITY, st = 0.f;
-    for (int l = lane; l < nlists; l += 32) {
-        tau2 = umax64(tau2, __ldcg((const unsigned long long*)&rk[(size_t)l * K + K - 1]));
-        const float2 p = __ldcg(&rms[l]);
-        ms_combine(mt, st, p.x, p.y, kLog2e);
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        const int c = lane + 32 * i;
+        cnt_l[i] = 0;
+        if (c < nchunks) {
+            tau2 = max(tau2, __ldcg(&ro[c].tau));
+            ms_combine(mt, st, __ldcg(&ro[c].m), __ldcg(&ro[c].s), kLog2e);
+            cnt_l[i] = __ldcg(&ro[c].count);
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-        tau2 = umax64(tau2, shfl_xor_u64(tau2, o));
+        tau2 = max(tau2, __shfl_xor_sync(0xffffffffu, tau2, o));
         const float mo = __shfl_xor_sync(0xffffffffu, mt, o);
         const float so = __shfl_xor_sync(0xffffffffu, st, o);
         ms_combine(mt, st, mo, so, kLog2e);
     }
     pdl_trigger();
+    // gather the kept keys >= tau2
+    constexpr int H = kChunkCand / 32;  // key slots per lane per chunk
     int cnt = 0;
-    for (int t0 = 0; t0 < nk; t0 += 32 * kMergeLoads) {
-        if (t0 > 0) {
+    for (int cb = 0; cb < nchunks; cb += kMergeBatch) {
+        uint64_t kv[kMergeBatch][H];
 #pragma unroll
-            for (int u = 0; u < kMergeLoads; ++u) {
-                const int t = t0 + lane + 32 * u;
-                kv[u] = t < nk ? __ldcg((const unsigned long long*)&rk[t]) : 0ull;
+        for (int q = 0; q < kMergeBatch; ++q) {
+            const int c = cb + q;
+            int own = cnt_l[0];  // lane (c & 31)'s count for chunk c (register select)
+#pragma unroll
+            for (int i = 1; i < kPerLane; ++i)
+                if (i == (c >> 5)) own = cnt_l[i];
+            const int n = __shfl_sync(0xffffffffu, own, c & 31);
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                const int k = lane + 32 * h;
+                kv[q][h] = (c < nchunks && k < n)
+                               ? __ldcg((const unsigned long long*)&ro[c].keys[k]) : 0ull;
             }
         }
 #pragma unroll
-        for (int u = 0; u < kMergeLoads; ++u) {
-            const bool in = kv[u] >= tau2 && kv[u] != 0ull;
-            const unsigned bal = __ballot_sync(0xffffffffu, in);
-            const int at = cnt + __popc(bal & ((1u << lane) - 1u));
-            if (in && at < kMergeCand) s_c[at] = kv[u];
-            cnt += __popc(bal);
+        for (int q = 0; q < kMergeBatch; ++q) {
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                const uint64_t key = kv[q][h];
+                const bool in = key != 0ull && (uint32_t)(key >> 32) >= tau2;
+                const unsigned bal = __ballot_sync(0xffffffffu, in);
+                const int at = cnt + __popc(bal & ((1u << lane) - 1u));
+                if (in && at < kMergeCand) s_c[at] = key;
+                cnt += __popc(bal);
+            }
         }
     }
     __syncwarp();
-    uint64_t sel;
+    uint64_t sel = 0ull;
     if (cnt <= kMergeCand) {
         sel = warp_top_k(s_c, cnt, kMergeCand, K, s_sel);
     } else {
-        // Degenerate ties: K rounds of a warp maximum below the previous one.
+        // Degenerate ties: K rounds of a warp maximum below the previous one
+        // over every kept key (correctness only).
         uint64_t prev = ~0ull;
-        sel = 0ull;
         for (int r = 0; r < K; ++r) {
             uint64_t tb = 0ull;
-            for (int t = lane; t < nk; t += 32) {
-                const uint64_t key = __ldcg((const unsigned long long*)&rk[t]);
-                if (key < prev && key > tb) tb = key;
+            for (int c = 0; c < nchunks; ++c) {
+                const int n = __ldcg(&ro[c].count);
+                for (int k = lane; k < n && k < kChunkCand; k += 32) {
+                    const uint64_t key = __ldcg((const unsigned long long*)&ro[c].keys[k]);
+                    if (key < prev && key > tb) tb = key;
+                }
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) tb = umax64(tb, shfl_xor_u64(tb, o));
@@ -375,18 +418,9 @@ ChunkPlan chunk_plan(int rows, int V, int dtype) {
     return {small, chunks_at(V, dtype, small ? kChunkSmall : kChunkBig)};
 }
 
-struct TopkWs {
-    size_t ms, keys, total;
-};
-// Workspace: (m, s) of every list, then its K keys (K <= 0: room for any K).
-TopkWs topk_layout(int rows, int V, int dtype, int K) {
-    const size_t lists = (size_t)rows * chunk_plan(rows, V, dtype).nch;
-    const size_t kk = (K > 0 && K <= DDTREE_MAX_K) ? (size_t)K : (size_t)DDTREE_MAX_K;
-    TopkWs w;
-    w.ms = 0;
-    w.keys = align_up(lists * sizeof(float2), 256);
-    w.total = w.keys + lists * kk * sizeof(uint64_t);
-    return w;
+// Workspace: one ChunkOut per (row, chunk).
+size_t topk_layout_bytes(int rows, int V, int dtype) {
+    return (size_t)rows * chunk_plan(rows, V, dtype).nch * sizeof(ChunkOut);
 }
 
 }  // namespace
@@ -398,12 +432,13 @@ bool topk_supported(int V, int dtype, int K) {
 int topk_chunks(int V, int dtype) { return chunks_at(V, dtype, kChunkSmall); }
 
 size_t topk_workspace_bytes(int rows, int V, int dtype, int K) {
-    return topk_layout(rows, V, dtype, K).total;
+    (void)K;
+    return topk_layout_bytes(rows, V, dtype);
 }
 
 template <bool BF16, int BYTES>
 cudaError_t launch_partials(const TopkArgs& a, int nch, bool aligned, int total, int per,
-                            float2* ms, uint64_t* keys, cudaStream_t s) {
+                            ChunkOut* outs, cudaStream_t s) {
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
     int dev = 0;
@@ -416,33 +451,29 @@ cudaError_t launch_partials(const TopkArgs& a, int nch, bool aligned, int total,
     if (attr_err[dev & 63] != cudaSuccess) return attr_err[dev & 63];
     const int grid = (total + per - 1) / per;
     return launch_pdl(topk_kernel<BF16, BYTES>, dim3(grid), dim3(kThreads), ring, s, a.logits,
-                      a.V, a.row_stride, a.K, nch, aligned, total, per, ms, keys, a.err);
+                      a.V, a.row_stride, a.K, nch, aligned, total, per, outs, a.err);
 }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
     const int es = a.dtype == DDTREE_BF16 ? 2 : 4;
     const bool aligned = ((uintptr_t)a.logits % 16 == 0) && ((a.row_stride * es) % 16 == 0);
-    const TopkWs wl = topk_layout(a.rows, a.V, a.dtype, a.K);
-    float2* ms = (float2*)((char*)a.ws + wl.ms);
-    uint64_t* keys = (uint64_t*)((char*)a.ws + wl.keys);
+    ChunkOut* outs = (ChunkOut*)a.ws;
     // one wave of persistent CTAs, each streaming a contiguous run of chunks
     const long slots = (long)num_sms_topk() * kCtasPerSm;
     const ChunkPlan cp = chunk_plan(a.rows, a.V, a.dtype);
-    const bool small = cp.small;
     const int nch = cp.nch;
     const long total = (long)nch * a.rows;
     const int per = (int)((total + slots - 1) / slots);
     cudaError_t e;
     if (a.dtype == DDTREE_BF16)
-        e = small ? launch_partials<true, kChunkSmall>(a, nch, aligned, (int)total, per, ms, keys, s)
-                  : launch_partials<true, kChunkBig>(a, nch, aligned, (int)total, per, ms, keys, s);
+        e = cp.small ? launch_partials<true, kChunkSmall>(a, nch, aligned, (int)total, per, outs, s)
+                     : launch_partials<true, kChunkBig>(a, nch, aligned, (int)total, per, outs, s);
     else
-        e = small ? launch_partials<false, kChunkSmall>(a, nch, aligned, (int)total, per, ms, keys, s)
-                  : launch_partials<false, kChunkBig>(a, nch, aligned, (int)total, per, ms, keys, s);
+        e = cp.small ? launch_partials<false, kChunkSmall>(a, nch, aligned, (int)total, per, outs, s)
+                     : launch_partials<false, kChunkBig>(a, nch, aligned, (int)total, per, outs, s);
     if (e != cudaSuccess) return e;
     return launch_pdl(topk_merge_kernel, dim3(a.rows), dim3(kMergeThreads), 0, s,
-                      (const float2*)ms, (const uint64_t*)keys, nch, a.K, a.topk_idx,
-                      a.topk_logp, a.lse);
+                      (const ChunkOut*)outs, nch, a.K, a.topk_idx, a.topk_logp, a.lse);
 }
 
 }  // namespace ddt
