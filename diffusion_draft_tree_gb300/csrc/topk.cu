@@ -3,21 +3,19 @@
 // Draft Trees", §3 marginals q_i; §4.3 log-probabilities; App. A restricted
 // prefix set).
 //
-// One row = one (sequence, draft position), V logits, split into chunks of
-// 32 KB (16384 bf16 or 8192 fp32 logits).  A persistent wave of CTAs streams
-// the (row, chunk) list, each CTA a contiguous run of chunks through a ring of
-// shared-memory stages filled by bulk copies a few chunks ahead, so HBM is
-// read once and stays busy.  Each warp of a CTA owns one eighth of a chunk and
-// needs no CTA-wide step: one pass over its vectors in shared memory gives
-// every vector's maximum and each lane's online (max, sum of exponentials);
-// the warp combines them into its (m, s) and selects its K best (value,
-// index) keys without per-element insertion: tau_w, the K-th largest of its
-// 32 lane maxima, bounds its K-th largest value from below, so only elements
-// >= tau_w (usually about 2K) are gathered and sorted (one warp bitonic sort;
-// ranked by counting when more than 32).  Every warp writes one sorted K-list
-// with its (m, s).  A second, PDL-chained kernel (one warp per row) merges a
-// row's lists the same way -- the keys at or above the largest list-K-th key,
-// sorted -- and forms the logsumexp.
+// One row = one (sequence, draft position), V logits, split into chunks (32 KB
+// = 16384 bf16 or 8192 fp32 logits; 16 KB when that many chunks still fit in
+// one wave).  A persistent wave of CTAs streams the (row, chunk) list, each
+// CTA a contiguous run of chunks through a ring of shared-memory stages
+// filled by bulk copies a few chunks ahead, so HBM is read once and stays
+// busy.  Per chunk, each warp makes one pass over its eighth in shared memory:
+// every vector's maximum, and each lane's online (max, sum of exponentials).
+// The chunk's K best keys need no sort here: tau_w, the K-th largest of a
+// warp's 32 lane maxima, bounds the chunk's K-th largest value from below, so
+// with tau = max_w tau_w the chunk keeps only its (value, index) keys >= tau
+// (usually K to 2K), together with its (m, s) and tau.  A second, PDL-chained
+// kernel (one CTA per row) bounds the row's K-th largest by the largest chunk
+// tau, ranks the kept keys above it by counting, and forms the logsumexp.
 #include <mutex>
 
 #include "chunk.cuh"
@@ -39,52 +37,12 @@ constexpr int kStages = 3;       // chunks in flight per CTA
 constexpr int kCtasPerSm = 2;
 constexpr int kMergeCand = 1024; // candidates the merge gathers before its slow path
 
-// Warp-wide bitonic sort of one uint64 per lane, descending (lane 0 largest).
-DDT_DEV uint64_t warp_sort_desc_u64(uint64_t v) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            const uint64_t o = __shfl_xor_sync(0xffffffffu, v, j);
-            const bool keep_max = (((lane & k) == 0) == ((lane & j) == 0));
-            v = keep_max ? (v > o ? v : o) : (v < o ? v : o);
-        }
-    }
-    return v;
-}
-
 // Merges (m, s) pairs: s2 rescaled to the larger maximum (exp base 2^(x c)).
 DDT_DEV void ms_combine(float& m, float& s, float m2, float s2, float c) {
     const float mx = fmaxf(m, m2);
     s = (m == -INFINITY ? 0.f : s * fast_exp2((m - mx) * c)) +
         (m2 == -INFINITY ? 0.f : s2 * fast_exp2((m2 - mx) * c));
     m = mx;
-}
-
-// The K largest of the `count` candidate keys in buf: lanes < K return them in
-// descending order, the others 0.  Not inlined: it is called at two places of
-// the streaming loop, whose code must stay small enough for the instruction
-// cache.
-__device__ __noinline__ uint64_t warp_top_k(uint64_t* buf, int count, int cap, int K,
-                                            uint64_t* sel) {
-    const int lane = threadIdx.x & 31;
-    if (count <= 32) {
-        const uint64_t key = warp_sort_desc_u64(lane < count ? buf[lane] : 0ull);
-        return lane < K ? key : 0ull;
-    }
-    (void)cap;
-    if (lane < K) sel[lane] = 0ull;
-    __syncwarp();
-    for (int i = lane; i < count; i += 32) {
-        const uint64_t key = buf[i];
-        const int rank = count_larger(buf, count, key);
-        if (rank < K) sel[rank] = key;
-    }
-    __syncwarp();
-    const uint64_t key = lane < K ? sel[lane] : 0ull;
-    __syncwarp();
-    return key;
 }
 
 // Per chunk, the streaming kernel leaves its (m, s), a bound tau on its K-th
@@ -282,38 +240,36 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     }
 }
 
-// One warp per row merges the row's chunk outputs.  Every chunk holds >= K
+// One CTA per row merges the row's chunk outputs.  Every chunk holds >= K
 // elements >= its tau, so the row's K best keys are >= tau2 = max over chunks
-// of tau; only the kept keys >= tau2 -- usually K to 2K of them -- are gathered
-// and sorted (bitonic, or ranked by counting when more than 32).  The
-// logsumexp combines the chunks' (max, sum) pairs.  Loads are issued in
-// batches of kMergeBatch chunks before any is used.
-constexpr int kMergeThreads = 32;
-constexpr int kMergeBatch = 8;
+// of tau; the kept keys >= tau2 are gathered and each is ranked by counting
+// the larger ones (the K of rank < K are the answer, in order).  The
+// logsumexp combines the chunks' (max, sum) pairs.  Each thread issues a batch
+// of kMergeLoads key loads before using any.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeLoads = 8;
 __global__ void __launch_bounds__(kMergeThreads)
 topk_merge_kernel(const ChunkOut* __restrict__ outs, int nchunks, int K,
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_logp,
                   float* __restrict__ lse) {
     __shared__ __align__(16) uint64_t s_c[kMergeCand];
     __shared__ uint64_t s_sel[DDTREE_MAX_K];
-    const int lane = threadIdx.x;
+    __shared__ int s_n[kMaxChunks];
+    __shared__ uint32_t s_tau[kMergeThreads / 32];
+    __shared__ float2 s_ms[kMergeThreads / 32];
+    __shared__ int s_cnt;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int row = blockIdx.x;
+    if (tid == 0) s_cnt = 0;
+    if (tid < K) s_sel[tid] = 0ull;
     pdl_wait();
     const ChunkOut* ro = outs + (size_t)row * nchunks;
-    // per chunk (lane c, c + 32, ...): tau, (m, s), count
-    constexpr int kPerLane = kMaxChunks / 32;
-    int cnt_l[kPerLane];
     uint32_t tau2 = 0u;
     float mt = -INFINITY, st = 0.f;
-#pragma unroll
-    for (int i = 0; i < kPerLane; ++i) {
-        const int c = lane + 32 * i;
-        cnt_l[i] = 0;
-        if (c < nchunks) {
-            tau2 = max(tau2, __ldcg(&ro[c].tau));
-            ms_combine(mt, st, __ldcg(&ro[c].m), __ldcg(&ro[c].s), kLog2e);
-            cnt_l[i] = __ldcg(&ro[c].count);
-        }
+    for (int c = tid; c < nchunks; c += kMergeThreads) {
+        tau2 = max(tau2, __ldcg(&ro[c].tau));
+        ms_combine(mt, st, __ldcg(&ro[c].m), __ldcg(&ro[c].s), kLog2e);
+        s_n[c] = min(__ldcg(&ro[c].count), kChunkCand);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -322,68 +278,79 @@ topk_merge_kernel(const ChunkOut* __restrict__ outs, int nchunks, int K,
         const float so = __shfl_xor_sync(0xffffffffu, st, o);
         ms_combine(mt, st, mo, so, kLog2e);
     }
+    if (lane == 0) {
+        s_tau[warp] = tau2;
+        s_ms[warp] = make_float2(mt, st);
+    }
+    __syncthreads();
+    tau2 = s_tau[0];
+    mt = s_ms[0].x;
+    st = s_ms[0].y;
+#pragma unroll
+    for (int i = 1; i < kMergeThreads / 32; ++i) {
+        tau2 = max(tau2, s_tau[i]);
+        ms_combine(mt, st, s_ms[i].x, s_ms[i].y, kLog2e);
+    }
     pdl_trigger();
-    // gather the kept keys >= tau2
-    constexpr int H = kChunkCand / 32;  // key slots per lane per chunk
-    int cnt = 0;
-    for (int cb = 0; cb < nchunks; cb += kMergeBatch) {
-        uint64_t kv[kMergeBatch][H];
+    // gather the kept keys >= tau2 (slot k of chunk c is index c * kChunkCand + k)
+    const int nslots = nchunks * kChunkCand;
+    for (int b0 = 0; b0 < nslots; b0 += kMergeLoads * kMergeThreads) {
+        uint64_t kv[kMergeLoads];
 #pragma unroll
-        for (int q = 0; q < kMergeBatch; ++q) {
-            const int c = cb + q;
-            int own = cnt_l[0];  // lane (c & 31)'s count for chunk c (register select)
-#pragma unroll
-            for (int i = 1; i < kPerLane; ++i)
-                if (i == (c >> 5)) own = cnt_l[i];
-            const int n = __shfl_sync(0xffffffffu, own, c & 31);
-#pragma unroll
-            for (int h = 0; h < H; ++h) {
-                const int k = lane + 32 * h;
-                kv[q][h] = (c < nchunks && k < n)
-                               ? __ldcg((const unsigned long long*)&ro[c].keys[k]) : 0ull;
-            }
+        for (int u = 0; u < kMergeLoads; ++u) {
+            const int i = b0 + u * kMergeThreads + tid;
+            const int c = i / kChunkCand, k = i - c * kChunkCand;
+            kv[u] = (i < nslots && k < s_n[c])
+                        ? __ldcg((const unsigned long long*)&ro[c].keys[k]) : 0ull;
         }
 #pragma unroll
-        for (int q = 0; q < kMergeBatch; ++q) {
-#pragma unroll
-            for (int h = 0; h < H; ++h) {
-                const uint64_t key = kv[q][h];
-                const bool in = key != 0ull && (uint32_t)(key >> 32) >= tau2;
-                const unsigned bal = __ballot_sync(0xffffffffu, in);
-                const int at = cnt + __popc(bal & ((1u << lane) - 1u));
-                if (in && at < kMergeCand) s_c[at] = key;
-                cnt += __popc(bal);
+        for (int u = 0; u < kMergeLoads; ++u) {
+            if (kv[u] != 0ull && (uint32_t)(kv[u] >> 32) >= tau2) {
+                const int at = atomicAdd(&s_cnt, 1);
+                if (at < kMergeCand) s_c[at] = kv[u];
             }
         }
     }
-    __syncwarp();
-    uint64_t sel = 0ull;
+    __syncthreads();
+    const int cnt = s_cnt;
     if (cnt <= kMergeCand) {
-        sel = warp_top_k(s_c, cnt, kMergeCand, K, s_sel);
+        for (int i = tid; i < cnt; i += kMergeThreads) {
+            const uint64_t key = s_c[i];
+            const int rank = count_larger(s_c, cnt, key);
+            if (rank < K) s_sel[rank] = key;
+        }
     } else {
-        // Degenerate ties: K rounds of a warp maximum below the previous one
-        // over every kept key (correctness only).
+        // Degenerate ties: K rounds of a CTA maximum below the previous one over
+        // every kept key (correctness only).
         uint64_t prev = ~0ull;
         for (int r = 0; r < K; ++r) {
             uint64_t tb = 0ull;
-            for (int c = 0; c < nchunks; ++c) {
-                const int n = __ldcg(&ro[c].count);
-                for (int k = lane; k < n && k < kChunkCand; k += 32) {
+            for (int i = tid; i < nslots; i += kMergeThreads) {
+                const int c = i / kChunkCand, k = i - c * kChunkCand;
+                if (k < s_n[c]) {
                     const uint64_t key = __ldcg((const unsigned long long*)&ro[c].keys[k]);
                     if (key < prev && key > tb) tb = key;
                 }
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) tb = umax64(tb, shfl_xor_u64(tb, o));
-            if (lane == r) sel = tb;
+            __syncthreads();
+            if (lane == 0) s_c[warp] = tb;
+            __syncthreads();
+            tb = s_c[0];
+            for (int i = 1; i < kMergeThreads / 32; ++i) tb = umax64(tb, s_c[i]);
+            if (tid == 0) s_sel[r] = tb;
             prev = tb;
         }
     }
+    __syncthreads();
+    if (warp != 0) return;
     const float M = (mt == -INFINITY) ? 0.f : mt;
     const float logS = logf(st);
     if (lane < K) {
-        topk_idx[(size_t)row * K + lane] = (int32_t)key_index(sel);
-        topk_logp[(size_t)row * K + lane] = (key_value(sel) - M) - logS;
+        const uint64_t key = s_sel[lane];
+        topk_idx[(size_t)row * K + lane] = (int32_t)key_index(key);
+        topk_logp[(size_t)row * K + lane] = (key_value(key) - M) - logS;
     }
     if (lane == 0 && lse) lse[row] = M + logS;
 }
