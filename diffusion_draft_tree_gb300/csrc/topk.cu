@@ -113,6 +113,7 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     __shared__ uint32_t s_wtau[kWarps];
     __shared__ float2 s_wms[kWarps];
     __shared__ uint64_t s_red[kWarps];
+    __shared__ int16_t s_vlist[kWarps][Chunk::NVEC / kWarps];  // passing vector ids per warp
     __shared__ int s_cnt;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -181,42 +182,44 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
         for (int i = 1; i < kWarps; ++i) tau = max(tau, s_wtau[i]);
         const float tv = (tau == 0u) ? -INFINITY : float_from_ord(tau);
 
-        // ---- the chunk's keys >= tau, from the vectors whose maximum reaches it ----
-        int mine = 0;
+        // ---- the chunk's keys >= tau, from the vectors whose maximum reaches it:
+        // their ids are compacted per warp first (a ballot per vector row), so
+        // each passing vector is unpacked by one lane instead of the whole warp
+        // stepping through every row in which any lane passes ----
+        int nv = 0;
 #pragma unroll
         for (int i = 0; i < PL; ++i) {
-            if (vmx[i] >= tv) {
-                float x[VEC];
-                Chunk::unpack(vw[lane + 32 * i], x);
-                const int e = e_lane + 32 * i * VEC;
+            const unsigned bal = __ballot_sync(0xffffffffu, vmx[i] >= tv);
+            if (vmx[i] >= tv) s_vlist[warp][nv + __popc(bal & ((1u << lane) - 1u))] = (int16_t)(lane + 32 * i);
+            nv += __popc(bal);
+        }
+        __syncwarp();
+        for (int b0 = 0; b0 < nv; b0 += 32) {
+            const int v = b0 + lane < nv ? s_vlist[warp][b0 + lane] : -1;
+            float x[VEC];
+            int mine = 0;
+            const int e = c0 + (warp * VPW + v) * VEC;
+            if (v >= 0) {
+                Chunk::unpack(vw[v], x);
 #pragma unroll
                 for (int k = 0; k < VEC; ++k) mine += (x[k] >= tv && e + k < V) ? 1 : 0;
             }
-        }
-        int incl = mine;
+            int incl = mine;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += t;
-        }
-        int wbase = 0;
-        if (lane == 31 && incl > 0) wbase = atomicAdd(&s_cnt, incl);
-        wbase = __shfl_sync(0xffffffffu, wbase, 31);
-        if (mine) {
-            int pos = wbase + incl - mine;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            int wbase = 0;
+            if (lane == 31 && incl > 0) wbase = atomicAdd(&s_cnt, incl);
+            wbase = __shfl_sync(0xffffffffu, wbase, 31);
+            if (mine) {
+                int pos = wbase + incl - mine;
 #pragma unroll
-            for (int i = 0; i < PL; ++i) {
-                if (vmx[i] >= tv) {
-                    float x[VEC];
-                    Chunk::unpack(vw[lane + 32 * i], x);
-                    const int e = e_lane + 32 * i * VEC;
-#pragma unroll
-                    for (int k = 0; k < VEC; ++k) {
-                        if (x[k] >= tv && e + k < V) {
-                            if (pos < kChunkCand)
-                                out->keys[pos] = value_index_key(x[k], (uint32_t)(e + k));
-                            ++pos;
-                        }
+                for (int k = 0; k < VEC; ++k) {
+                    if (x[k] >= tv && e + k < V) {
+                        if (pos < kChunkCand) out->keys[pos] = value_index_key(x[k], (uint32_t)(e + k));
+                        ++pos;
                     }
                 }
             }
