@@ -10,10 +10,11 @@
 // filled by bulk copies a few chunks ahead, so HBM is read once and stays
 // busy.  Per chunk, each warp makes one pass over its eighth in shared memory:
 // every vector's maximum, and each lane's online (max, sum of exponentials).
-// The chunk's K best keys need no sort here: tau_w, the K-th largest of a
-// warp's 32 lane maxima, bounds the chunk's K-th largest value from below, so
-// with tau = max_w tau_w the chunk keeps only its (value, index) keys >= tau
-// (usually K to 2K), together with its (m, s) and tau.  A second, PDL-chained
+// The chunk's K best keys need no sort here: tau_w, the K-th largest vector
+// maximum of a warp's slice (found by sorting the few vector maxima above the
+// K-th largest lane maximum), bounds the chunk's K-th largest value from
+// below, so with tau = max_w tau_w the chunk keeps only its (value, index)
+// keys >= tau (usually K to 2K), together with its (m, s) and tau.  A second, PDL-chained
 // kernel (one CTA per row) bounds the row's K-th largest by the largest chunk
 // tau, ranks the kept keys above it by counting, and forms the logsumexp.
 #include <mutex>
@@ -36,6 +37,21 @@ constexpr int kMaxChunks = 128;  // per row, at the small size
 constexpr int kStages = 3;       // chunks in flight per CTA
 constexpr int kCtasPerSm = 2;
 constexpr int kMergeCand = 1024; // candidates the merge gathers before its slow path
+
+// Warp-wide bitonic sort of one uint32 per lane, descending (lane 0 largest).
+DDT_DEV uint32_t warp_sort_desc_u32(uint32_t v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const uint32_t o = __shfl_xor_sync(0xffffffffu, v, j);
+            const bool keep_max = (((lane & k) == 0) == ((lane & j) == 0));
+            v = keep_max ? max(v, o) : min(v, o);
+        }
+    }
+    return v;
+}
 
 // Merges (m, s) pairs: s2 rescaled to the larger maximum (exp base 2^(x c)).
 DDT_DEV void ms_combine(float& m, float& s, float m2, float s2, float c) {
@@ -114,6 +130,7 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     __shared__ float2 s_wms[kWarps];
     __shared__ uint64_t s_red[kWarps];
     __shared__ int16_t s_vlist[kWarps][Chunk::NVEC / kWarps];  // passing vector ids per warp
+    __shared__ uint32_t s_vm[kWarps][32];                      // a warp's top vector maxima
     __shared__ int s_cnt;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -163,8 +180,29 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
             }
             if (mt != -INFINITY) Chunk::exp_sum(v, kLog2e, -mt * kLog2e, a0, a1);
         }
-        // tau_w: the warp's slice has >= K elements >= it (K lanes' maxima)
-        const uint32_t tau_w = warp_kth_largest(e_lane < V ? ord_from_float(mt) : 0u, K);
+        // tau_w: the K-th largest vector maximum of the warp's slice (K distinct
+        // elements are >= it).  First a loose bound, the K-th largest lane
+        // maximum; the vector maxima at or above it (usually K to 3K) are then
+        // sorted by the warp.
+        const uint32_t tau_l = warp_kth_largest(e_lane < V ? ord_from_float(mt) : 0u, K);
+        uint32_t tau_w = tau_l;
+        {
+            const float tl = (tau_l == 0u) ? -INFINITY : float_from_ord(tau_l);
+            int nm = 0;
+#pragma unroll
+            for (int i = 0; i < PL; ++i) {
+                const bool in = vmx[i] >= tl && e_lane + 32 * i * VEC < V;
+                const unsigned bal = __ballot_sync(0xffffffffu, in);
+                const int at = nm + __popc(bal & ((1u << lane) - 1u));
+                if (in && at < 32) s_vm[warp][at] = ord_from_float(vmx[i]);
+                nm += __popc(bal);
+            }
+            __syncwarp();
+            if (nm <= 32) {
+                const uint32_t sorted = warp_sort_desc_u32(lane < nm ? s_vm[warp][lane] : 0u);
+                tau_w = max(tau_l, __shfl_sync(0xffffffffu, sorted, K - 1));
+            }
+        }
         float m_w = mt, s_w = a0 + a1;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
