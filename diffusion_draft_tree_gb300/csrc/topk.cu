@@ -10,11 +10,12 @@
 // filled by bulk copies a few chunks ahead, so HBM is read once and stays
 // busy.  Per chunk, each warp makes one pass over its eighth in shared memory:
 // every vector's maximum, and each lane's online (max, sum of exponentials).
-// The chunk's K best keys need no sort here: tau_w, the K-th largest vector
-// maximum of a warp's slice (found by sorting the few vector maxima above the
-// K-th largest lane maximum), bounds the chunk's K-th largest value from
-// below, so with tau = max_w tau_w the chunk keeps only its (value, index)
-// keys >= tau (usually K to 2K), together with its (m, s) and tau.  A second, PDL-chained
+// The chunk's K best keys need no sort here: every warp sorts the few vector
+// maxima of its slice above its K-th largest lane maximum and publishes its K
+// largest; tau, the K-th largest of those lists, is the K-th largest vector
+// maximum of the chunk -- K distinct elements are >= it -- so the chunk keeps
+// only its (value, index) keys >= tau (usually K to 1.5K), together with its
+// (m, s) and tau.  A second, PDL-chained
 // kernel (one CTA per row) bounds the row's K-th largest by the largest chunk
 // tau, ranks the kept keys above it by counting, and forms the logsumexp.
 #include <mutex>
@@ -126,7 +127,6 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
     constexpr int PL = VPW / 32;               // vectors per lane
     extern __shared__ __align__(128) uint8_t s_ring[];  // kStages x Chunk::BYTES
     __shared__ __align__(8) uint64_t s_bar[kStages];
-    __shared__ uint32_t s_wtau[kWarps];
     __shared__ float2 s_wms[kWarps];
     __shared__ uint64_t s_red[kWarps];
     __shared__ int16_t s_vlist[kWarps][Chunk::NVEC / kWarps];  // passing vector ids per warp
@@ -180,13 +180,12 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
             }
             if (mt != -INFINITY) Chunk::exp_sum(v, kLog2e, -mt * kLog2e, a0, a1);
         }
-        // tau_w: the K-th largest vector maximum of the warp's slice (K distinct
-        // elements are >= it).  First a loose bound, the K-th largest lane
-        // maximum; the vector maxima at or above it (usually K to 3K) are then
-        // sorted by the warp.
-        const uint32_t tau_l = warp_kth_largest(e_lane < V ? ord_from_float(mt) : 0u, K);
-        uint32_t tau_w = tau_l;
+        // The warp's K largest vector maxima (K distinct elements), descending,
+        // into s_vm[warp]: the vector maxima at or above the K-th largest lane
+        // maximum (usually K to 3K) sorted by the warp; if there are too many,
+        // K copies of that lane bound (still K elements >= each).
         {
+            const uint32_t tau_l = warp_kth_largest(e_lane < V ? ord_from_float(mt) : 0u, K);
             const float tl = (tau_l == 0u) ? -INFINITY : float_from_ord(tau_l);
             int nm = 0;
 #pragma unroll
@@ -198,10 +197,10 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
                 nm += __popc(bal);
             }
             __syncwarp();
-            if (nm <= 32) {
-                const uint32_t sorted = warp_sort_desc_u32(lane < nm ? s_vm[warp][lane] : 0u);
-                tau_w = max(tau_l, __shfl_sync(0xffffffffu, sorted, K - 1));
-            }
+            uint32_t top = tau_l;
+            if (nm <= 32) top = warp_sort_desc_u32(lane < nm ? s_vm[warp][lane] : 0u);
+            __syncwarp();
+            if (lane < K) s_vm[warp][lane] = top;
         }
         float m_w = mt, s_w = a0 + a1;
 #pragma unroll
@@ -210,14 +209,23 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
             const float so = __shfl_xor_sync(0xffffffffu, s_w, o);
             ms_combine(m_w, s_w, mo, so, kLog2e);
         }
-        if (lane == 0) {
-            s_wtau[warp] = tau_w;
-            s_wms[warp] = make_float2(m_w, s_w);
-        }
+        if (lane == 0) s_wms[warp] = make_float2(m_w, s_w);
         __syncthreads();
-        uint32_t tau = s_wtau[0];
-#pragma unroll
-        for (int i = 1; i < kWarps; ++i) tau = max(tau, s_wtau[i]);
+        // tau: the K-th largest of the warps' lists (each warp, redundantly),
+        // a bound on the chunk's K-th largest value
+        uint32_t tau = 0u;
+        {
+            int ptr = 0;
+            uint32_t head = lane < kWarps ? s_vm[lane][0] : 0u;
+            for (int r = 0; r < K; ++r) {
+                tau = __reduce_max_sync(0xffffffffu, head);
+                const unsigned holders = __ballot_sync(0xffffffffu, head == tau);
+                if (lane == __ffs(holders) - 1) {
+                    ++ptr;
+                    head = ptr < K ? s_vm[lane][ptr] : 0u;
+                }
+            }
+        }
         const float tv = (tau == 0u) ? -INFINITY : float_from_ord(tau);
 
         // ---- the chunk's keys >= tau, from the vectors whose maximum reaches it:
