@@ -71,6 +71,42 @@ def work_model(w, tree_anc_total: int) -> dict:
             "accept": {"bytes": accept_bytes}}
 
 
+# Kernels one round launches: top-K partials and row merge, tree build, tree
+# attention, accept.
+LAUNCHES_PER_ROUND = 5
+# Sources a kernel's DRAM traffic depends on (its own file and shared headers).
+KERNEL_SOURCES = {"tree_attn": ["tree_attn.cu", "sm100.cuh", "common.cuh"]}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "diffusion_draft_tree_gb300",
+                        "csrc")
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) that an
+    ncu capture recorded in profiles/traffic.md for this kernel and workload, or
+    None if there is none or the kernel's sources changed since."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash(kernel)
+    for line in open(path):
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 4 and cells[0] == kernel and cells[1] == workload and cells[3] == want:
+            try:
+                return int(cells[2])
+            except ValueError:
+                return None
+    return None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -554,7 +590,7 @@ def main():
         roof = {"kernel": "tree_attn", "bound": "hbm", "achieved": a["bytes"] / (ams * 1e-3) / 1e9,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = measured_traffic("tree_attn", w.name)
     roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json burst figure)"
     roof["algorithmic_bytes"] = a["bytes"]
     roof["algorithmic_flops"] = a["flops"]
@@ -563,7 +599,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_of(w, res["R"]), "roofline": roof, "kernels": kernels,
-            "kernel_timing": res["kern_method"], "gpu_launches": 4 * args.steps,
+            "kernel_timing": res["kern_method"], "gpu_launches": LAUNCHES_PER_ROUND * args.steps,
             "clocks": res["clocks"], "e2e": res["e2e"]}
     if res["x36"]:
         line["rounds_per_s_x36_layers"] = res["x36"]["rounds_per_s"] * world
