@@ -58,8 +58,9 @@ def _load():
             lib.ddo_uniform.restype = f64
             lib.ddo_accept.argtypes = [P, i32, i64, P, P, P, i32, i32, i32, i32, f64, u64, u64,
                                        P, P, P, P, P, P]
+            lib.ddo_commit.argtypes = [P, P, i64, P, P, P, P, P, i32, i32, i32, i32, i32]
             for f in (lib.ddo_topk, lib.ddo_build, lib.ddo_tree_attn_unit, lib.ddo_tree_attn,
-                      lib.ddo_accept):
+                      lib.ddo_accept, lib.ddo_commit):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -177,3 +178,23 @@ def accept(logits, dtype: int, tree: dict, L: int, temperature: float = 0.0, see
                               _p(out["out_tokens"]), _p(out["next_bonus"]), _p(out["margin"])),
            "accept")
     return out
+
+
+def commit(k_cache, v_cache, k_tree, v_tree, accept_len, accepted_nodes, prefix_len):
+    """Commit the accepted path -- the root (this round's bonus token) and the
+    accepted nodes -- to the KV cache (pages §3, §4.1: verified tokens join the
+    prefix).  Caches are [B][Hkv][cap][D] uint16 bf16 bits, tree K/V
+    [B][N+1][Hkv][D]; returns (k_cache, v_cache, prefix_len) as new arrays."""
+    kc = np.array(k_cache, dtype=np.uint16, order="C", copy=True)
+    vc = np.array(v_cache, dtype=np.uint16, order="C", copy=True)
+    kt = np.ascontiguousarray(k_tree, dtype=np.uint16)
+    vt = np.ascontiguousarray(v_tree, dtype=np.uint16)
+    B, Hkv, cap, D = kc.shape
+    N = kt.shape[1] - 1
+    L = np.asarray(accepted_nodes).shape[1]
+    plen = np.array(prefix_len, dtype=np.int32, copy=True)
+    _check(_load().ddo_commit(_p(kc), _p(vc), cap, _p(kt), _p(vt),
+                              _p(np.ascontiguousarray(accept_len, dtype=np.int32)),
+                              _p(np.ascontiguousarray(accepted_nodes, dtype=np.int32)), _p(plen),
+                              B, L, N, Hkv, D), "commit")
+    return kc, vc, plen

@@ -421,3 +421,48 @@ int ddo_accept(const void* logits, int dtype, int64_t row_stride, const int32_t*
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* After the walk: commit the accepted path to the KV cache (§3 / §4.1: the  */
+/* bonus token and the accepted tokens become part of the verified prefix).  */
+/* ------------------------------------------------------------------------ */
+
+/* For every sequence b with P = prefix_len[b] and a = accept_len[b], the path
+ * rows are node 0 (the root: this round's bonus token) followed by
+ * accepted_nodes[b][0..a).  Row i of that path (i = 0..a) is copied, for every
+ * KV head g, from k_tree/v_tree[b][node_i][g][:] to k_cache/v_cache[b][g][P+i][:]
+ * (bf16 bytes, unchanged), and prefix_len[b] becomes P + a + 1.  The tree
+ * rows' keys and values were computed with position id P + depth, and the
+ * node at path index i has depth i, so the copied rows sit at their own
+ * positions.  Returns 0, or -1 on invalid arguments (a outside [0, L], an
+ * accepted node outside [1, N], or P + a + 1 > cache_cap), changing nothing
+ * for that sequence and later ones. */
+int ddo_commit(uint16_t* k_cache, uint16_t* v_cache, int64_t cache_cap, const uint16_t* k_tree,
+               const uint16_t* v_tree, const int32_t* accept_len, const int32_t* accepted_nodes,
+               int32_t* prefix_len, int B, int L, int N, int Hkv, int D)
+{
+    if (B < 0 || L <= 0 || N < 0 || Hkv <= 0 || D <= 0 || cache_cap < 0) return -1;
+    const int R = N + 1;
+    for (int b = 0; b < B; ++b) {
+        const int64_t P = prefix_len[b];
+        const int a = accept_len[b];
+        if (a < 0 || a > L || P < 0 || P + a + 1 > cache_cap) return -1;
+        for (int i = 0; i < a; ++i) {
+            const int u = accepted_nodes[(int64_t)b * L + i];
+            if (u < 1 || u > N) return -1;
+        }
+        for (int i = 0; i <= a; ++i) {
+            const int u = (i == 0) ? 0 : accepted_nodes[(int64_t)b * L + i - 1];
+            for (int g = 0; g < Hkv; ++g) {
+                const int64_t src = (((int64_t)b * R + u) * Hkv + g) * D;
+                const int64_t dst = (((int64_t)b * Hkv + g) * cache_cap + P + i) * D;
+                for (int d = 0; d < D; ++d) {
+                    k_cache[dst + d] = k_tree[src + d];
+                    v_cache[dst + d] = v_tree[src + d];
+                }
+            }
+        }
+        prefix_len[b] = (int32_t)(P + a + 1);
+    }
+    return 0;
+}

@@ -436,3 +436,78 @@ def test_sampling_frequencies_match_softmax():
     p /= p.sum()
     obs = np.bincount(draws, minlength=V)
     assert chisquare(obs, p * len(draws)).pvalue > 1e-4
+
+
+# --------------------------------------------------------------------------
+# after the walk: committing the accepted path to the KV cache
+# --------------------------------------------------------------------------
+
+def _commit_case(seed, B=3, N=20, Hkv=2, D=16, L=5, K=3, cap=40):
+    rng = np.random.default_rng(seed)
+    P = rng.integers(0, cap - L - 1, size=B).astype(np.int32)
+    q, kc, vc, kt, vt = _attn_inputs(rng, B, N, 2 * Hkv, Hkv, D, list(P), cap)
+    t = _random_tree(rng, B, N, L=L, K=K)
+    # an accepted path per sequence: follow a random child from the root
+    acc = np.full((B, L), -1, np.int32)
+    alen = np.zeros(B, np.int32)
+    for b in range(B):
+        cur, depth = 0, 0
+        while depth < L:
+            kids = [c for c in range(1, t["n_nodes"][b] + 1) if t["parent"][b, c] == cur]
+            if not kids or rng.random() < 0.2:
+                break
+            cur = int(rng.choice(kids))
+            acc[b, depth] = cur
+            depth += 1
+        alen[b] = depth
+    return q, kc, vc, kt, vt, P, t, acc, alen
+
+
+def test_commit_is_a_gather_of_the_root_path():
+    """§4.1: the bonus token (the root) and the accepted tokens join the
+    prefix, in path order, at positions P..P+a; nothing else changes."""
+    for seed in range(4):
+        q, kc, vc, kt, vt, P, t, acc, alen = _commit_case(seed)
+        k2, v2, p2 = oracle.commit(kc, vc, kt, vt, alen, acc, P)
+        np.testing.assert_array_equal(p2, P + alen + 1)
+        for b in range(len(P)):
+            rows = np.concatenate([[0], acc[b, :alen[b]]])
+            seg = slice(P[b], P[b] + alen[b] + 1)
+            # numpy's gather of the tree rows, transposed to [Hkv][a+1][D]
+            np.testing.assert_array_equal(k2[b, :, seg], np.take(kt[b], rows, axis=0).transpose(1, 0, 2))
+            np.testing.assert_array_equal(v2[b, :, seg], np.take(vt[b], rows, axis=0).transpose(1, 0, 2))
+            keep = np.ones(kc.shape[2], bool)
+            keep[seg] = False
+            np.testing.assert_array_equal(k2[b][:, keep].view(np.uint16), kc[b][:, keep])
+            np.testing.assert_array_equal(v2[b][:, keep].view(np.uint16), vc[b][:, keep])
+
+
+def test_commit_then_decode_equals_tree_attention_of_the_last_accepted_node():
+    """The committed rows are exactly the last accepted node's root path, so its
+    tree-attention row (prefix + ancestors) equals plain attention of the same
+    query over the extended cache (torch SDPA, fp64)."""
+    q, kc, vc, kt, vt, P, t, acc, alen = _commit_case(11)
+    out, _ = oracle.tree_attn(q, kc, vc, kt, vt, P, t["n_nodes"], t["anc_mask"])
+    k2, v2, p2 = oracle.commit(kc, vc, kt, vt, alen, acc, P)
+    Hq, Hkv = q.shape[2], kc.shape[1]
+    G = Hq // Hkv
+    for b in range(len(P)):
+        u = 0 if alen[b] == 0 else int(acc[b, alen[b] - 1])
+        for h in range(Hq):
+            k = _f64(k2[b, h // G, :p2[b]])
+            v = _f64(v2[b, h // G, :p2[b]])
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                _f64(q[b, u, h])[None, None], k[None], v[None])[0, 0]
+            np.testing.assert_allclose(out[b, u, h], ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_commit_rejects_bad_paths():
+    q, kc, vc, kt, vt, P, t, acc, alen = _commit_case(3)
+    with pytest.raises(ValueError):
+        oracle.commit(kc, vc, kt, vt, np.full_like(alen, 6), acc, P)  # longer than L
+    bad = acc.copy()
+    bad[0, 0] = 21  # past the tree
+    with pytest.raises(ValueError):
+        oracle.commit(kc, vc, kt, vt, np.maximum(alen, 1), bad, P)
+    with pytest.raises(ValueError):
+        oracle.commit(kc, vc, kt, vt, alen, acc, np.full_like(P, kc.shape[2] - alen.min()))
