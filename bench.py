@@ -361,6 +361,34 @@ def gpu_arm(args, rank, world, dev):
         kern_ms = np.full(4, np.nan)
         kern_method = f"unavailable: {e!r}"
 
+    # the step after the round: commit the accepted path to the KV cache (not
+    # part of the round's metric; timed alone, prefix lengths restored first)
+    commit = None
+    try:
+        r0 = rounds[0]
+        cap2 = w.P_cap + w.L + 1
+        kc2 = torch.empty((w.B, w.Hkv, cap2, w.D), dtype=torch.bfloat16, device=dev)
+        vc2 = torch.empty_like(kc2)
+        plen0 = base["prefix_len"]
+        plen = plen0.clone()
+        c_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        n_c, t_c = 50, 0.0
+        for i in range(n_c + 3):
+            plen.copy_(plen0)
+            c_ev[0].record()
+            ops.ddtree_commit(kc2, vc2, base["k_tree"][0], base["v_tree"][0],
+                              r0.acc["accept_len"], r0.acc["accepted_nodes"], plen)
+            c_ev[1].record()
+            torch.cuda.synchronize()
+            if i >= 3:
+                t_c += c_ev[0].elapsed_time(c_ev[1])
+        ops.ddtree_device_check()
+        rows = int(r0.acc["accept_len"].sum().item()) + w.B
+        commit = {"ms": t_c / n_c, "bytes": 8 * rows * w.Hkv * w.D}
+        del kc2, vc2
+    except Exception as e:  # noqa: BLE001
+        commit = {"unavailable": repr(e)}
+
     # 36-layer round: 36 tree-attention launches, each on its own KV cache
     x36 = None
     if not args.no_x36:
@@ -442,6 +470,7 @@ def gpu_arm(args, rank, world, dev):
                            rounds[0].tree["anc_mask"].cpu().numpy().view(np.uint32).ravel()]))
     return {"w": w, "ms_total": ms_total, "R": R, "per_copy": per_copy, "clocks": clocks,
             "kern_ms": kern_ms, "kern_method": kern_method, "x36": x36, "e2e": e2e,
+            "commit": commit,
             "tree_anc": tree_anc}
 
 
@@ -579,6 +608,12 @@ def main():
             k["TFLOPps"] = model[n]["flops"] / (ms * 1e-3) / 1e12
             k["tensor_frac"] = k["TFLOPps"] / peaks["bf16_tflops"]
         kernels[n] = k
+    c = res.get("commit")
+    if c and "ms" in c:
+        kernels["commit"] = {"ms": c["ms"], "GBps": c["bytes"] / (c["ms"] * 1e-3) / 1e9,
+                             "hbm_frac": c["bytes"] / (c["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                             "note": "after the round, not in its metric: the accepted "
+                                     "path's K/V rows into the cache"}
     a = model["tree_attn"]
     t_hbm = a["bytes"] / (peaks["hbm_gbs"] * 1e9)
     t_tc = a["flops"] / (peaks["bf16_tflops"] * 1e12)

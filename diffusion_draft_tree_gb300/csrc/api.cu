@@ -180,6 +180,25 @@ ddtree_status ddtree_accept(const void* target_logits, int dtype, int64_t row_st
     return launched(ddt::launch_accept(a, (cudaStream_t)stream));
 }
 
+ddtree_status ddtree_commit(void* k_cache, void* v_cache, int64_t cache_cap, const void* k_tree,
+                            const void* v_tree, const int32_t* accept_len,
+                            const int32_t* accepted_nodes, int32_t* prefix_len, int B, int L,
+                            int N, int Hkv, int D, void* stream) {
+    if (!k_cache || !v_cache || !k_tree || !v_tree || !accept_len || !accepted_nodes ||
+        !prefix_len)
+        return DDTREE_ERR_INVALID_ARG;
+    if (B <= 0 || B > 65535 || L <= 0 || N < 0 || Hkv <= 0 || D <= 0 || cache_cap <= 0)
+        return DDTREE_ERR_INVALID_ARG;
+    if (L > DDTREE_MAX_L || N > DDTREE_MAX_N || D % 8 != 0) return DDTREE_ERR_UNSUPPORTED;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_tree, 16) ||
+        !aligned(v_tree, 16) || !aligned(accept_len, 4) || !aligned(accepted_nodes, 4) ||
+        !aligned(prefix_len, 4))
+        return DDTREE_ERR_INVALID_ARG;
+    ddt::CommitArgs a{k_cache, v_cache, cache_cap, k_tree, v_tree, accept_len, accepted_nodes,
+                      prefix_len, B, L, N, Hkv, D, error_word()};
+    return launched(ddt::launch_commit(a, (cudaStream_t)stream));
+}
+
 ddtree_status ddtree_device_check(void* stream, uint32_t* detail) {
     uint32_t* p = error_word();
     if (!p) return DDTREE_ERR_CUDA;

@@ -78,6 +78,18 @@ size_t accept_workspace_bytes(int B, int N, int V, int dtype);
 bool accept_supported(int V, int dtype);
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s);
 
+// ---- after the walk: commit the accepted path to the KV cache -----------------
+struct CommitArgs {
+    void *k_cache, *v_cache;
+    int64_t cache_cap;
+    const void *k_tree, *v_tree;
+    const int32_t *accept_len, *accepted_nodes;
+    int32_t* prefix_len;
+    int B, L, N, Hkv, D;
+    uint32_t* err;
+};
+cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s);
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace ddt

@@ -58,13 +58,14 @@ def _load() -> ctypes.CDLL:
                                      P, P, P, sz, P]
     lib.ddtree_accept.argtypes = [P, i32, i64, P, P, P, i32, i32, i32, i32, f32, u64, u64, P, P,
                                   P, P, P, P, sz, P]
+    lib.ddtree_commit.argtypes = [P, P, i64, P, P, P, P, P, i32, i32, i32, i32, i32, P]
     lib.ddtree_device_check.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
     lib.ddtree_last_cuda_error.argtypes = []
     lib.ddtree_last_cuda_error.restype = ctypes.c_char_p
     lib.ddtree_status_str.argtypes = [i32]
     lib.ddtree_status_str.restype = ctypes.c_char_p
     for f in ("ddtree_topk", "ddtree_build", "ddtree_build_heap", "ddtree_tree_attn",
-              "ddtree_accept", "ddtree_device_check"):
+              "ddtree_accept", "ddtree_commit", "ddtree_device_check"):
         getattr(lib, f).restype = i32
     return lib
 
@@ -162,6 +163,18 @@ def ddtree_accept(target_logits, parent, token, n_nodes, L, out: dict, temperatu
         _ptr(out.get("target_token")), _ptr(out["accept_len"]), _ptr(out["accepted_nodes"]),
         _ptr(out["out_tokens"]), _ptr(out["next_bonus"]), _ptr(ws),
         ws.numel() if ws is not None else 0, _stream(stream)))
+
+
+def ddtree_commit(k_cache, v_cache, k_tree, v_tree, accept_len, accepted_nodes, prefix_len,
+                  stream=None):
+    """Commit the accepted path (root + accepted nodes) to the KV cache in place
+    and advance prefix_len in place."""
+    B, Hkv, cap, D = k_cache.shape
+    R = k_tree.shape[1]
+    L = accepted_nodes.shape[1]
+    _check("ddtree_commit", lib.ddtree_commit(
+        _ptr(k_cache), _ptr(v_cache), cap, _ptr(k_tree), _ptr(v_tree), _ptr(accept_len),
+        _ptr(accepted_nodes), _ptr(prefix_len), B, L, R - 1, Hkv, D, _stream(stream)))
 
 
 def ddtree_device_check(stream=None) -> int:

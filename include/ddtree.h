@@ -207,9 +207,33 @@ ddtree_status ddtree_accept(const void* target_logits, int dtype, int64_t row_st
                             int32_t* accepted_nodes, int32_t* out_tokens, int32_t* next_bonus,
                             void* workspace, size_t ws_bytes, void* stream);
 
+/* After the walk -- commit the accepted path to the KV cache.
+ * Pages: §3 (the bonus token is not yet in the cache when the round starts),
+ * §4.1 (the root is the bonus token; the matched path is accepted): the
+ * verified tokens join the prefix the next round attends to.
+ *   k_cache, v_cache bf16 [B][Hkv][cache_cap][D], written in place.
+ *   k_tree, v_tree   bf16 [B][N+1][Hkv][D]: the tree K/V given to
+ *                    ddtree_tree_attn (keys computed at position P_b + depth).
+ *   accept_len [B], accepted_nodes [B][L] from ddtree_accept.
+ *   prefix_len [B]: read, then advanced in place to P_b + accept_len[b] + 1.
+ * For each sequence the path rows -- node 0 (this round's bonus) followed by
+ * the accepted nodes -- are copied, for every KV head, to cache positions
+ * P_b .. P_b + accept_len[b] (path index = depth = position offset).  D must be
+ * a multiple of 8 and every K/V pointer 16-byte aligned.  A sequence whose
+ * path does not fit (P_b + accept_len + 1 > cache_cap) or names a node outside
+ * [1, N] is left unchanged and recorded in the device error word.
+ * No workspace. */
+ddtree_status ddtree_commit(void* k_cache, void* v_cache, int64_t cache_cap, const void* k_tree,
+                            const void* v_tree, const int32_t* accept_len,
+                            const int32_t* accepted_nodes, int32_t* prefix_len, int B, int L,
+                            int N, int Hkv, int D, void* stream);
+
 /* Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns DDTREE_OK, DDTREE_ERR_DEVICE (and the recorded code in
- * *detail when non-null: which kernel and what was wrong), or DDTREE_ERR_CUDA. */
+ * *detail when non-null: which kernel and what was wrong), or DDTREE_ERR_CUDA.
+ * Code: high byte = kernel (1 top-K, 2 build, 3 tree attention, 4 accept,
+ * 5 commit), low byte = reason (1 bad prefix length, 2 bad node count, 3 bad
+ * tree or path, 4 a bounded wait timed out, 5 bad input, 6 internal plan). */
 ddtree_status ddtree_device_check(void* stream, uint32_t* detail);
 
 /* Name of the CUDA error behind the calling thread's most recent

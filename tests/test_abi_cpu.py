@@ -27,7 +27,8 @@ def _declared():
 def test_header_declares_the_round(lib):
     names = _declared()
     for n in ("ddtree_topk", "ddtree_build", "ddtree_tree_attn", "ddtree_accept",
-              "ddtree_workspace_size", "ddtree_device_check", "ddtree_status_str"):
+              "ddtree_commit", "ddtree_workspace_size", "ddtree_device_check",
+              "ddtree_status_str"):
         assert n in names
 
 
@@ -83,3 +84,10 @@ def test_invalid_arguments_rejected_before_launch(lib):
     # accept without workspace
     assert L.ddtree_accept(fake, 0, 10, fake, fake, fake, 1, 4, 4, 10, 0.0, 0, 0, None, fake,
                            fake, fake, fake, None, 0, None) == 1
+    # commit: null cache, a head dimension that is not a multiple of 8, unaligned K/V
+    assert L.ddtree_commit(None, fake, 64, fake, fake, fake, fake, fake, 1, 4, 8, 2, 64,
+                           None) == 1
+    assert L.ddtree_commit(fake, fake, 64, fake, fake, fake, fake, fake, 1, 4, 8, 2, 60,
+                           None) == 2
+    assert L.ddtree_commit(P(0x1008), fake, 64, fake, fake, fake, fake, fake, 1, 4, 8, 2, 64,
+                           None) == 1
