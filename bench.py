@@ -45,6 +45,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-x36", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--acceptance-stats", type=int, default=0, metavar="ROUNDS",
+                    help="instead of timing: run ROUNDS independent synthetic rounds per node "
+                         "budget (and the K = 1 chain) and report acceptance lengths")
     ap.add_argument("--profile-rounds", type=int, default=0,
                     help="only run this many eager rounds (rotating input copies) and exit; "
                          "for kernel profilers")
@@ -581,6 +584,58 @@ def config_of(w, R):
     return c
 
 
+def acceptance_stats(rounds: int) -> dict:
+    """Acceptance length against the node budget on the budget-sweep shape
+    (L = 16, V = 151936, bf16, greedy), plus the vanilla chain (K = 1, N = L):
+    a synthetic analogue of the pages' acceptance-vs-budget study (§5).  Every
+    round draws fresh draft logits (3 N(0,1) + a +6 spike per position) and
+    target rows (the draft row at the node's depth + N(0,1)) on the device and
+    runs top-K -> build -> accept through the library.  Also reports the
+    surrogate of §4.2, sum over drafted nodes of exp(score): the expected
+    accepted length if the target followed the factorised draft exactly."""
+    import torch
+    from diffusion_draft_tree_gb300 import ops
+
+    dev = torch.device("cuda", 0)
+    base = wl.CONFIGS["budget_sweep_n512"]
+    L, V = base.L, base.V
+    out = {"metric": "acceptance length (accepted draft tokens per round)", "rounds": rounds,
+           "shape": {"L": L, "V": V, "draft": "3*N(0,1) + 6 spike", "target": "draft row at "
+                     "depth + N(0,1)", "temperature": 0.0}, "budgets": {}}
+    for label, K, N in [("chain K=1 N=16", 1, 16), ("N=32", 16, 32), ("N=64", 16, 64),
+                        ("N=128", 16, 128), ("N=256", 16, 256), ("N=512", 16, 512),
+                        ("N=1024", 16, 1024)]:
+        g = torch.Generator(device=dev)
+        g.manual_seed(0xACC + 7919 * K + N)
+        lens, surr = [], []
+        bonus = torch.zeros(1, dtype=torch.int32, device=dev)
+        plen = torch.zeros(1, dtype=torch.int32, device=dev)
+        for _ in range(rounds):
+            d32 = torch.randn((L, V), generator=g, device=dev) * 3.0
+            spike = torch.randint(0, V, (L,), generator=g, device=dev)
+            d32[torch.arange(L, device=dev), spike] += 6.0
+            draft = d32.to(torch.bfloat16)
+            idx, lp, _ = ops.topk(draft, K)
+            tree = ops.build(lp.view(1, L, K), idx.view(1, L, K), bonus, plen, N)
+            depth = tree["depth"][0].long()
+            rows = draft.float()[depth.clamp(min=0).clamp(max=L - 1)]
+            noise = torch.randn(rows.shape, generator=g, device=dev)
+            target = (rows + noise).to(torch.bfloat16)[None]
+            acc = ops.accept(target, tree, L)
+            lens.append(int(acc["accept_len"][0].item()))
+            n = int(tree["n_nodes"][0].item())
+            surr.append(float(torch.exp(tree["score"][0, 1:n + 1].double()).sum().item()))
+        ops.ddtree_device_check()
+        a = np.array(lens)
+        entry = {"K": K, "N": N, "mean_accept_len": float(a.mean()),
+                 "tokens_per_round": float(a.mean() + 1), "std": float(a.std()),
+                 "surrogate_mean": float(np.mean(surr))}
+        if N in (512, 16):
+            entry["histogram"] = [int((a == k).sum()) for k in range(L + 1)]
+        out["budgets"][label] = entry
+    return out
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -589,6 +644,10 @@ def main():
         world = 1
     if args.impl == "reference":
         reference_arm(args, rank, world)
+        return
+    if args.acceptance_stats:
+        if rank == 0:
+            print(json.dumps(acceptance_stats(args.acceptance_stats)), flush=True)
         return
     import torch
     if world > 1:

@@ -15,9 +15,12 @@ from tests.gpu_util import dev_bf16, dev_i32, dev_logits, host
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("name", ["tiny", "8b_single"])
+@pytest.mark.parametrize("name", ["tiny", "8b_single", "8b_single_chain"])
 def test_round_chain_matches_oracle_chain(cuda_device, name):
-    w = wl.CONFIGS[name]
+    """8b_single_chain is the vanilla DFlash chain (K = 1, N = L): one token per
+    draft position, accepted while it matches the target's token."""
+    w = (wl.CONFIGS["8b_single"].with_(K=1, N=16) if name == "8b_single_chain"
+         else wl.CONFIGS[name])
     dev = cuda_device
     draft, bonus, plen = wl.draft_logits(w), wl.bonus_tokens(w), wl.prefix_lengths(w)
     o_idx, _, o_lp32, _ = oracle.topk(draft, w.dtype, w.K)
@@ -49,6 +52,15 @@ def test_round_chain_matches_oracle_chain(cuda_device, name):
     n_acc = o_acc["accept_len"][0]
     assert [g_paths[u] for u in host(acc["accepted_nodes"])[0, :n_acc]] == \
         [o_paths[u] for u in o_acc["accepted_nodes"][0, :n_acc]]
+    if w.K == 1:
+        # the chain: node d is the draft argmax at position d-1; accepted while it
+        # equals the target's argmax at node d-1
+        t = np.argmax(wl.bf16_to_f32(x[0]), axis=1)
+        chain_tok = np.argmax(wl.bf16_to_f32(draft[0]), axis=1)
+        expect = 0
+        while expect < w.L and chain_tok[expect] == t[expect]:
+            expect += 1
+        assert host(acc["accept_len"])[0] == expect
 
 
 def _paths(parent, token, n):
