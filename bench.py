@@ -404,6 +404,42 @@ def gpu_arm(args, rank, world, dev):
     except Exception as e:  # noqa: BLE001
         commit = {"unavailable": repr(e)}
 
+    # the path-only walk on the same round's tree and target rows (an alternative
+    # to the full-tree accept; timed alone, not in the round's metric)
+    accept_path = None
+    try:
+        r0 = rounds[0]
+        acc2 = ops.accept_buffers(w.B, w.L, w.N, dev)
+        n_p = 20
+        p_ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+                for _ in range(n_p)]
+
+        def path_once(ev):
+            ev[0].record()
+            ops.ddtree_accept_path(r0.inp["target"], r0.tree["parent"], r0.tree["token"],
+                                   r0.tree["n_nodes"], w.L, acc2, w.T, wl.philox_seed(w), 0)
+            ev[1].record()
+
+        path_once(p_ev[0])
+        torch.cuda.synchronize()
+        g_p = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_p, stream=stream):
+            for ev in p_ev:
+                path_once(ev)
+        t_p = 0.0
+        for _ in range(5):
+            g_p.replay()
+            torch.cuda.synchronize()
+            t_p += sum(ev[0].elapsed_time(ev[1]) for ev in p_ev)
+        ops.ddtree_device_check()
+        same = bool(torch.equal(acc2["out_tokens"], r0.acc["out_tokens"]))
+        rows = int(acc2["accept_len"].sum().item()) + w.B
+        accept_path = {"ms": t_p / (5 * n_p), "bytes": rows * w.V * w.esize,
+                       "same_tokens_as_full_walk": same}
+        del acc2
+    except Exception as e:  # noqa: BLE001
+        accept_path = {"unavailable": repr(e)}
+
     # 36-layer round: 36 tree-attention launches, each on its own KV cache
     x36 = None
     if not args.no_x36:
@@ -485,7 +521,7 @@ def gpu_arm(args, rank, world, dev):
                            rounds[0].tree["anc_mask"].cpu().numpy().view(np.uint32).ravel()]))
     return {"w": w, "ms_total": ms_total, "R": R, "per_copy": per_copy, "clocks": clocks,
             "kern_ms": kern_ms, "kern_method": kern_method, "x36": x36, "e2e": e2e,
-            "commit": commit,
+            "commit": commit, "accept_path": accept_path,
             "tree_anc": tree_anc}
 
 
@@ -685,6 +721,14 @@ def main():
                              "hbm_frac": c["bytes"] / (c["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
                              "note": "after the round, not in its metric: the accepted "
                                      "path's K/V rows into the cache"}
+    c = res.get("accept_path")
+    if c and "ms" in c:
+        kernels["accept_path"] = {
+            "ms": c["ms"], "GBps": c["bytes"] / (c["ms"] * 1e-3) / 1e9,
+            "hbm_frac": c["bytes"] / (c["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "same_tokens_as_full_walk": c["same_tokens_as_full_walk"],
+            "note": "alternative step 4 reading only the accepted path's rows "
+                    "(bytes = (accept_len + 1) x V x elem per sequence); timed alone"}
     a = model["tree_attn"]
     t_hbm = a["bytes"] / (peaks["hbm_gbs"] * 1e9)
     t_tc = a["flops"] / (peaks["bf16_tflops"] * 1e12)

@@ -180,6 +180,29 @@ ddtree_status ddtree_accept(const void* target_logits, int dtype, int64_t row_st
     return launched(ddt::launch_accept(a, (cudaStream_t)stream));
 }
 
+ddtree_status ddtree_accept_path(const void* target_logits, int dtype, int64_t row_stride,
+                                 const int32_t* parent, const int32_t* token,
+                                 const int32_t* n_nodes, int B, int L, int N, int V,
+                                 float temperature, uint64_t seed, uint64_t step,
+                                 int32_t* target_token, int32_t* accept_len,
+                                 int32_t* accepted_nodes, int32_t* out_tokens,
+                                 int32_t* next_bonus, void* stream) {
+    if (!target_logits || !parent || !token || !n_nodes || !accept_len || !accepted_nodes ||
+        !out_tokens || !next_bonus)
+        return DDTREE_ERR_INVALID_ARG;
+    if (dtype != DDTREE_BF16 && dtype != DDTREE_FP32) return DDTREE_ERR_INVALID_ARG;
+    if (B <= 0 || B > 65535 || L <= 0 || N < 0 || V <= 0 || row_stride < V ||
+        !(temperature >= 0.f) || temperature > 1e30f)
+        return DDTREE_ERR_INVALID_ARG;
+    if (N > DDTREE_MAX_N || L > DDTREE_MAX_L || !ddt::accept_path_supported(V, dtype))
+        return DDTREE_ERR_UNSUPPORTED;
+    if (!aligned(target_logits, dtype == DDTREE_BF16 ? 2 : 4)) return DDTREE_ERR_INVALID_ARG;
+    ddt::AcceptArgs a{target_logits, dtype, row_stride, parent, token, n_nodes, B, L, N, V,
+                      temperature, seed, step, target_token, accept_len, accepted_nodes,
+                      out_tokens, next_bonus, nullptr, error_word()};
+    return launched(ddt::launch_accept_path(a, (cudaStream_t)stream));
+}
+
 ddtree_status ddtree_commit(void* k_cache, void* v_cache, int64_t cache_cap, const void* k_tree,
                             const void* v_tree, const int32_t* accept_len,
                             const int32_t* accepted_nodes, int32_t* prefix_len, int B, int L,

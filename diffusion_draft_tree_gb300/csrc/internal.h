@@ -77,6 +77,9 @@ struct AcceptArgs {
 size_t accept_workspace_bytes(int B, int N, int V, int dtype);
 bool accept_supported(int V, int dtype);
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s);
+// The walk reading only the rows on the accepted path (no workspace).
+bool accept_path_supported(int V, int dtype);
+cudaError_t launch_accept_path(const AcceptArgs& a, cudaStream_t s);
 
 // ---- after the walk: commit the accepted path to the KV cache -----------------
 struct CommitArgs {

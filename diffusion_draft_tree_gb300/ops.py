@@ -59,13 +59,15 @@ def _load() -> ctypes.CDLL:
     lib.ddtree_accept.argtypes = [P, i32, i64, P, P, P, i32, i32, i32, i32, f32, u64, u64, P, P,
                                   P, P, P, P, sz, P]
     lib.ddtree_commit.argtypes = [P, P, i64, P, P, P, P, P, i32, i32, i32, i32, i32, P]
+    lib.ddtree_accept_path.argtypes = [P, i32, i64, P, P, P, i32, i32, i32, i32, f32, u64, u64,
+                                       P, P, P, P, P, P]
     lib.ddtree_device_check.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
     lib.ddtree_last_cuda_error.argtypes = []
     lib.ddtree_last_cuda_error.restype = ctypes.c_char_p
     lib.ddtree_status_str.argtypes = [i32]
     lib.ddtree_status_str.restype = ctypes.c_char_p
     for f in ("ddtree_topk", "ddtree_build", "ddtree_build_heap", "ddtree_tree_attn",
-              "ddtree_accept", "ddtree_commit", "ddtree_device_check"):
+              "ddtree_accept", "ddtree_accept_path", "ddtree_commit", "ddtree_device_check"):
         getattr(lib, f).restype = i32
     return lib
 
@@ -163,6 +165,27 @@ def ddtree_accept(target_logits, parent, token, n_nodes, L, out: dict, temperatu
         _ptr(out.get("target_token")), _ptr(out["accept_len"]), _ptr(out["accepted_nodes"]),
         _ptr(out["out_tokens"]), _ptr(out["next_bonus"]), _ptr(ws),
         ws.numel() if ws is not None else 0, _stream(stream)))
+
+
+def ddtree_accept_path(target_logits, parent, token, n_nodes, L, out: dict, temperature=0.0,
+                       seed=0, step=0, stream=None):
+    """The walk reading only the rows on the accepted path (same outputs as
+    ddtree_accept; target_token on the path only)."""
+    B, R, V = target_logits.shape
+    _check("ddtree_accept_path", lib.ddtree_accept_path(
+        _ptr(target_logits), _dtype_code(target_logits), V, _ptr(parent), _ptr(token),
+        _ptr(n_nodes), B, L, R - 1, V, float(temperature), int(seed), int(step),
+        _ptr(out.get("target_token")), _ptr(out["accept_len"]), _ptr(out["accepted_nodes"]),
+        _ptr(out["out_tokens"]), _ptr(out["next_bonus"]), _stream(stream)))
+
+
+def accept_path(target_logits, tree: dict, L: int, temperature=0.0, seed=0, step=0,
+                stream=None) -> dict:
+    B, R, V = target_logits.shape
+    out = accept_buffers(B, L, R - 1, target_logits.device)
+    ddtree_accept_path(target_logits, tree["parent"], tree["token"], tree["n_nodes"], L, out,
+                       temperature, seed, step, stream)
+    return out
 
 
 def ddtree_commit(k_cache, v_cache, k_tree, v_tree, accept_len, accepted_nodes, prefix_len,

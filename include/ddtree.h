@@ -207,6 +207,23 @@ ddtree_status ddtree_accept(const void* target_logits, int dtype, int64_t row_st
                             int32_t* accepted_nodes, int32_t* out_tokens, int32_t* next_bonus,
                             void* workspace, size_t ws_bytes, void* stream);
 
+/* Step 4, reading only the accepted path.  Same arguments and results as
+ * ddtree_accept (accept_len, accepted_nodes, out_tokens, next_bonus are
+ * identical; the same Philox uniform per node), except that target_token is
+ * written only for the nodes the walk visits (the root and the accepted
+ * nodes; -1 elsewhere) and no workspace is needed.  The pages' walk needs the
+ * target's token only on that path (§4.1), so HBM traffic is
+ * (accept_len + 1) x V x elem per sequence instead of (n + 1) x V x elem; the
+ * rows are resolved one after another, so it pays when N >> accept_len.  One
+ * CTA per sequence. */
+ddtree_status ddtree_accept_path(const void* target_logits, int dtype, int64_t row_stride,
+                                 const int32_t* parent, const int32_t* token,
+                                 const int32_t* n_nodes, int B, int L, int N, int V,
+                                 float temperature, uint64_t seed, uint64_t step,
+                                 int32_t* target_token, int32_t* accept_len,
+                                 int32_t* accepted_nodes, int32_t* out_tokens,
+                                 int32_t* next_bonus, void* stream);
+
 /* After the walk -- commit the accepted path to the KV cache.
  * Pages: §3 (the bonus token is not yet in the cache when the round starts),
  * §4.1 (the root is the bonus token; the matched path is accepted): the

@@ -27,8 +27,8 @@ def _declared():
 def test_header_declares_the_round(lib):
     names = _declared()
     for n in ("ddtree_topk", "ddtree_build", "ddtree_tree_attn", "ddtree_accept",
-              "ddtree_commit", "ddtree_workspace_size", "ddtree_device_check",
-              "ddtree_status_str"):
+              "ddtree_accept_path", "ddtree_commit", "ddtree_workspace_size",
+              "ddtree_device_check", "ddtree_status_str"):
         assert n in names
 
 
@@ -84,6 +84,11 @@ def test_invalid_arguments_rejected_before_launch(lib):
     # accept without workspace
     assert L.ddtree_accept(fake, 0, 10, fake, fake, fake, 1, 4, 4, 10, 0.0, 0, 0, None, fake,
                            fake, fake, fake, None, 0, None) == 1
+    # path-only accept: negative temperature, budget above the limit
+    assert L.ddtree_accept_path(fake, 0, 10, fake, fake, fake, 1, 4, 4, 10, -1.0, 0, 0, None,
+                                fake, fake, fake, fake, None) == 1
+    assert L.ddtree_accept_path(fake, 0, 10, fake, fake, fake, 1, 4, 5000, 10, 0.0, 0, 0, None,
+                                fake, fake, fake, fake, None) == 2
     # commit: null cache, a head dimension that is not a multiple of 8, unaligned K/V
     assert L.ddtree_commit(None, fake, 64, fake, fake, fake, fake, fake, 1, 4, 8, 2, 64,
                            None) == 1
