@@ -13,10 +13,10 @@
 //
 // T_d is the top N among all prefixes of depth <= d (a depth-d prefix in it
 // has its parent in it, and that parent is among the top N of depth <= d-1).
-// When T_{d-1} is full, a child must beat its last element: a strictly higher
-// score, because the child is deeper.  Children of one parent are generated in
-// rank order, sorted (rank counting for small batches, bitonic otherwise, in
-// shared memory) and merged into T with a rank-by-binary-search merge.  The result -- nodes, their order, fp32 scores
+// When T is full, a child must beat its last key.  The qualifying children
+// are gathered (in any order), sorted (rank counting for small batches,
+// bitonic otherwise, in shared memory) and merged into T with a
+// rank-by-binary-search merge.  The result -- nodes, their order, fp32 scores
 // formed as parent score + log-prob -- is identical to the heap's.
 //
 // One CTA per sequence (128 threads for budgets up to 128, else 512).  T holds 64-bit keys:
@@ -49,28 +49,16 @@ DDT_DEV uint64_t lk_with_ppos(uint64_t k, int ppos) {
     return (k & ~(0x7ffull << 16)) | ((uint64_t)(2046 - ppos) << 16);
 }
 
-// Exclusive scan of one int per thread over the CTA; *total gets the sum.
-template <int kThreads>
-DDT_DEV int block_scan(int v, int* s_warp, int* total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-    }
-    if (lane == 31) s_warp[warp] = incl;
-    __syncthreads();
-    int before = 0, tot = 0;
-#pragma unroll
-    for (int i = 0; i < kThreads / 32; ++i) {
-        const int w = s_warp[i];
-        before += (i < warp) ? w : 0;
-        tot += w;
-    }
-    *total = tot;
-    __syncthreads();
-    return before + incl - v;
+// A slot for this lane's item (when `take`) at the end of a shared list whose
+// length is *cnt: one atomic per warp.  Every lane of the warp calls it; the
+// order of the warps' runs is arbitrary.
+DDT_DEV int warp_append_slot(bool take, int* cnt) {
+    const unsigned m = __ballot_sync(0xffffffffu, take);
+    const int lane = threadIdx.x & 31;
+    int base = 0;
+    if (lane == 0 && m) base = atomicAdd(cnt, __popc(m));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    return base + __popc(m & ((1u << lane) - 1u));
 }
 
 // Number of keys of the descending array a[0..n) that are larger than x.
@@ -100,18 +88,19 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
     __shared__ float s_pscore[DDTREE_MAX_N];   // ... and their scores
     __shared__ int16_t s_map[DDTREE_MAX_N];
     __shared__ float s_lp[DDTREE_MAX_L * DDTREE_MAX_K];
-    __shared__ int s_warp[kThreads / 32];
     __shared__ int s_flag;
-    constexpr int kPairsPerThread = kCandCap / kThreads;
-    constexpr int kPosPerThread = DDTREE_MAX_N / kThreads;
+    // list lengths, double-buffered so that a counter is reset while its
+    // previous value can no longer be read: parents by level, children by batch
+    __shared__ int s_np[2], s_nc[2];
 
     const int b = blockIdx.x, tid = threadIdx.x;
     const int LK = L * K;
     pdl_wait();
     for (int i = tid; i < LK; i += kThreads) s_lp[i] = topk_logp[(size_t)b * LK + i];
+    if (tid < 2) s_np[tid] = s_nc[tid] = 0;
     __syncthreads();
 
-    int t = 0, cur = 0;
+    int t = 0, cur = 0, nb = 0;
     for (int d = 1; d <= L && N > 0; ++d) {
         // ---- parents: the depth-(d-1) nodes of T, in T order -----------------------
         int npar;
@@ -123,26 +112,20 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
             }
             __syncthreads();
         } else {
-            int f[kPosPerThread];
-            int fs = 0;
-#pragma unroll
-            for (int j = 0; j < kPosPerThread; ++j) {
-                const int i = tid * kPosPerThread + j;
-                f[j] = (i < t && lk_depth(s_T[cur][i]) == d - 1) ? 1 : 0;
-                fs += f[j];
-            }
-            int tot;
-            int pos = block_scan<kThreads>(fs, s_warp, &tot);
-#pragma unroll
-            for (int j = 0; j < kPosPerThread; ++j) {
-                if (f[j]) {
-                    s_plist[pos] = (int16_t)(tid * kPosPerThread + j);
-                    s_pscore[pos] = lk_score(s_T[cur][tid * kPosPerThread + j]);
-                    ++pos;
+            // (in any order: the children are sorted by their full keys below)
+            if (tid == 0) s_np[(d + 1) & 1] = 0;
+            const int tr = (t + kThreads - 1) / kThreads * kThreads;
+            for (int i = tid; i < tr; i += kThreads) {
+                const uint64_t k = i < t ? s_T[cur][i] : 0ull;
+                const bool f = i < t && lk_depth(k) == d - 1;
+                const int pos = warp_append_slot(f, &s_np[d & 1]);
+                if (f) {
+                    s_plist[pos] = (int16_t)i;
+                    s_pscore[pos] = lk_score(k);
                 }
             }
-            npar = tot;
             __syncthreads();
+            npar = s_np[d & 1];
         }
         if (npar == 0) break;
         for (int i = tid; i < t; i += kThreads) s_orig[cur][i] = (int16_t)i;
@@ -152,38 +135,29 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
         const float* lp = s_lp + (d - 1) * K;
         for (int base = 0; base < pairs; base += kCandCap) {
             const bool full = (t == N);
-            const float theta = full ? lk_score(s_T[cur][t - 1]) : 0.f;
-            uint64_t key[kPairsPerThread];
-            int cnt = 0;
-            // pair q = (parent q / K, rank q % K); strided over the threads so that
-            // a small batch spreads over all of them (the batch is sorted below,
-            // so the order of the keys is free); one division, then increments
-            const int step_pi = kThreads / K, step_r = kThreads - step_pi * K;
-            int pi = (base + tid) / K, r = base + tid - pi * K;
-#pragma unroll
-            for (int j = 0; j < kPairsPerThread; ++j) {
-                const int q = base + j * kThreads + tid;
-                key[j] = 0ull;
-                if (q < pairs) {
-                    const int pp = s_plist[pi];
+            // a child enters a full T only by beating its last key (keys are a
+            // total order, so the batches may come in any parent order)
+            const uint64_t theta = full ? s_T[cur][t - 1] : 0ull;
+            // pair q = (parent q / K, rank q % K), appended when it can enter T
+            // (the batch is sorted below, so the order of the keys is free)
+            const int q_end = min(pairs, base + kCandCap);
+            const int qr = base + (q_end - base + kThreads - 1) / kThreads * kThreads;
+            int* cnt = &s_nc[nb & 1];
+            if (tid == 0) s_nc[(nb + 1) & 1] = 0;
+            ++nb;
+            for (int q = base + tid; q < qr; q += kThreads) {
+                uint64_t key = 0ull;
+                if (q < q_end) {
+                    const int pi = q / K, r = q - pi * K;
                     const float sc = __fadd_rn(s_pscore[pi], lp[r]);
-                    if (!full || sc > theta) {
-                        key[j] = lkey(sc, d, pp, r);
-                        ++cnt;
-                    }
+                    const uint64_t k = lkey(sc, d, s_plist[pi], r);
+                    if (k > theta) key = k;
                 }
-                pi += step_pi;
-                r += step_r;
-                if (r >= K) {
-                    r -= K;
-                    ++pi;
-                }
+                const int pos = warp_append_slot(key != 0ull, cnt);
+                if (key != 0ull) s_cand[pos] = key;
             }
-            int c;
-            int pos = block_scan<kThreads>(cnt, s_warp, &c);
-#pragma unroll
-            for (int j = 0; j < kPairsPerThread; ++j)
-                if (key[j]) s_cand[pos++] = key[j];
+            __syncthreads();
+            const int c = *cnt;
             if (c == 0) {
                 __syncthreads();
                 continue;
