@@ -49,6 +49,30 @@ DDT_DEV uint64_t lk_with_ppos(uint64_t k, int ppos) {
     return (k & ~(0x7ffull << 16)) | ((uint64_t)(2046 - ppos) << 16);
 }
 
+// Exclusive scan of one int per thread over the CTA; *total gets the sum.
+template <int kThreads>
+DDT_DEV int block_scan(int v, int* s_warp, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    int before = 0, tot = 0;
+#pragma unroll
+    for (int i = 0; i < kThreads / 32; ++i) {
+        const int w = s_warp[i];
+        before += (i < warp) ? w : 0;
+        tot += w;
+    }
+    *total = tot;
+    __syncthreads();
+    return before + incl - v;
+}
+
 // A slot for this lane's item (when `take`) at the end of a shared list whose
 // length is *cnt: one atomic per warp.  Every lane of the warp calls it; the
 // order of the warps' runs is arbitrary.
@@ -89,6 +113,8 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
     __shared__ int16_t s_map[DDTREE_MAX_N];
     __shared__ float s_lp[DDTREE_MAX_L * DDTREE_MAX_K];
     __shared__ int s_flag;
+    __shared__ int s_warp[kThreads / 32];
+    constexpr int kPosPerThread = DDTREE_MAX_N / kThreads;
     // list lengths, double-buffered so that a counter is reset while its
     // previous value can no longer be read: parents by level, children by batch
     __shared__ int s_np[2], s_nc[2];
@@ -111,8 +137,32 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
                 s_pscore[0] = 0.f;  // the root: the empty prefix, probability 1
             }
             __syncthreads();
+        } else if (t * K > kCandCap) {
+            // children in several batches: parents in T order, so that the first
+            // batches hold the strongest children and T's last key rises early
+            if (tid == 0) s_np[(d + 1) & 1] = 0;
+            int f[kPosPerThread];
+            int fs = 0;
+#pragma unroll
+            for (int j = 0; j < kPosPerThread; ++j) {
+                const int i = tid * kPosPerThread + j;
+                f[j] = (i < t && lk_depth(s_T[cur][i]) == d - 1) ? 1 : 0;
+                fs += f[j];
+            }
+            int tot;
+            int pos = block_scan<kThreads>(fs, s_warp, &tot);
+#pragma unroll
+            for (int j = 0; j < kPosPerThread; ++j) {
+                if (f[j]) {
+                    s_plist[pos] = (int16_t)(tid * kPosPerThread + j);
+                    s_pscore[pos] = lk_score(s_T[cur][tid * kPosPerThread + j]);
+                    ++pos;
+                }
+            }
+            npar = tot;
+            __syncthreads();
         } else {
-            // (in any order: the children are sorted by their full keys below)
+            // one batch: parents in any order (the children are sorted below)
             if (tid == 0) s_np[(d + 1) & 1] = 0;
             const int tr = (t + kThreads - 1) / kThreads * kThreads;
             for (int i = tid; i < tr; i += kThreads) {
