@@ -118,18 +118,22 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
     // list lengths, double-buffered so that a counter is reset while its
     // previous value can no longer be read: parents by level, children by batch
     __shared__ int s_np[2], s_nc[2];
+    __shared__ int s_fp[2];  // T position of the strongest parent, by level parity
 
     const int b = blockIdx.x, tid = threadIdx.x;
     const int LK = L * K;
     pdl_wait();
     for (int i = tid; i < LK; i += kThreads) s_lp[i] = topk_logp[(size_t)b * LK + i];
-    if (tid < 2) s_np[tid] = s_nc[tid] = 0;
+    if (tid < 2) {
+        s_np[tid] = s_nc[tid] = 0;
+        s_fp[tid] = 0x7fffffff;
+    }
     __syncthreads();
 
     int t = 0, cur = 0, nb = 0;
     for (int d = 1; d <= L && N > 0; ++d) {
-        // ---- parents: the depth-(d-1) nodes of T, in T order -----------------------
-        int npar;
+        // ---- parents: the depth-(d-1) nodes of T -----------------------------------
+        int npar, first = 0;
         if (d == 1) {
             npar = 1;
             if (tid == 0) {
@@ -161,9 +165,13 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
             }
             npar = tot;
             __syncthreads();
+            first = s_plist[0];
         } else {
             // one batch: parents in any order (the children are sorted below)
-            if (tid == 0) s_np[(d + 1) & 1] = 0;
+            if (tid == 0) {
+                s_np[(d + 1) & 1] = 0;
+                s_fp[(d + 1) & 1] = 0x7fffffff;
+            }
             const int tr = (t + kThreads - 1) / kThreads * kThreads;
             for (int i = tid; i < tr; i += kThreads) {
                 const uint64_t k = i < t ? s_T[cur][i] : 0ull;
@@ -173,11 +181,21 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
                     s_plist[pos] = (int16_t)i;
                     s_pscore[pos] = lk_score(k);
                 }
+                const int fm = __reduce_min_sync(0xffffffffu, f ? i : 0x7fffffff);
+                if ((tid & 31) == 0 && fm != 0x7fffffff) atomicMin(&s_fp[d & 1], fm);
             }
             __syncthreads();
             npar = s_np[d & 1];
+            first = s_fp[d & 1];
         }
         if (npar == 0) break;
+        // T is sorted, so its first depth-(d-1) node is the strongest parent, and
+        // lkey(its score + the best log-prob, d, position 0, rank 0) bounds every
+        // child's key: when that cannot beat a full T's last key, no node of
+        // depth >= d enters and the tree is complete.
+        if (t == N && lkey(__fadd_rn(lk_score(s_T[cur][first]), s_lp[(d - 1) * K]), d, 0, 0) <=
+                          s_T[cur][t - 1])
+            break;
         for (int i = tid; i < t; i += kThreads) s_orig[cur][i] = (int16_t)i;
 
         // ---- children in batches of kCandCap (parent, rank) pairs --------------------

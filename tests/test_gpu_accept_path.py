@@ -171,3 +171,27 @@ def test_accept_path_bad_n_nodes_is_reported(cuda_device):
     with pytest.raises(ops.DDTreeError) as e:
         ops.ddtree_device_check()
     assert e.value.detail == 0x04000002
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_accept_budget_1024(cuda_device, T):
+    """The largest budget (1025 rows, ancestor masks of 33 words): both walks
+    against the oracle."""
+    from tests.test_gpu_accept import _check as check_full
+    rng = np.random.default_rng(1024 + int(T))
+    B, L, K, N, V = 2, 16, 32, 1024, 3000
+    lp = -np.sort(rng.exponential(0.5, size=(B, L, K)).astype(np.float32), axis=2)
+    lp = -np.sort(-lp, axis=2)
+    tok = np.stack([[rng.permutation(V)[:K] for _ in range(L)] for _ in range(B)]).astype(np.int32)
+    t = oracle.build_tree(lp, tok, rng.integers(0, V, size=B).astype(np.int32),
+                          np.zeros(B, np.int32), N)
+    assert np.all(t["n_nodes"] == N)
+    x = (rng.standard_normal((B, N + 1, V)) * 2).astype(np.float32)
+    for b in range(B):
+        for c in range(1, N + 1):
+            if t["rank"][b, c] == 0:
+                x[b, t["parent"][b, c], t["token"][b, c]] += 12
+    ref, _ = _check(x, wl.FP32, t, L, T, 77, 5, cuda_device)
+    check_full(x, wl.FP32, t, L, T, 77, 5, cuda_device)
+    if T == 0.0:
+        assert ref["accept_len"].min() >= 2  # the planted rank-0 chain is walked
