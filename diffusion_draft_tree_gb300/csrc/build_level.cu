@@ -73,6 +73,61 @@ DDT_DEV int block_scan(int v, int* s_warp, int* total) {
     return before + incl - v;
 }
 
+// Sorts s[0..p2) descending, p2 a power of two <= 4 kThreads (the keys past
+// the batch are zero): a bitonic network with four keys a thread, strides below
+// 4 inside the thread, below 128 by warp shuffles, only the longer strides
+// through shared memory (2 barriers each instead of one per stage).
+template <int kThreads>
+DDT_DEV void bitonic_desc_regs(uint64_t* s, int p2) {
+    constexpr int E = 4;
+    const int tid = threadIdx.x;
+    uint64_t a[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) a[e] = s[tid * E + e];
+#pragma unroll 1
+    for (int k2 = 2; k2 <= p2; k2 <<= 1) {
+#pragma unroll 1
+        for (int j = k2 >> 1; j > 0; j >>= 1) {
+            if (j < E) {
+                uint64_t b[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int i = tid * E + e;
+                    const uint64_t q = (j == 1) ? a[e ^ 1] : a[e ^ 2];
+                    const bool keep_max = ((i & j) == 0) == ((i & k2) == 0);
+                    b[e] = keep_max ? umax64(a[e], q) : umin64(a[e], q);
+                }
+#pragma unroll
+                for (int e = 0; e < E; ++e) a[e] = b[e];
+            } else if (j < 32 * E) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int i = tid * E + e;
+                    const uint64_t q = shfl_xor_u64(a[e], j / E);
+                    const bool keep_max = ((i & j) == 0) == ((i & k2) == 0);
+                    a[e] = keep_max ? umax64(a[e], q) : umin64(a[e], q);
+                }
+            } else {
+                __syncthreads();  // the previous shared stage has been read
+#pragma unroll
+                for (int e = 0; e < E; ++e) s[tid * E + e] = a[e];
+                __syncthreads();
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int i = tid * E + e;
+                    const uint64_t q = s[i ^ j];
+                    const bool keep_max = ((i & j) == 0) == ((i & k2) == 0);
+                    a[e] = keep_max ? umax64(a[e], q) : umin64(a[e], q);
+                }
+            }
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < E; ++e) s[tid * E + e] = a[e];
+    __syncthreads();
+}
+
 // A slot for this lane's item (when `take`) at the end of a shared list whose
 // length is *cnt: one atomic per warp.  Every lane of the warp calls it; the
 // order of the warps' runs is arbitrary.
@@ -246,6 +301,11 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
             } else {
                 int p2 = 1;
                 while (p2 < c) p2 <<= 1;
+                if constexpr (4 * kThreads == kCandCap) {
+                    for (int i = c + tid; i < kCandCap; i += kThreads) s_cand[i] = 0ull;
+                    __syncthreads();
+                    bitonic_desc_regs<kThreads>(s_cand, p2);
+                } else {
                 for (int i = c + tid; i < p2; i += kThreads) s_cand[i] = 0ull;
                 __syncthreads();
                 for (int k2 = 2; k2 <= p2; k2 <<= 1) {
@@ -263,6 +323,7 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
                         }
                         __syncthreads();
                     }
+                }
                 }
             }
             // merge T[0..t) and cand[0..c) by output rank; keep the first N
