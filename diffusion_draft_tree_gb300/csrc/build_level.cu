@@ -73,13 +73,15 @@ DDT_DEV int block_scan(int v, int* s_warp, int* total) {
     return before + incl - v;
 }
 
-// Sorts s[0..p2) descending, p2 a power of two <= 4 kThreads (the keys past
-// the batch are zero): a bitonic network with four keys a thread, strides below
-// 4 inside the thread, below 128 by warp shuffles, only the longer strides
-// through shared memory (2 barriers each instead of one per stage).
+// Sorts s[0..p2) descending, p2 a power of two <= kCandCap (the buffer is
+// zero past the batch, up to kCandCap): a bitonic network with E = kCandCap /
+// kThreads keys a thread, strides below E inside the thread, below 32 E by warp
+// shuffles, only the longer strides through shared memory (two barriers each,
+// instead of one barrier for every stage).
 template <int kThreads>
 DDT_DEV void bitonic_desc_regs(uint64_t* s, int p2) {
-    constexpr int E = 4;
+    constexpr int E = kCandCap / kThreads;
+    static_assert(E == 4 || E == 16, "keys a thread");
     const int tid = threadIdx.x;
     uint64_t a[E];
 #pragma unroll
@@ -93,7 +95,10 @@ DDT_DEV void bitonic_desc_regs(uint64_t* s, int p2) {
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                     const int i = tid * E + e;
-                    const uint64_t q = (j == 1) ? a[e ^ 1] : a[e ^ 2];
+                    uint64_t q = a[e ^ 1];
+                    if (j == 2) q = a[e ^ 2];
+                    if (E > 4 && j == 4) q = a[(e ^ 4) % E];
+                    if (E > 8 && j == 8) q = a[(e ^ 8) % E];
                     const bool keep_max = ((i & j) == 0) == ((i & k2) == 0);
                     b[e] = keep_max ? umax64(a[e], q) : umin64(a[e], q);
                 }
@@ -287,8 +292,8 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
             }
             // Sort the batch, descending.  Small batches: each key's rank is
             // counted by its own thread and the key is scattered to that rank in
-            // the upper half of the buffer (one barrier).  Large batches: an
-            // in-place bitonic sort padded to a power of two.
+            // the upper half of the buffer (one barrier).  Large batches: a
+            // bitonic network held in registers, padded to a power of two.
             const uint64_t* sorted = s_cand;
             if (c <= kRankCountMax) {
                 __syncthreads();  // the batch's keys are in place
@@ -301,30 +306,9 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
             } else {
                 int p2 = 1;
                 while (p2 < c) p2 <<= 1;
-                if constexpr (4 * kThreads == kCandCap) {
-                    for (int i = c + tid; i < kCandCap; i += kThreads) s_cand[i] = 0ull;
-                    __syncthreads();
-                    bitonic_desc_regs<kThreads>(s_cand, p2);
-                } else {
-                for (int i = c + tid; i < p2; i += kThreads) s_cand[i] = 0ull;
+                for (int i = c + tid; i < kCandCap; i += kThreads) s_cand[i] = 0ull;
                 __syncthreads();
-                for (int k2 = 2; k2 <= p2; k2 <<= 1) {
-                    for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
-                        for (int i = tid; i < p2; i += kThreads) {
-                            const int ix = i ^ j2;
-                            if (ix > i) {
-                                const uint64_t a = s_cand[i], e = s_cand[ix];
-                                const bool desc = (i & k2) == 0;
-                                if (desc ? (a < e) : (a > e)) {
-                                    s_cand[i] = e;
-                                    s_cand[ix] = a;
-                                }
-                            }
-                        }
-                        __syncthreads();
-                    }
-                }
-                }
+                bitonic_desc_regs<kThreads>(s_cand, p2);
             }
             // merge T[0..t) and cand[0..c) by output rank; keep the first N
             const int nxt = cur ^ 1;
