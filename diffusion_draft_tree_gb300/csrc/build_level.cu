@@ -19,7 +19,7 @@
 // rank-by-binary-search merge.  The result -- nodes, their order, fp32 scores
 // formed as parent score + log-prob -- is identical to the heap's.
 //
-// One CTA per sequence (128 threads for budgets up to 128, else 512).  T holds 64-bit keys:
+// One CTA per sequence (128 threads for budgets up to 64, else 512).  T holds 64-bit keys:
 //   [63:32] orderable fp32 score, [31:27] 31 - depth,
 //   [26:16] 2046 - parent position (2047 for the root), [15:10] 63 - rank.
 // Parent positions refer to T_{d-1} while level d is built and are remapped to
@@ -35,7 +35,7 @@ namespace ddt {
 namespace {
 
 constexpr int kCandCap = 2048;  // children merged per batch
-constexpr int kRankCountMax = 256;  // batches up to this size are ranked by counting
+constexpr int kRankCountMax = 512;  // batches up to this size are ranked by counting
 
 DDT_DEV uint64_t lkey(float score, int depth, int ppos, int rank) {
     return ((uint64_t)ord_from_float(score) << 32) | ((uint32_t)(31 - depth) << 27) |
@@ -74,14 +74,14 @@ DDT_DEV int block_scan(int v, int* s_warp, int* total) {
 }
 
 // Sorts s[0..p2) descending, p2 a power of two <= kCandCap (the buffer is
-// zero past the batch, up to kCandCap): a bitonic network with E = kCandCap /
-// kThreads keys a thread, strides below E inside the thread, below 32 E by warp
-// shuffles, only the longer strides through shared memory (two barriers each,
-// instead of one barrier for every stage).
+// zero past the batch, up to kCandCap): a bitonic network with E = 4 keys a
+// thread (kThreads = 512), strides below E inside the thread, below 32 E by
+// warp shuffles, only the longer strides through shared memory (two barriers
+// each, instead of one barrier for every stage).
 template <int kThreads>
 DDT_DEV void bitonic_desc_regs(uint64_t* s, int p2) {
     constexpr int E = kCandCap / kThreads;
-    static_assert(E == 4 || E == 16, "keys a thread");
+    static_assert(E == 4, "keys a thread");
     const int tid = threadIdx.x;
     uint64_t a[E];
 #pragma unroll
@@ -95,10 +95,7 @@ DDT_DEV void bitonic_desc_regs(uint64_t* s, int p2) {
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                     const int i = tid * E + e;
-                    uint64_t q = a[e ^ 1];
-                    if (j == 2) q = a[e ^ 2];
-                    if (E > 4 && j == 4) q = a[(e ^ 4) % E];
-                    if (E > 8 && j == 8) q = a[(e ^ 8) % E];
+                    const uint64_t q = (j == 1) ? a[e ^ 1] : a[e ^ 2];
                     const bool keep_max = ((i & j) == 0) == ((i & k2) == 0);
                     b[e] = keep_max ? umax64(a[e], q) : umin64(a[e], q);
                 }
@@ -131,6 +128,35 @@ DDT_DEV void bitonic_desc_regs(uint64_t* s, int p2) {
 #pragma unroll
     for (int e = 0; e < E; ++e) s[tid * E + e] = a[e];
     __syncthreads();
+}
+
+// Writes each of the c distinct keys s[0..c) to s[kCandCap/2 + its rank in
+// descending order]; M keys a thread, ranked in one pass over the batch.
+template <int M, int kThreads>
+DDT_DEV void rank_scatter(uint64_t* s, int c) {
+    const int tid = threadIdx.x;
+    uint64_t kk[M];
+    int rk[M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        const int i = tid + m * kThreads;
+        kk[m] = i < c ? s[i] : ~0ull;
+        rk[m] = 0;
+    }
+    const ulonglong2* a2 = reinterpret_cast<const ulonglong2*>(s);
+#pragma unroll 4
+    for (int j = 0; j < (c >> 1); ++j) {
+        const ulonglong2 v = a2[j];
+#pragma unroll
+        for (int m = 0; m < M; ++m) rk[m] += (v.x > kk[m] ? 1 : 0) + (v.y > kk[m] ? 1 : 0);
+    }
+    if (c & 1) {
+#pragma unroll
+        for (int m = 0; m < M; ++m) rk[m] += s[c - 1] > kk[m] ? 1 : 0;
+    }
+#pragma unroll
+    for (int m = 0; m < M; ++m)
+        if (tid + m * kThreads < c) s[kCandCap / 2 + rk[m]] = kk[m];
 }
 
 // A slot for this lane's item (when `take`) at the end of a shared list whose
@@ -290,25 +316,48 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
                 __syncthreads();
                 continue;
             }
-            // Sort the batch, descending.  Small batches: each key's rank is
-            // counted by its own thread and the key is scattered to that rank in
-            // the upper half of the buffer (one barrier).  Large batches: a
-            // bitonic network held in registers, padded to a power of two.
+            // Sort the batch, descending.  Up to 512 keys: each key's rank is
+            // counted by its own thread (up to four keys a thread in one pass
+            // over the batch) and the key is scattered to that rank in the upper
+            // half of the buffer.  Larger batches: a bitonic network padded to a
+            // power of two (held in registers, four keys a thread, for the
+            // 512-thread variant; in shared memory for the 128-thread one).
             const uint64_t* sorted = s_cand;
             if (c <= kRankCountMax) {
                 __syncthreads();  // the batch's keys are in place
-                for (int i = tid; i < c; i += kThreads) {
-                    const uint64_t k = s_cand[i];
-                    s_cand[kCandCap / 2 + count_larger(s_cand, c, k)] = k;
-                }
+                // up to four keys a thread, counted in one pass over the batch
+                if (c <= kThreads) rank_scatter<1, kThreads>(s_cand, c);
+                else if (c <= 2 * kThreads) rank_scatter<2, kThreads>(s_cand, c);
+                else rank_scatter<(kRankCountMax + kThreads - 1) / kThreads, kThreads>(s_cand, c);
                 sorted = s_cand + kCandCap / 2;
                 __syncthreads();
             } else {
                 int p2 = 1;
                 while (p2 < c) p2 <<= 1;
-                for (int i = c + tid; i < kCandCap; i += kThreads) s_cand[i] = 0ull;
-                __syncthreads();
-                bitonic_desc_regs<kThreads>(s_cand, p2);
+                if constexpr (4 * kThreads == kCandCap) {
+                    for (int i = c + tid; i < kCandCap; i += kThreads) s_cand[i] = 0ull;
+                    __syncthreads();
+                    bitonic_desc_regs<kThreads>(s_cand, p2);
+                } else {
+                    for (int i = c + tid; i < p2; i += kThreads) s_cand[i] = 0ull;
+                    __syncthreads();
+                    for (int k2 = 2; k2 <= p2; k2 <<= 1) {
+                        for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
+                            for (int i = tid; i < p2; i += kThreads) {
+                                const int ix = i ^ j2;
+                                if (ix > i) {
+                                    const uint64_t a = s_cand[i], e = s_cand[ix];
+                                    const bool desc = (i & k2) == 0;
+                                    if (desc ? (a < e) : (a > e)) {
+                                        s_cand[i] = e;
+                                        s_cand[ix] = a;
+                                    }
+                                }
+                            }
+                            __syncthreads();
+                        }
+                    }
+                }
             }
             // merge T[0..t) and cand[0..c) by output rank; keep the first N
             const int nxt = cur ^ 1;
@@ -403,7 +452,7 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
 
 cudaError_t launch_build_level(const BuildArgs& a, cudaStream_t s) {
     // small budgets: fewer threads make each of the level's barriers cheaper
-    if (a.N <= 128)
+    if (a.N <= 64)
         return launch_pdl(build_level_kernel<128>, dim3(a.B), dim3(128), 0, s, a.topk_logp,
                           a.topk_idx, a.bonus, a.prefix_len, a.L, a.K, a.N, a.parent, a.depth,
                           a.rank, a.token, a.pos_id, a.score, a.child_count, a.anc_mask,
