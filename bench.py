@@ -480,41 +480,86 @@ def gpu_arm(args, rank, world, dev):
 
         pin = {k: host_t(h[k]) for k in ("draft", "target", "q", "k_tree", "v_tree", "bonus",
                                          "prefix_len")}
-        dst = copies[0]
-        out_pin = {k: torch.empty(rounds[0].acc[k].shape, dtype=torch.int32).pin_memory()
-                   for k in ("accept_len", "out_tokens", "next_bonus")}
+        # two input sets: step s+1's inputs are copied on a second stream while
+        # step s computes; the host reads every step's outputs, and reuses a
+        # pinned output buffer only after it has read the previous step's
+        sets = [copies[0], copies[1]]
+        out_pin = [{k: torch.empty(rounds[0].acc[k].shape, dtype=torch.int32).pin_memory()
+                    for k in ("accept_len", "out_tokens", "next_bonus")} for _ in range(2)]
+        cps = torch.cuda.Stream(device=dev)
+        comp_cap = torch.cuda.Stream(device=dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+        used = [False, False]
+        got = []
 
         def h2d(dst_t, src):
             d = dst_t.view(torch.int16) if dst_t.dtype == torch.bfloat16 else dst_t
             d.copy_(src.view(d.shape), non_blocking=True)
 
         h2d_bytes = sum(t.numel() * t.element_size() for t in pin.values())
-        d2h_bytes = sum(t.numel() * t.element_size() for t in out_pin.values())
+        d2h_bytes = sum(t.numel() * t.element_size() for t in out_pin[0].values())
 
-        def e2e_step():
-            for k in ("draft", "target", "bonus", "prefix_len"):
-                h2d(dst[k], pin[k])
-            for k in ("q", "k_tree", "v_tree"):
-                h2d(dst[k][0], pin[k])
-            rounds[0].run()
-            for k, t in out_pin.items():
-                t.copy_(rounds[0].acc[k], non_blocking=True)
-            torch.cuda.current_stream().synchronize()
+        # every step's work captured once per input set: the copies in (on the
+        # copy stream) and the round with its outputs copied out (on the compute
+        # stream), so that a step costs the host a few calls
+        g_copy, g_round = [], []
+        for i in range(2):
+            gc = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gc, stream=cps):
+                for k in ("draft", "target", "bonus", "prefix_len"):
+                    h2d(sets[i][k], pin[k])
+                for k in ("q", "k_tree", "v_tree"):
+                    h2d(sets[i][k][0], pin[k])
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=comp_cap):
+                rounds[i].run()
+                for k, t in out_pin[i].items():
+                    t.copy_(rounds[i].acc[k], non_blocking=True)
+            g_copy.append(gc)
+            g_round.append(gr)
+        torch.cuda.synchronize()
 
-        for _ in range(max(3, args.warmup // 4)):
-            e2e_step()
+        def e2e_step(step):
+            i = step & 1
+            if used[i]:
+                ev_out[i].synchronize()  # this set's previous outputs are on the host
+                got.append(int(out_pin[i]["accept_len"][0]))
+                cps.wait_event(ev_out[i])  # ... and the round that read its inputs is done
+            with torch.cuda.stream(cps):
+                g_copy[i].replay()
+                ev_in[i].record(cps)
+            with torch.cuda.stream(comp_cap):
+                comp_cap.wait_event(ev_in[i])
+                g_round[i].replay()
+                ev_out[i].record(comp_cap)
+            used[i] = True
+
+        def drain():
+            for i in range(2):
+                if used[i]:
+                    ev_out[i].synchronize()
+                    got.append(int(out_pin[i]["accept_len"][0]))
+                    used[i] = False
+
+        for st in range(max(4, args.warmup // 4)):
+            e2e_step(st)
+        drain()
         n_e2e = max(20, min(500, args.steps // 4))
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for _ in range(n_e2e):
-            e2e_step()
+        for st in range(n_e2e):
+            e2e_step(st)
+        drain()
         t1 = time.perf_counter()
+        assert len(set(got)) == 1, "every step reads the same inputs, so the same result"
         e2e = {"value": w.B * n_e2e / (t1 - t0), "unit": "rounds/s",
                "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes),
                "steps": n_e2e,
-               "note": "public Python API (ops.*) over the C ABI; pinned host inputs copied "
-                       "in and accept outputs copied out every step; the KV cache is "
-                       "device-resident state"}
+               "note": "public Python API (ops.*) over the C ABI; every step copies its inputs "
+                       "in from pinned host memory (on a second stream, overlapping the "
+                       "previous step's round) and its accept outputs out, which the host "
+                       "reads; the KV cache is device-resident state"}
 
     ops.ddtree_device_check()
     tree_anc = int(np.sum([bin(int(x)).count("1") for x in
