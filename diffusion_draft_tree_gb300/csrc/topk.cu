@@ -313,6 +313,16 @@ topk_merge_kernel(const ChunkOut* __restrict__ outs, int nchunks, int K,
     if (tid < K) s_sel[tid] = 0ull;
     pdl_wait();
     const ChunkOut* ro = outs + (size_t)row * nchunks;
+    // the first batch of key slots is loaded with the chunk headers (one round
+    // trip); slots past a chunk's count are dropped once the counts are known
+    const int nslots = nchunks * kChunkCand;
+    uint64_t kv0[kMergeLoads];
+#pragma unroll
+    for (int u = 0; u < kMergeLoads; ++u) {
+        const int i = u * kMergeThreads + tid;
+        kv0[u] = i < nslots ? __ldcg((const unsigned long long*)&ro[i / kChunkCand].keys[i % kChunkCand])
+                            : 0ull;
+    }
     uint32_t tau2 = 0u;
     float mt = -INFINITY, st = 0.f;
     for (int c = tid; c < nchunks; c += kMergeThreads) {
@@ -342,15 +352,15 @@ topk_merge_kernel(const ChunkOut* __restrict__ outs, int nchunks, int K,
     }
     pdl_trigger();
     // gather the kept keys >= tau2 (slot k of chunk c is index c * kChunkCand + k)
-    const int nslots = nchunks * kChunkCand;
     for (int b0 = 0; b0 < nslots; b0 += kMergeLoads * kMergeThreads) {
         uint64_t kv[kMergeLoads];
 #pragma unroll
         for (int u = 0; u < kMergeLoads; ++u) {
             const int i = b0 + u * kMergeThreads + tid;
             const int c = i / kChunkCand, k = i - c * kChunkCand;
-            kv[u] = (i < nslots && k < s_n[c])
-                        ? __ldcg((const unsigned long long*)&ro[c].keys[k]) : 0ull;
+            if (b0 == 0) kv[u] = (i < nslots && k < s_n[c]) ? kv0[u] : 0ull;
+            else kv[u] = (i < nslots && k < s_n[c])
+                             ? __ldcg((const unsigned long long*)&ro[c].keys[k]) : 0ull;
         }
 #pragma unroll
         for (int u = 0; u < kMergeLoads; ++u) {
