@@ -198,6 +198,7 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
     __shared__ float s_pscore[DDTREE_MAX_N];   // ... and their scores
     __shared__ int16_t s_map[DDTREE_MAX_N];
     __shared__ float s_lp[DDTREE_MAX_L * DDTREE_MAX_K];
+    __shared__ int32_t s_idx[DDTREE_MAX_L * DDTREE_MAX_K];  // tokens, staged with s_lp
     __shared__ int s_flag;
     __shared__ int s_warp[kThreads / 32];
     constexpr int kPosPerThread = DDTREE_MAX_N / kThreads;
@@ -209,7 +210,11 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
     const int b = blockIdx.x, tid = threadIdx.x;
     const int LK = L * K;
     pdl_wait();
-    for (int i = tid; i < LK; i += kThreads) s_lp[i] = topk_logp[(size_t)b * LK + i];
+    for (int i = tid; i < LK; i += kThreads) {
+        s_lp[i] = topk_logp[(size_t)b * LK + i];
+        s_idx[i] = topk_idx[(size_t)b * LK + i];
+    }
+    const int P = prefix_len[b], bon = bonus[b];  // (read now: used by the outputs)
     if (tid < 2) {
         s_np[tid] = s_nc[tid] = 0;
         s_fp[tid] = 0x7fffffff;
@@ -414,11 +419,10 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
     for (int u = 1 + tid; u <= n; u += kThreads) atomicAdd(&s_cc[s_par[u]], 1);
     __syncthreads();
     const int R = N + 1, W = (N + 1 + 31) / 32;
-    const int P = prefix_len[b];
     for (int u = tid; u < R; u += kThreads) {
         const size_t o = (size_t)b * R + u;
         if (u == 0) {
-            parent[o] = -1; depth[o] = 0; rank[o] = -1; token[o] = bonus[b]; pos_id[o] = P;
+            parent[o] = -1; depth[o] = 0; rank[o] = -1; token[o] = bon; pos_id[o] = P;
             score[o] = 0.f; child_count[o] = s_cc[0];
         } else if (u <= n) {
             const uint64_t k = s_T[cur][u - 1];
@@ -426,7 +430,7 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
             parent[o] = s_par[u];
             depth[o] = dp;
             rank[o] = rk;
-            token[o] = topk_idx[(size_t)b * LK + (dp - 1) * K + rk];
+            token[o] = s_idx[(dp - 1) * K + rk];
             pos_id[o] = P + dp;
             score[o] = lk_score(k);
             child_count[o] = s_cc[u];
