@@ -138,6 +138,11 @@ accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nc
     }
 
     __shared__ int s_tok[DDTREE_MAX_N + 1];
+    // the walk's tree lives in the chunk buffer, free once the chunk is reduced
+    int* s_par = reinterpret_cast<int*>(s_buf);
+    int* s_tk = s_par + (DDTREE_MAX_N + 1);
+    int* s_chosen = s_tk + (DDTREE_MAX_N + 1);
+    static_assert(3 * (DDTREE_MAX_N + 1) * 4 <= Chunk::BYTES, "walk arrays fit the chunk buffer");
     pdl_trigger();
     if (!sample) {
         // greedy: one 64-bit atomicMax per CTA resolves the row; the last CTA of
@@ -151,6 +156,9 @@ accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nc
         for (int i = tid; i <= n; i += kThreads) {
             unsigned long long* rb = &ws.row_best[(size_t)b * R + i];
             const unsigned long long k = __ldcg(rb);
+            s_par[i] = parent[(size_t)b * R + i];  // the tree, in the same round trip
+            s_tk[i] = token[(size_t)b * R + i];
+            s_chosen[i] = -1;
             s_tok[i] = (int)key_index(k);
             *rb = 0ull;  // ready for the next call
             if (target_token) target_token[(size_t)b * R + i] = (int)key_index(k);
@@ -252,24 +260,24 @@ accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nc
     }
     __syncthreads();
     if (!s_flag) return;
-    for (int i = tid; i <= n; i += kThreads) s_tok[i] = __ldcg(&ws.tok[(size_t)b * R + i]);
+    for (int i = tid; i <= n; i += kThreads) {
+        s_tok[i] = __ldcg(&ws.tok[(size_t)b * R + i]);
+        s_par[i] = parent[(size_t)b * R + i];  // the tree, in the same round trip
+        s_tk[i] = token[(size_t)b * R + i];
+        s_chosen[i] = -1;
+    }
     __syncthreads();
     }  // sampling
 
     // ---- last row of the sequence: the walk ---------------------------------------
     // chosen[p] = the child c of p whose token equals the target's token at p.
-    __shared__ int s_chosen[DDTREE_MAX_N + 1];
-    for (int i = tid; i <= n; i += kThreads) s_chosen[i] = -1;
-    __syncthreads();
-    const int32_t* par = parent + (size_t)b * R;
-    const int32_t* tk = token + (size_t)b * R;
     for (int c = 1 + tid; c <= n; c += kThreads) {
-        const int p = par[c];
+        const int p = s_par[c];
         if (p < 0 || p >= c) {
             record_error(err, ERR_ACCEPT | ERR_BAD_TREE);
             continue;
         }
-        if (tk[c] == s_tok[p]) s_chosen[p] = c;  // children have distinct tokens
+        if (s_tk[c] == s_tok[p]) s_chosen[p] = c;  // children have distinct tokens
     }
     __syncthreads();
     if (tid == 0) {
@@ -279,7 +287,7 @@ accept_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int nc
         while (len < L && s_chosen[cur] >= 0) {
             cur = s_chosen[cur];
             acc[len] = cur;
-            ot[len] = tk[cur];
+            ot[len] = s_tk[cur];
             ++len;
         }
         for (int i = len; i < L; ++i) acc[i] = -1;
