@@ -214,8 +214,12 @@ ddtree_status ddtree_accept(const void* target_logits, int dtype, int64_t row_st
  * nodes; -1 elsewhere) and no workspace is needed.  The pages' walk needs the
  * target's token only on that path (§4.1), so HBM traffic is
  * (accept_len + 1) x V x elem per sequence instead of (n + 1) x V x elem; the
- * rows are resolved one after another, so it pays when N >> accept_len.  One
- * CTA per sequence. */
+ * rows are resolved one after another, so it pays when N >> accept_len.  Each
+ * sequence runs on a thread-block cluster of up to 16 CTAs that split every
+ * row (V <= 128 x 32 KB of logits per row).  A greedy result is identical to
+ * ddtree_accept's; a sampled token can differ from it only when U·Z lies
+ * within the fp32 rounding of a CDF boundary (the chunk sums are combined in
+ * fp32 here, in fp64 there). */
 ddtree_status ddtree_accept_path(const void* target_logits, int dtype, int64_t row_stride,
                                  const int32_t* parent, const int32_t* token,
                                  const int32_t* n_nodes, int B, int L, int N, int V,
