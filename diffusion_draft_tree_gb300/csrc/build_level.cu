@@ -199,7 +199,7 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
     __shared__ int16_t s_map[DDTREE_MAX_N];
     __shared__ float s_lp[DDTREE_MAX_L * DDTREE_MAX_K];
     __shared__ int32_t s_idx[DDTREE_MAX_L * DDTREE_MAX_K];  // tokens, staged with s_lp
-    __shared__ int s_flag;
+    __shared__ int s_flag[2];  // a node of depth d is in T, by level parity
     __shared__ int s_warp[kThreads / 32];
     constexpr int kPosPerThread = DDTREE_MAX_N / kThreads;
     // list lengths, double-buffered so that a counter is reset while its
@@ -217,6 +217,7 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
     const int P = prefix_len[b], bon = bonus[b];  // (read now: used by the outputs)
     if (tid < 2) {
         s_np[tid] = s_nc[tid] = 0;
+        s_flag[tid] = 0;
         s_fp[tid] = 0x7fffffff;
     }
     __syncthreads();
@@ -290,6 +291,7 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
         for (int i = tid; i < t; i += kThreads) s_orig[cur][i] = (int16_t)i;
 
         // ---- children in batches of kCandCap (parent, rank) pairs --------------------
+        bool merged = false;
         const int pairs = npar * K;
         const float* lp = s_lp + (d - 1) * K;
         for (int base = 0; base < pairs; base += kCandCap) {
@@ -371,8 +373,10 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
                     const uint64_t a = s_T[cur][i];
                     const int rk = i + count_greater(sorted, c, a);
                     if (rk < N) {
+                        const int o = s_orig[cur][i];
                         s_T[nxt][rk] = a;
-                        s_orig[nxt][rk] = s_orig[cur][i];
+                        s_orig[nxt][rk] = (int16_t)o;
+                        if (o >= 0) s_map[o] = (int16_t)rk;  // the last merge's position wins
                     }
                 } else {
                     const int j = i - t;
@@ -386,24 +390,23 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
             }
             t = min(N, t + c);
             cur = nxt;
+            merged = true;
             __syncthreads();
         }
 
-        // ---- level end: parent positions T_{d-1} -> T_d; stop when nothing is deep --
-        if (tid == 0) s_flag = 0;
-        for (int i = tid; i < t; i += kThreads) {
-            const int o = s_orig[cur][i];
-            if (o >= 0) s_map[o] = (int16_t)i;
-        }
-        __syncthreads();
+        // ---- level end: parent positions T_{d-1} -> T_d (s_map was written by the
+        // merges: a node of T_{d-1} that survives was moved by every merge, and a
+        // dropped one has no descendant in T); stop when nothing reached depth d --
+        if (!merged) break;  // no child entered: T is complete
         for (int i = tid; i < t; i += kThreads) {
             const uint64_t k = s_T[cur][i];
             const int pp = lk_ppos(k);
             if (pp >= 0) s_T[cur][i] = lk_with_ppos(k, s_map[pp]);
-            if (lk_depth(k) == d) s_flag = 1;
+            if (lk_depth(k) == d) s_flag[d & 1] = 1;
         }
+        if (tid == 0) s_flag[(d + 1) & 1] = 0;  // read last a level ago
         __syncthreads();
-        if (!s_flag) break;
+        if (!s_flag[d & 1]) break;
     }
 
     pdl_trigger();
