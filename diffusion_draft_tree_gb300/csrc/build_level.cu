@@ -331,7 +331,7 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
             // 512-thread variant; in shared memory for the 128-thread one).
             const uint64_t* sorted = s_cand;
             if (c <= kRankCountMax) {
-                __syncthreads();  // the batch's keys are in place
+                // (the batch's keys are in place: the count was read after a barrier)
                 // up to four keys a thread, counted in one pass over the batch
                 if (c <= kThreads) rank_scatter<1, kThreads>(s_cand, c);
                 else if (c <= 2 * kThreads) rank_scatter<2, kThreads>(s_cand, c);
