@@ -45,6 +45,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-x36", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--walk", default="auto", choices=["auto", "full", "path"],
+                    help="step 4: the full-tree walk (ddtree_accept), the path-only walk "
+                         "(ddtree_accept_path), or auto: the path-only walk once the batch "
+                         "has >= 128 tree rows, B (N + 1)")
     ap.add_argument("--acceptance-stats", type=int, default=0, metavar="ROUNDS",
                     help="instead of timing: run ROUNDS independent synthetic rounds per node "
                          "budget (and the K = 1 chain) and report acceptance lengths")
@@ -202,6 +206,7 @@ class Round:
         self.out = [torch.empty_like(inputs["q"][0]) for _ in range(layers)]
         self.acc = ops.accept_buffers(B, L, N, dev)
         self.ws = ws
+        self.walk = walk_for(w)
 
     def run(self, layers=1):
         ops, w, x = self.ops, self.w, self.inp
@@ -213,9 +218,17 @@ class Round:
                                  x["v_tree"][l], x["prefix_len"], self.tree["n_nodes"],
                                  self.tree["anc_mask"], self.out[l], None, None,
                                  self.ws["attn"])
-        ops.ddtree_accept(x["target"], self.tree["parent"], self.tree["token"],
-                          self.tree["n_nodes"], w.L, self.acc, w.T, wl.philox_seed(w), 0,
-                          self.ws["accept"])
+        self.accept()
+
+    def accept(self):
+        ops, w, x = self.ops, self.w, self.inp
+        if self.walk == "path":
+            ops.ddtree_accept_path(x["target"], self.tree["parent"], self.tree["token"],
+                                   self.tree["n_nodes"], w.L, self.acc, w.T, wl.philox_seed(w), 0)
+        else:
+            ops.ddtree_accept(x["target"], self.tree["parent"], self.tree["token"],
+                              self.tree["n_nodes"], w.L, self.acc, w.T, wl.philox_seed(w), 0,
+                              self.ws["accept"])
 
     def stages(self):
         """The four calls as separate closures (for per-kernel event timing)."""
@@ -230,9 +243,7 @@ class Round:
                                          x["k_tree"][0], x["v_tree"][0], x["prefix_len"],
                                          self.tree["n_nodes"], self.tree["anc_mask"],
                                          self.out[0], None, None, self.ws["attn"]),
-            lambda: ops.ddtree_accept(x["target"], self.tree["parent"], self.tree["token"],
-                                      self.tree["n_nodes"], w.L, self.acc, w.T,
-                                      wl.philox_seed(w), 0, self.ws["accept"]),
+            self.accept,
         ]
 
 
@@ -406,39 +417,55 @@ def gpu_arm(args, rank, world, dev):
 
     # the path-only walk on the same round's tree and target rows (an alternative
     # to the full-tree accept; timed alone, not in the round's metric)
-    accept_path = None
+    # both step-4 walks timed alone on the same round's tree and target rows
+    # (whichever the round uses), and their emitted tokens compared
+    walks = {}
     try:
         r0 = rounds[0]
-        acc2 = ops.accept_buffers(w.B, w.L, w.N, dev)
-        n_p = 20
-        p_ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
-                for _ in range(n_p)]
+        outs = {"path": ops.accept_buffers(w.B, w.L, w.N, dev),
+                "full": ops.accept_buffers(w.B, w.L, w.N, dev)}
 
-        def path_once(ev):
-            ev[0].record()
-            ops.ddtree_accept_path(r0.inp["target"], r0.tree["parent"], r0.tree["token"],
-                                   r0.tree["n_nodes"], w.L, acc2, w.T, wl.philox_seed(w), 0)
-            ev[1].record()
+        def run_walk(kind):
+            if kind == "path":
+                ops.ddtree_accept_path(r0.inp["target"], r0.tree["parent"], r0.tree["token"],
+                                       r0.tree["n_nodes"], w.L, outs[kind], w.T,
+                                       wl.philox_seed(w), 0)
+            else:
+                ops.ddtree_accept(r0.inp["target"], r0.tree["parent"], r0.tree["token"],
+                                  r0.tree["n_nodes"], w.L, outs[kind], w.T, wl.philox_seed(w), 0,
+                                  ws["accept"])
 
-        path_once(p_ev[0])
-        torch.cuda.synchronize()
-        g_p = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_p, stream=stream):
-            for ev in p_ev:
-                path_once(ev)
-        t_p = 0.0
-        for _ in range(5):
-            g_p.replay()
+        for kind in ("path", "full"):
+            n_p = 20
+            p_ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+                    for _ in range(n_p)]
+
+            def once(ev):
+                ev[0].record()
+                run_walk(kind)
+                ev[1].record()
+
+            once(p_ev[0])
             torch.cuda.synchronize()
-            t_p += sum(ev[0].elapsed_time(ev[1]) for ev in p_ev)
-        ops.ddtree_device_check()
-        same = bool(torch.equal(acc2["out_tokens"], r0.acc["out_tokens"]))
-        rows = int(acc2["accept_len"].sum().item()) + w.B
-        accept_path = {"ms": t_p / (5 * n_p), "bytes": rows * w.V * w.esize,
-                       "same_tokens_as_full_walk": same}
-        del acc2
+            g_p = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_p, stream=stream):
+                for ev in p_ev:
+                    once(ev)
+            t_p = 0.0
+            for _ in range(5):
+                g_p.replay()
+                torch.cuda.synchronize()
+                t_p += sum(ev[0].elapsed_time(ev[1]) for ev in p_ev)
+            ops.ddtree_device_check()
+            walks[kind] = {"ms": t_p / (5 * n_p)}
+        same = bool(torch.equal(outs["path"]["out_tokens"], outs["full"]["out_tokens"]))
+        rows = int(outs["path"]["accept_len"].sum().item()) + w.B
+        walks["path"]["bytes"] = rows * w.V * w.esize
+        walks["full"]["bytes"] = w.B * (w.N + 1) * w.V * w.esize
+        walks["same_tokens"] = same
+        del outs
     except Exception as e:  # noqa: BLE001
-        accept_path = {"unavailable": repr(e)}
+        walks = {"unavailable": repr(e)}
 
     # 36-layer round: 36 tree-attention launches, each on its own KV cache
     x36 = None
@@ -566,7 +593,7 @@ def gpu_arm(args, rank, world, dev):
                            rounds[0].tree["anc_mask"].cpu().numpy().view(np.uint32).ravel()]))
     return {"w": w, "ms_total": ms_total, "R": R, "per_copy": per_copy, "clocks": clocks,
             "kern_ms": kern_ms, "kern_method": kern_method, "x36": x36, "e2e": e2e,
-            "commit": commit, "accept_path": accept_path,
+            "commit": commit, "walks": walks,
             "tree_anc": tree_anc}
 
 
@@ -659,7 +686,7 @@ def aggregate_replicas(ms_local: float, world: int, B: int, steps: int, device):
 def config_of(w, R):
     c = {"workload": w.name, "B": w.B, "L": w.L, "V": w.V, "K": w.K, "N": w.N,
          "P": list(w.P) if len(set(w.P)) > 1 else w.P[0], "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
-         "temperature": w.T, "layers": 1}
+         "temperature": w.T, "layers": 1, "walk": walk_for(w)}
     if R is not None:
         c["l2"] = f"inputs rotated over {R} copies per step (> 2x the 129 MB L2)"
     return c
@@ -717,8 +744,24 @@ def acceptance_stats(rounds: int) -> dict:
     return out
 
 
+WALK = "auto"  # step 4 of the timed round (--walk)
+
+
+def walk_for(w) -> str:
+    """The walk the round uses: measured on the five workloads, the path-only
+    walk (a dependent chain of rows) is faster once the batch's trees hold
+    128 rows or more (N = 128: 73 -> 66 us a round, ragged_serving 976 -> 736
+    us), the full-tree walk (every row at once) below (8b_single: 40.1 vs
+    40.5 us)."""
+    if WALK != "auto":
+        return WALK
+    return "path" if w.B * (w.N + 1) >= 128 else "full"
+
+
 def main():
+    global WALK
     args = parse()
+    WALK = args.walk
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
     if world > 1 and "RANK" not in os.environ:
@@ -749,6 +792,9 @@ def main():
     ms_step = ms_total / args.steps
     peaks = load_peaks()
     model = work_model(w, res["tree_anc"])
+    wk = res.get("walks") or {}
+    if walk_for(w) == "path" and "path" in wk:  # the round's step 4 reads the path's rows only
+        model["accept"] = {"bytes": wk["path"]["bytes"]}
     names = ["topk", "build", "tree_attn", "accept"]
     kernels = {}
     for n, ms in zip(names, res["kern_ms"]):
@@ -766,14 +812,18 @@ def main():
                              "hbm_frac": c["bytes"] / (c["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
                              "note": "after the round, not in its metric: the accepted "
                                      "path's K/V rows into the cache"}
-    c = res.get("accept_path")
-    if c and "ms" in c:
-        kernels["accept_path"] = {
-            "ms": c["ms"], "GBps": c["bytes"] / (c["ms"] * 1e-3) / 1e9,
-            "hbm_frac": c["bytes"] / (c["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
-            "same_tokens_as_full_walk": c["same_tokens_as_full_walk"],
-            "note": "alternative step 4 reading only the accepted path's rows "
-                    "(bytes = (accept_len + 1) x V x elem per sequence); timed alone"}
+    wk = res.get("walks") or {}
+    for kind in ("path", "full"):
+        c = wk.get(kind)
+        if c and "ms" in c:
+            kernels["accept_" + kind] = {
+                "ms": c["ms"], "GBps": c["bytes"] / (c["ms"] * 1e-3) / 1e9,
+                "hbm_frac": c["bytes"] / (c["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                "same_tokens_as_other_walk": wk.get("same_tokens"),
+                "note": ("step 4 reading only the accepted path's rows (bytes = (accept_len + 1)"
+                         " x V x elem per sequence)" if kind == "path" else
+                         "step 4 resolving every tree row (bytes = (N + 1) x V x elem per "
+                         "sequence)") + "; timed alone, outside the round"}
     a = model["tree_attn"]
     t_hbm = a["bytes"] / (peaks["hbm_gbs"] * 1e9)
     t_tc = a["flops"] / (peaks["bf16_tflops"] * 1e12)
