@@ -195,3 +195,24 @@ def test_accept_budget_1024(cuda_device, T):
     check_full(x, wl.FP32, t, L, T, 77, 5, cuda_device)
     if T == 0.0:
         assert ref["accept_len"].min() >= 2  # the planted rank-0 chain is walked
+
+
+@pytest.mark.parametrize("B,V,dtype,T", [
+    (2, 151936, wl.FP32, 1.0),   # 19 chunks over a cluster of 10: two chunks on most CTAs
+    (320, 40000, wl.FP32, 0.0),  # more sequences than CTA slots: one CTA each, 5 chunks in turn
+    (320, 40000, wl.BF16, 1.0)])
+def test_accept_path_cluster_shapes(cuda_device, B, V, dtype, T):
+    rng = np.random.default_rng(B * 7 + V + int(T))
+    L, K, N = 4, 3, 6
+    lp = -np.sort(rng.exponential(1.0, size=(B, L, K)).astype(np.float32), axis=2)
+    lp = -np.sort(-lp, axis=2)
+    tok = np.stack([[rng.permutation(V)[:K] for _ in range(L)] for _ in range(B)]).astype(np.int32)
+    t = oracle.build_tree(lp, tok, rng.integers(0, V, size=B).astype(np.int32),
+                          np.zeros(B, np.int32), N)
+    x = (rng.standard_normal((B, N + 1, V)) * 2).astype(np.float32)
+    for b in range(B):
+        for c in range(1, t["n_nodes"][b] + 1):
+            if rng.random() < 0.6:
+                x[b, t["parent"][b, c], t["token"][b, c]] += 12
+    raw = wl.bf16_bits(x) if dtype == wl.BF16 else x
+    _check(raw, dtype, t, L, T, 99, 1, cuda_device)
