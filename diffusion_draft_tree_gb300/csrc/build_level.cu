@@ -13,9 +13,10 @@
 //
 // T_d is the top N among all prefixes of depth <= d (a depth-d prefix in it
 // has its parent in it, and that parent is among the top N of depth <= d-1).
-// When T is full, a child must beat its last key.  The qualifying children
-// are gathered (in any order), sorted (rank counting for small batches,
-// bitonic otherwise, in shared memory) and merged into T with a
+// When T is full, a child must beat its last key, and once the strongest
+// parent's best child cannot, no deeper node can enter and the build stops.
+// The qualifying children are gathered (in any order), sorted (rank counting
+// up to 512 keys, a bitonic network above) and merged into T with a
 // rank-by-binary-search merge.  The result -- nodes, their order, fp32 scores
 // formed as parent score + log-prob -- is identical to the heap's.
 //
@@ -23,8 +24,9 @@
 //   [63:32] orderable fp32 score, [31:27] 31 - depth,
 //   [26:16] 2046 - parent position (2047 for the root), [15:10] 63 - rank.
 // Parent positions refer to T_{d-1} while level d is built and are remapped to
-// the new positions when the level ends (the relative order of survivors, and
-// so every comparison, is unchanged by the remap).
+// the new positions when the level ends, through a map that the merges fill in
+// (the relative order of survivors, and so every comparison, is unchanged by
+// the remap).
 #include "common.cuh"
 #include "internal.h"
 
