@@ -225,17 +225,18 @@ build_level_kernel(const float* __restrict__ topk_logp, const int32_t* __restric
     __syncthreads();
 
     int t = 0, cur = 0, nb = 0;
-    for (int d = 1; d <= L && N > 0; ++d) {
+    // ---- level 1: the root's children (the empty prefix has score 0), which the
+    // sorted log-probs already put in priority order (equal log-probs: lower
+    // rank first, as in the key) ----
+    if (N > 0) {
+        t = min(N, K);
+        for (int i = tid; i < t; i += kThreads) s_T[cur][i] = lkey(__fadd_rn(0.f, s_lp[i]), 1, -1, i);
+        __syncthreads();
+    }
+    for (int d = 2; d <= L && t > 0; ++d) {
         // ---- parents: the depth-(d-1) nodes of T -----------------------------------
         int npar, first = 0;
-        if (d == 1) {
-            npar = 1;
-            if (tid == 0) {
-                s_plist[0] = -1;
-                s_pscore[0] = 0.f;  // the root: the empty prefix, probability 1
-            }
-            __syncthreads();
-        } else if (t * K > kCandCap) {
+        if (t * K > kCandCap) {
             // children in several batches: parents in T order, so that the first
             // batches hold the strongest children and T's last key rises early
             if (tid == 0) s_np[(d + 1) & 1] = 0;
