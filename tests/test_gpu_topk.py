@@ -1,6 +1,9 @@
 """GPU parity of step 1 (log-softmax + top-K) against the oracle.
 Criteria: indices bit-exact; log-probs and logsumexp within 1e-5 absolute of
-the oracle's fp64 values."""
+the oracle's fp64 values.  Both chunk sizes are covered: 16 KB chunks when
+every chunk of every row fits one wave of CTAs, 32 KB otherwise; the edge
+shapes run once as they are (six rows: 16 KB) and once with their rows
+repeated 64 times (32 KB)."""
 import numpy as np
 import pytest
 import torch
@@ -43,7 +46,10 @@ def test_topk_workloads(cuda_device, name):
     (16384, 32, wl.BF16, False), (16385, 1, wl.BF16, True), (40000, 8, wl.FP32, False),
     (40001, 8, wl.FP32, True), (50, 32, wl.BF16, False), (7, 1, wl.FP32, False),
     (151936, 2, wl.BF16, False), (300000, 16, wl.BF16, False)])
-def test_topk_edge_shapes_and_ties(cuda_device, V, K, dtype, unaligned):
+@pytest.mark.parametrize("reps", [1, 64])
+def test_topk_edge_shapes_and_ties(cuda_device, V, K, dtype, unaligned, reps):
+    if reps > 1 and V > 100000:
+        pytest.skip("the long-row workloads above already take 32 KB chunks")
     rng = np.random.default_rng(V + K)
     x = (rng.standard_normal((6, V)) * 3).astype(np.float32)
     x[1, :] = 0.0                                     # a constant row: ties everywhere
@@ -52,6 +58,7 @@ def test_topk_edge_shapes_and_ties(cuda_device, V, K, dtype, unaligned):
     x[3, ::2] = np.float32(-0.0)                      # signed zeros tie by index
     x[3, 1::2] = np.float32(0.0)
     x[4, :] = np.round(x[4] * 2) / 2                  # heavy quantisation: many ties
+    x = np.tile(x, (reps, 1))
     raw = wl.bf16_bits(x) if dtype == wl.BF16 else x
     _check(raw, dtype, K, cuda_device, unaligned)
 
