@@ -1,6 +1,7 @@
 // api.cu -- the C ABI (include/ddtree.h): host-side validation, the per-device
 // error word, and dispatch to the kernel launchers.  No allocation, no
 // synchronisation except in ddtree_device_check().
+#include <initializer_list>
 #include <mutex>
 
 #include "internal.h"
@@ -34,6 +35,13 @@ uint32_t* error_word() {
 }
 
 inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+// Every pointer of 4-byte elements (int32, uint32, float) on its grid; null
+// entries (optional outputs) pass.
+inline bool aligned4(std::initializer_list<const void*> ps) {
+    for (const void* p : ps)
+        if (p && !aligned(p, 4)) return false;
+    return true;
+}
 
 thread_local const char* t_last_cuda_error = "no error";
 
@@ -86,6 +94,7 @@ ddtree_status ddtree_topk(const void* draft_logits, int dtype, int rows, int V,
         return DDTREE_ERR_INVALID_ARG;
     if (K > DDTREE_MAX_K || !ddt::topk_supported(V, dtype, K)) return DDTREE_ERR_UNSUPPORTED;
     if (!aligned(draft_logits, dtype == DDTREE_BF16 ? 2 : 4)) return DDTREE_ERR_INVALID_ARG;
+    if (!aligned4({topk_idx, topk_logp, lse})) return DDTREE_ERR_INVALID_ARG;
     const size_t need = ddt::topk_workspace_bytes(rows, V, dtype, K);
     if (need && (!workspace || ws_bytes < need || !aligned(workspace, 256)))
         return DDTREE_ERR_INVALID_ARG;
@@ -104,6 +113,9 @@ ddtree_status build_common(bool heap, const float* topk_logp, const int32_t* top
         !token || !pos_id || !score || !child_count || !anc_mask || !n_nodes)
         return DDTREE_ERR_INVALID_ARG;
     if (B <= 0 || B > 65535 || L <= 0 || K <= 0 || N < 0) return DDTREE_ERR_INVALID_ARG;
+    if (!aligned4({topk_logp, topk_idx, bonus, prefix_len, parent, depth, rank, token, pos_id,
+                   score, child_count, anc_mask, n_nodes}))
+        return DDTREE_ERR_INVALID_ARG;
     if (L > DDTREE_MAX_L || K > DDTREE_MAX_K || N > DDTREE_MAX_N) return DDTREE_ERR_UNSUPPORTED;
     ddt::BuildArgs a{topk_logp, topk_idx, bonus, prefix_len, B, L, K, N, parent, depth, rank,
                      token, pos_id, score, child_count, anc_mask, n_nodes, error_word()};
@@ -147,7 +159,7 @@ ddtree_status ddtree_tree_attn(const void* q, const void* k_cache, const void* v
         return DDTREE_ERR_UNSUPPORTED;
     for (const void* p : {q, k_cache, v_cache, k_tree, v_tree, (const void*)out})
         if (!aligned(p, 16)) return DDTREE_ERR_INVALID_ARG;
-    if (lse && !aligned(lse, 4)) return DDTREE_ERR_INVALID_ARG;
+    if (!aligned4({prefix_len, n_nodes, anc_mask, lse})) return DDTREE_ERR_INVALID_ARG;
     const size_t need = ddt::attn_workspace_bytes(B, N, Hq, Hkv, D, cache_cap);
     if (need && (!workspace || ws_bytes < need || !aligned(workspace, 256)))
         return DDTREE_ERR_INVALID_ARG;
@@ -172,6 +184,9 @@ ddtree_status ddtree_accept(const void* target_logits, int dtype, int64_t row_st
     if (N > DDTREE_MAX_N || L > DDTREE_MAX_L || !ddt::accept_supported(V, dtype))
         return DDTREE_ERR_UNSUPPORTED;
     if (!aligned(target_logits, dtype == DDTREE_BF16 ? 2 : 4)) return DDTREE_ERR_INVALID_ARG;
+    if (!aligned4({parent, token, n_nodes, target_token, accept_len, accepted_nodes, out_tokens,
+                   next_bonus}))
+        return DDTREE_ERR_INVALID_ARG;
     const size_t need = ddt::accept_workspace_bytes(B, N, V, dtype);
     if (!workspace || ws_bytes < need || !aligned(workspace, 256)) return DDTREE_ERR_INVALID_ARG;
     ddt::AcceptArgs a{target_logits, dtype, row_stride, parent, token, n_nodes, B, L, N, V,
@@ -197,6 +212,9 @@ ddtree_status ddtree_accept_path(const void* target_logits, int dtype, int64_t r
     if (N > DDTREE_MAX_N || L > DDTREE_MAX_L || !ddt::accept_path_supported(V, dtype))
         return DDTREE_ERR_UNSUPPORTED;
     if (!aligned(target_logits, dtype == DDTREE_BF16 ? 2 : 4)) return DDTREE_ERR_INVALID_ARG;
+    if (!aligned4({parent, token, n_nodes, target_token, accept_len, accepted_nodes, out_tokens,
+                   next_bonus}))
+        return DDTREE_ERR_INVALID_ARG;
     ddt::AcceptArgs a{target_logits, dtype, row_stride, parent, token, n_nodes, B, L, N, V,
                       temperature, seed, step, target_token, accept_len, accepted_nodes,
                       out_tokens, next_bonus, nullptr, error_word()};

@@ -548,6 +548,8 @@ extern "C" ddtree_status ddtree_topk_noalloc(const void* draft_logits, int dtype
         return DDTREE_ERR_INVALID_ARG;
     if (K > DDTREE_MAX_K || !ddt::topk_supported(V, dtype, K)) return DDTREE_ERR_UNSUPPORTED;
     if ((uintptr_t)draft_logits % (dtype == DDTREE_BF16 ? 2 : 4)) return DDTREE_ERR_INVALID_ARG;
+    if ((uintptr_t)topk_idx % 4 || (uintptr_t)topk_logp % 4 || (lse && (uintptr_t)lse % 4))
+        return DDTREE_ERR_INVALID_ARG;
     const size_t need = ddt::topk_workspace_bytes(rows, V, dtype, K);
     if (need > DDTREE_NOALLOC_SCRATCH_BYTES) return DDTREE_ERR_UNSUPPORTED;
     void* scratch = nullptr;

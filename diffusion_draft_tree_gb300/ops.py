@@ -61,13 +61,15 @@ def _load() -> ctypes.CDLL:
     lib.ddtree_commit.argtypes = [P, P, i64, P, P, P, P, P, i32, i32, i32, i32, i32, P]
     lib.ddtree_accept_path.argtypes = [P, i32, i64, P, P, P, i32, i32, i32, i32, f32, u64, u64,
                                        P, P, P, P, P, P]
+    lib.ddtree_topk_noalloc.argtypes = [P, i32, i32, i32, i64, i32, P, P, P, P]
     lib.ddtree_device_check.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
     lib.ddtree_last_cuda_error.argtypes = []
     lib.ddtree_last_cuda_error.restype = ctypes.c_char_p
     lib.ddtree_status_str.argtypes = [i32]
     lib.ddtree_status_str.restype = ctypes.c_char_p
     for f in ("ddtree_topk", "ddtree_build", "ddtree_build_heap", "ddtree_tree_attn",
-              "ddtree_accept", "ddtree_accept_path", "ddtree_commit", "ddtree_device_check"):
+              "ddtree_accept", "ddtree_accept_path", "ddtree_commit", "ddtree_topk_noalloc",
+              "ddtree_device_check"):
         getattr(lib, f).restype = i32
     return lib
 

@@ -19,7 +19,9 @@
  *     [d0][d1]...; "bf16" means IEEE bfloat16 bit patterns.
  *   - Arguments are validated on the host before any launch; a bad argument
  *     returns DDTREE_ERR_INVALID_ARG (or DDTREE_ERR_UNSUPPORTED for a legal but
- *     unimplemented shape) and enqueues nothing.  A launch failure returns
+ *     unimplemented shape) and enqueues nothing.  Every int32 / uint32 / float
+ *     array must be aligned to its element size (4 bytes); bf16 logits to 2
+ *     bytes; the stricter rules of individual calls are stated with them.  A launch failure returns
  *     DDTREE_ERR_CUDA.  Inconsistent device-side data (an index out of range,
  *     a prefix longer than the cache) is skipped by the kernels, never
  *     dereferenced, and recorded in a per-device error word that

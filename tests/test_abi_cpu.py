@@ -96,3 +96,35 @@ def test_invalid_arguments_rejected_before_launch(lib):
                            None) == 2
     assert L.ddtree_commit(P(0x1008), fake, 64, fake, fake, fake, fake, fake, 1, 4, 8, 2, 64,
                            None) == 1
+
+
+def test_misaligned_element_arrays_rejected(lib):
+    """Every int32 / uint32 / float array off its 4-byte grid is refused on the
+    host (a device access through it would fault); the other arguments of each
+    call are well formed, so the misaligned pointer is the only fault."""
+    L = lib.lib
+    P = ctypes.c_void_p
+    ok, odd = P(0x10000), P(0x10002)
+    ws, wsb = P(0x100000), 1 << 24
+    for i in range(3):  # top-K: indices, log-probs, logsumexp
+        outs = [ok, ok, ok]
+        outs[i] = odd
+        assert L.ddtree_topk(ok, 0, 1, 1000, 1000, 4, *outs, ws, wsb, None) == 1
+    for i in range(13):  # the build's inputs and outputs
+        ptrs = [ok] * 13
+        ptrs[i] = odd
+        assert L.ddtree_build(*ptrs[:4], 1, 4, 4, 16, *ptrs[4:], None) == 1
+        assert L.ddtree_build_heap(*ptrs[:4], 1, 4, 4, 16, *ptrs[4:], None) == 1
+    for i in range(4):  # tree attention: prefix lengths, tree sizes, mask, lse
+        p4 = [ok] * 4
+        p4[i] = odd
+        assert L.ddtree_tree_attn(ok, ok, ok, 64, ok, ok, p4[0], p4[1], p4[2], 1, 16, 2, 1, 64,
+                                  0.125, ok, p4[3], ws, wsb, None) == 1
+    for i in range(8):  # both walks: tree arrays and outputs
+        p8 = [ok] * 8
+        p8[i] = odd
+        common = [ok, 0, 1000, p8[0], p8[1], p8[2], 1, 4, 16, 1000, 0.0, 1, 0, *p8[3:]]
+        assert L.ddtree_accept(*common, ws, wsb, None) == 1
+        assert L.ddtree_accept_path(*common, None) == 1
+    # the no-workspace top-K checks the same
+    assert L.ddtree_topk_noalloc(ok, 0, 1, 1000, 1000, 4, odd, ok, None, None) == 1
