@@ -149,11 +149,13 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
                           chunk * Chunk::SIZE, V, aligned);
     };
     for (int j = 0; j < kStages - 1 && j < nmine; ++j) issue(j);
+    uint32_t tau_run = 0u;  // a bound <= the current row's K-th largest (0: none yet)
     for (int j = 0; j < nmine; ++j) {
         if (j + kStages - 1 < nmine) issue(j + kStages - 1);  // into the stage freed last step
         if (j == nmine - 1) pdl_trigger();
         const int w = w0 + j;
         const int c0 = (w % nchunks) * Chunk::SIZE;
+        if (c0 == 0) tau_run = 0u;  // a new row
         ChunkOut* out = outs + w;
         if (tid == 0) s_cnt = 0;
         if (!Chunk::wait_ring(&s_bar[j % kStages], (uint32_t)((j / kStages) & 1))) {
@@ -180,28 +182,6 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
             }
             if (mt != -INFINITY) Chunk::exp_sum(v, kLog2e, -mt * kLog2e, a0, a1);
         }
-        // The warp's K largest vector maxima (K distinct elements), descending,
-        // into s_vm[warp]: the vector maxima at or above the K-th largest lane
-        // maximum (usually K to 3K) sorted by the warp; if there are too many,
-        // K copies of that lane bound (still K elements >= each).
-        {
-            const uint32_t tau_l = warp_kth_largest(e_lane < V ? ord_from_float(mt) : 0u, K);
-            const float tl = (tau_l == 0u) ? -INFINITY : float_from_ord(tau_l);
-            int nm = 0;
-#pragma unroll
-            for (int i = 0; i < PL; ++i) {
-                const bool in = vmx[i] >= tl && e_lane + 32 * i * VEC < V;
-                const unsigned bal = __ballot_sync(0xffffffffu, in);
-                const int at = nm + __popc(bal & ((1u << lane) - 1u));
-                if (in && at < 32) s_vm[warp][at] = ord_from_float(vmx[i]);
-                nm += __popc(bal);
-            }
-            __syncwarp();
-            uint32_t top = tau_l;
-            if (nm <= 32) top = warp_sort_desc_u32(lane < nm ? s_vm[warp][lane] : 0u);
-            __syncwarp();
-            if (lane < K) s_vm[warp][lane] = top;
-        }
         float m_w = mt, s_w = a0 + a1;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -210,75 +190,123 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
             ms_combine(m_w, s_w, mo, so, kLog2e);
         }
         if (lane == 0) s_wms[warp] = make_float2(m_w, s_w);
-        __syncthreads();
-        // tau: the K-th largest of the warps' lists (each warp, redundantly),
-        // a bound on the chunk's K-th largest value
-        uint32_t tau = 0u;
-        {
-            int ptr = 0;
-            uint32_t head = lane < kWarps ? s_vm[lane][0] : 0u;
-            for (int r = 0; r < K; ++r) {
-                tau = __reduce_max_sync(0xffffffffu, head);
-                const unsigned holders = __ballot_sync(0xffffffffu, head == tau);
-                if (lane == __ffs(holders) - 1) {
-                    ++ptr;
-                    head = ptr < K ? s_vm[lane][ptr] : 0u;
-                }
-            }
-        }
-        const float tv = (tau == 0u) ? -INFINITY : float_from_ord(tau);
 
-        // ---- the chunk's keys >= tau, from the vectors whose maximum reaches it:
-        // their ids are compacted per warp first (a ballot per vector row), so
-        // each passing vector is unpacked by one lane instead of the whole warp
-        // stepping through every row in which any lane passes ----
-        int nv = 0;
+        // The chunk's keys >= tv, from the vectors whose maximum reaches it: their
+        // ids are compacted per warp first (a ballot per vector row), so each
+        // passing vector is unpacked by one lane instead of the whole warp
+        // stepping through every row in which any lane passes.  Counts them in
+        // s_cnt; stores the first kChunkCand.
+        auto gather = [&](float tv) {
+            int nv = 0;
 #pragma unroll
-        for (int i = 0; i < PL; ++i) {
-            const unsigned bal = __ballot_sync(0xffffffffu, vmx[i] >= tv);
-            if (vmx[i] >= tv) s_vlist[warp][nv + __popc(bal & ((1u << lane) - 1u))] = (int16_t)(lane + 32 * i);
-            nv += __popc(bal);
-        }
-        __syncwarp();
-        for (int b0 = 0; b0 < nv; b0 += 32) {
-            const int v = b0 + lane < nv ? s_vlist[warp][b0 + lane] : -1;
-            float x[VEC];
-            int mine = 0;
-            const int e = c0 + (warp * VPW + v) * VEC;
-            if (v >= 0) {
-                Chunk::unpack(vw[v], x);
-#pragma unroll
-                for (int k = 0; k < VEC; ++k) mine += (x[k] >= tv && e + k < V) ? 1 : 0;
+            for (int i = 0; i < PL; ++i) {
+                const unsigned bal = __ballot_sync(0xffffffffu, vmx[i] >= tv);
+                if (vmx[i] >= tv) s_vlist[warp][nv + __popc(bal & ((1u << lane) - 1u))] = (int16_t)(lane + 32 * i);
+                nv += __popc(bal);
             }
-            int incl = mine;
+            __syncwarp();
+            for (int b0 = 0; b0 < nv; b0 += 32) {
+                const int v = b0 + lane < nv ? s_vlist[warp][b0 + lane] : -1;
+                float x[VEC];
+                int mine = 0;
+                const int e = c0 + (warp * VPW + v) * VEC;
+                if (v >= 0) {
+                    Chunk::unpack(vw[v], x);
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int t = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += t;
-            }
-            int wbase = 0;
-            if (lane == 31 && incl > 0) wbase = atomicAdd(&s_cnt, incl);
-            wbase = __shfl_sync(0xffffffffu, wbase, 31);
-            if (mine) {
-                int pos = wbase + incl - mine;
+                    for (int k = 0; k < VEC; ++k) mine += (x[k] >= tv && e + k < V) ? 1 : 0;
+                }
+                int incl = mine;
 #pragma unroll
-                for (int k = 0; k < VEC; ++k) {
-                    if (x[k] >= tv && e + k < V) {
-                        if (pos < kChunkCand) out->keys[pos] = value_index_key(x[k], (uint32_t)(e + k));
-                        ++pos;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += t;
+                }
+                int wbase = 0;
+                if (lane == 31 && incl > 0) wbase = atomicAdd(&s_cnt, incl);
+                wbase = __shfl_sync(0xffffffffu, wbase, 31);
+                if (mine) {
+                    int pos = wbase + incl - mine;
+#pragma unroll
+                    for (int k = 0; k < VEC; ++k) {
+                        if (x[k] >= tv && e + k < V) {
+                            if (pos < kChunkCand) out->keys[pos] = value_index_key(x[k], (uint32_t)(e + k));
+                            ++pos;
+                        }
                     }
                 }
             }
+        };
+
+        // A later chunk of the row this CTA already met: every key below tau_run
+        // (an earlier chunk's bound) is out of the row's K best, so the chunk
+        // keeps its keys >= tau_run and reports tau_run as its bound -- valid for
+        // the merge, which needs only a bound <= the row's K-th largest and every
+        // key >= it.  Too many such keys: the chunk takes the full path below.
+        bool cheap = false;
+        int cnt = 0;
+        if (tau_run != 0u) {
+            gather(float_from_ord(tau_run));
+            __syncthreads();
+            cnt = s_cnt;
+            cheap = cnt <= kChunkCand;
+            if (!cheap) {
+                __syncthreads();  // every thread has read the count
+                if (tid == 0) s_cnt = 0;
+            }
         }
-        __syncthreads();
-        const int cnt = s_cnt;
-        if (cnt > kChunkCand) {
-            cta_exact_top_k<Chunk>(vec, c0, V, K, s_red, out);  // degenerate ties
-        } else if (tid == 0) {
-            out->count = cnt;
-            out->tau = tau;
+        uint32_t tau = tau_run;
+        if (!cheap) {
+            // The warp's K largest vector maxima (K distinct elements), descending,
+            // into s_vm[warp]: the vector maxima at or above the K-th largest lane
+            // maximum (usually K to 3K) sorted by the warp; if there are too many,
+            // K copies of that lane bound (still K elements >= each).
+            {
+                const uint32_t tau_l = warp_kth_largest(e_lane < V ? ord_from_float(mt) : 0u, K);
+                const float tl = (tau_l == 0u) ? -INFINITY : float_from_ord(tau_l);
+                int nm = 0;
+#pragma unroll
+                for (int i = 0; i < PL; ++i) {
+                    const bool in = vmx[i] >= tl && e_lane + 32 * i * VEC < V;
+                    const unsigned bal = __ballot_sync(0xffffffffu, in);
+                    const int at = nm + __popc(bal & ((1u << lane) - 1u));
+                    if (in && at < 32) s_vm[warp][at] = ord_from_float(vmx[i]);
+                    nm += __popc(bal);
+                }
+                __syncwarp();
+                uint32_t top = tau_l;
+                if (nm <= 32) top = warp_sort_desc_u32(lane < nm ? s_vm[warp][lane] : 0u);
+                __syncwarp();
+                if (lane < K) s_vm[warp][lane] = top;
+            }
+            __syncthreads();
+            // tau: the K-th largest of the warps' lists (each warp, redundantly),
+            // a bound on the chunk's K-th largest value
+            {
+                int ptr = 0;
+                uint32_t head = lane < kWarps ? s_vm[lane][0] : 0u;
+                for (int r = 0; r < K; ++r) {
+                    tau = __reduce_max_sync(0xffffffffu, head);
+                    const unsigned holders = __ballot_sync(0xffffffffu, head == tau);
+                    if (lane == __ffs(holders) - 1) {
+                        ++ptr;
+                        head = ptr < K ? s_vm[lane][ptr] : 0u;
+                    }
+                }
+            }
+            gather((tau == 0u) ? -INFINITY : float_from_ord(tau));
+            __syncthreads();
+            cnt = s_cnt;
+            if (cnt > kChunkCand) {
+                cta_exact_top_k<Chunk>(vec, c0, V, K, s_red, out);  // degenerate ties
+            } else {
+                tau_run = max(tau_run, tau);  // (uniform: every warp computed tau)
+            }
         }
         if (tid == 0) {
+            if (cnt <= kChunkCand) {
+                out->count = cnt;
+                out->tau = tau;
+            }
             float m = s_wms[0].x, sm = s_wms[0].y;
 #pragma unroll
             for (int i = 1; i < kWarps; ++i) ms_combine(m, sm, s_wms[i].x, s_wms[i].y, kLog2e);
