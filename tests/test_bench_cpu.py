@@ -1,10 +1,13 @@
 """Host-side logic of bench.py that needs no GPU: the step-4 walk policy of the
 timed round, the workload's byte and flop model, and the DRAM-traffic table
-lookup (reported only while the kernel's sources match the capture)."""
+lookup (reported only while the kernel's sources match the capture), and the
+`--impl reference` arm (the oracle timed on the host)."""
 import os
 
 import bench
 from diffusion_draft_tree_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def test_walk_policy():
@@ -43,3 +46,39 @@ def test_traffic_lookup_follows_the_sources(tmp_path, monkeypatch):
     got = bench.measured_traffic("tree_attn", "8b_single")
     assert got is None or got > 9_000_000
     assert bench.measured_traffic("tree_attn", "no_such_workload") is None
+
+
+def _run_bench(args, env_extra=None):
+    import json
+    import subprocess
+    import sys
+    env = dict(os.environ, **(env_extra or {}))
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], capture_output=True,
+                       text=True, env=env, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    return [json.loads(l) for l in lines]
+
+
+def test_reference_arm_line():
+    """`--impl reference` times the oracle on the host and prints one line with
+    the GPU arm's metric, unit and direction, its own cpu_baseline and an e2e
+    equal to its value with no host-device traffic."""
+    (line,) = _run_bench(["--impl", "reference", "--workload", "tiny", "--steps", "2",
+                          "--warmup", "1"])
+    assert line["impl"] == "reference"
+    assert line["metric"] == bench.METRIC
+    assert line["unit"] == "rounds/s" and line["higher_is_better"] is True
+    assert line["value"] > 0 and line["steps"] == 2 and line["warmup"] == 1
+    assert line["config"]["workload"] == "tiny"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["sample"] and cb["value"] == line["value"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    assert _run_bench(["--impl", "reference", "--workload", "tiny", "--steps", "1",
+                       "--warmup", "0", "--gpus", "2"],
+                      {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}) == []
