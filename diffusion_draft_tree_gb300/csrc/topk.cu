@@ -15,9 +15,12 @@
 // largest; tau, the K-th largest of those lists, is the K-th largest vector
 // maximum of the chunk -- K distinct elements are >= it -- so the chunk keeps
 // only its (value, index) keys >= tau (usually K to 1.5K), together with its
-// (m, s) and tau.  A second, PDL-chained
-// kernel (one CTA per row) bounds the row's K-th largest by the largest chunk
-// tau, ranks the kept keys above it by counting, and forms the logsumexp.
+// (m, s) and tau.  Any chunk's tau bounds its row's K-th largest from below,
+// so a CTA's later chunks of a row it has already met skip the sorts: they
+// keep their keys >= the bound found so far and report it as their tau.  A
+// second, PDL-chained kernel (one CTA per row) bounds the row's K-th largest
+// by the largest chunk tau, ranks the kept keys above it by counting, and
+// forms the logsumexp.
 #include <mutex>
 
 #include "chunk.cuh"
