@@ -13,6 +13,8 @@
 //
 // T_d is the top N among all prefixes of depth <= d (a depth-d prefix in it
 // has its parent in it, and that parent is among the top N of depth <= d-1).
+// T_1 needs no merge: the root's children are position 1's K tokens, which
+// the top-K step already returns in priority order, so it is written directly.
 // When T is full, a child must beat its last key, and once the strongest
 // parent's best child cannot, no deeper node can enter and the build stops.
 // The qualifying children are gathered (in any order), sorted (rank counting
