@@ -29,40 +29,49 @@ _lib = None
 BF16, FP32 = 0, 1
 
 
+def _compile(src: str, so: str) -> None:
+    """gcc with portable flags: the same source runs on x86 and Arm."""
+    tmp = so + f".{os.getpid()}.tmp"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+                           "-o", tmp, src, "-lm"])
+    os.replace(tmp, so)
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (portable flags: the same source runs on x86 and Arm)."""
+    """Compile the oracle (once; again when the source is newer)."""
     os.makedirs(_OUT_DIR, exist_ok=True)
     if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
-        tmp = _SO + f".{os.getpid()}.tmp"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
-                               "-o", tmp, _SRC, "-lm"])
-        os.replace(tmp, _SO)
+        _compile(_SRC, _SO)
     return _SO
+
+
+def _bind(lib):
+    """Declares the C signatures on a loaded oracle library."""
+    P = ctypes.c_void_p
+    i32, i64, f64, u64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_uint64
+    lib.ddo_topk.argtypes = [P, i32, i32, i32, i64, i32, P, P, P, P]
+    lib.ddo_build.argtypes = [P, P, P, P, i32, i32, i32, i32] + [P] * 9
+    lib.ddo_tree_attn_unit.argtypes = [i32, i32, i32, i32, P, P, P, i64, P, P, P, P, P, i32, i32,
+                                       i32, i32, i32, f64, P, P]
+    lib.ddo_tree_attn.argtypes = [P, P, P, i64, P, P, P, P, P, i32, i32, i32, i32, i32, f64, P,
+                                  P]
+    lib.ddo_philox4x64_10.argtypes = [P, P, P]
+    lib.ddo_uniform.argtypes = [u64, u64, u64, u64]
+    lib.ddo_uniform.restype = f64
+    lib.ddo_accept.argtypes = [P, i32, i64, P, P, P, i32, i32, i32, i32, f64, u64, u64, P, P,
+                               P, P, P, P]
+    lib.ddo_commit.argtypes = [P, P, i64, P, P, P, P, P, i32, i32, i32, i32, i32]
+    for f in (lib.ddo_topk, lib.ddo_build, lib.ddo_tree_attn_unit, lib.ddo_tree_attn,
+              lib.ddo_accept, lib.ddo_commit):
+        f.restype = ctypes.c_int
+    return lib
 
 
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            P = ctypes.c_void_p
-            i32, i64, f64, u64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_uint64
-            lib.ddo_topk.argtypes = [P, i32, i32, i32, i64, i32, P, P, P, P]
-            lib.ddo_build.argtypes = [P, P, P, P, i32, i32, i32, i32] + [P] * 9
-            lib.ddo_tree_attn_unit.argtypes = [i32, i32, i32, i32, P, P, P, i64, P, P, P, P, P, i32, i32,
-                                               i32, i32, i32, f64, P, P]
-            lib.ddo_tree_attn.argtypes = [P, P, P, i64, P, P, P, P, P, i32, i32, i32, i32, i32,
-                                          f64, P, P]
-            lib.ddo_philox4x64_10.argtypes = [P, P, P]
-            lib.ddo_uniform.argtypes = [u64, u64, u64, u64]
-            lib.ddo_uniform.restype = f64
-            lib.ddo_accept.argtypes = [P, i32, i64, P, P, P, i32, i32, i32, i32, f64, u64, u64,
-                                       P, P, P, P, P, P]
-            lib.ddo_commit.argtypes = [P, P, i64, P, P, P, P, P, i32, i32, i32, i32, i32]
-            for f in (lib.ddo_topk, lib.ddo_build, lib.ddo_tree_attn_unit, lib.ddo_tree_attn,
-                      lib.ddo_accept, lib.ddo_commit):
-                f.restype = ctypes.c_int
-            _lib = lib
+            _lib = _bind(ctypes.CDLL(build()))
     return _lib
 
 

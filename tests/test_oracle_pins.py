@@ -422,6 +422,45 @@ def test_sampling_rule_is_inverse_cdf():
             assert out["margin"][0, u] > 0
 
 
+def _margin_by_numpy(x64, T, seed, step, b, u):
+    """The distance from U*Z to the nearest edge of the sampled token's CDF bin,
+    over Z, written from the definition with numpy (fp64 sequential cumsum,
+    searchsorted): bin t = [C_{t-1}, C_t) with C_{-1} = 0."""
+    p = np.exp((x64 - x64.max()) / T)
+    c = np.cumsum(p)
+    z = c[-1]
+    tgt = oracle.uniform(seed, step, b, u) * z
+    t = int(np.searchsorted(c, tgt, side="right"))
+    lo = c[t - 1] if t > 0 else 0.0
+    return t, min(tgt - lo, c[t] - tgt) / z
+
+
+@pytest.mark.parametrize("V,T,flat", [(40, 1.0, False), (1000, 1.0, False), (1000, 0.5, True),
+                                      (151936, 1.0, False)])
+def test_sampling_margin_is_distance_to_nearest_cdf_edge(V, T, flat):
+    """The oracle's per-node margin (the band the T > 0 GPU parity check admits)
+    equals min(U*Z - C_{t-1}, C_t - U*Z) / Z for every node, recomputed from the
+    definition; the flat rows put many tokens of similar mass next to U*Z."""
+    rng = np.random.default_rng(V + int(10 * T))
+    R = 6 if V > 10000 else 31
+    x = (rng.standard_normal((2, R, V)) * (0.05 if flat else 2.5)).astype(np.float32)
+    par = np.array([[-1] + [max(0, (u - 1) // 2) for u in range(1, R)]] * 2, np.int32)
+    tree = {"parent": par, "token": rng.integers(0, V, size=(2, R)).astype(np.int32),
+            "n_nodes": np.array([R - 1, R - 3], np.int32)}
+    for seed, step in [(11, 0), (0xDD7EE, 5)]:
+        out = oracle.accept(x, wl.FP32, tree, L=4, temperature=T, seed=seed, step=step)
+        for b in range(2):
+            n = tree["n_nodes"][b]
+            for u in range(n + 1):
+                t, mg = _margin_by_numpy(x[b, u].astype(np.float64), T, seed, step, b, u)
+                assert out["target_token"][b, u] == t
+                assert abs(out["margin"][b, u] - mg) <= 1e-12, (b, u)
+            assert np.all(np.isinf(out["margin"][b, n + 1:]))
+    # greedy: no band at all
+    out = oracle.accept(x, wl.FP32, tree, L=4, temperature=0.0)
+    assert np.all(np.isinf(out["margin"]))
+
+
 @pytest.mark.slow
 def test_sampling_frequencies_match_softmax():
     from scipy.stats import chisquare
