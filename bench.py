@@ -4,14 +4,17 @@ attention (one target layer) -> acceptance walk, through libddtree.so.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gb300|reference]
 
 Prints ONE JSON line (rank 0).  `value` is sequence-rounds per second with all
-inputs resident in HBM; a "step" is one round over one batch.  The round's four
+inputs resident in HBM; a "step" is one round over one batch.  The default
+workload is the largest single-GPU one (long_context_70b).  The round's four
 C-ABI calls are captured in CUDA graphs; to keep the 129 MB L2 from serving a
-step's inputs, steps rotate over R copies of every per-step input (R copies
-> 2x L2).  `e2e` repeats the measurement through the public API from pinned
-host buffers (inputs copied in and results copied out every step).
-`--impl reference` times the CPU oracle on the host cores instead (a reported
-baseline; it runs a bounded sample of the same workload per step).
-Multi-GPU runs are independent replicas (sequences are independent units).
+step's inputs, steps rotate over copies of every per-step input (together
+> 3x L2).  Each call is also timed alone (graphs of back-to-back launches) for
+the per-call rates and the roofline.  `e2e` repeats the measurement through the
+public API from pinned host buffers (inputs copied in and results copied out
+every step).  `--impl reference` times the CPU oracle on the host cores
+instead (a reported baseline; on the large workloads each step computes the
+tree attention of a seeded sample of node rows).  Multi-GPU runs are
+independent replicas (sequences are independent units).
 """
 from __future__ import annotations
 
@@ -37,9 +40,11 @@ X36 = 36  # layers of the 8B-class target (Qwen3-8B)
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="8b_single", choices=sorted(wl.CONFIGS))
+    ap.add_argument("--workload", default="long_context_70b", choices=sorted(wl.CONFIGS),
+                    help="default: the largest single-GPU workload (B = 4, P = 131072, "
+                         "N = 256, 64/8 heads)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -100,19 +105,18 @@ def kernel_source_hash(kernel: str) -> str:
 
 def measured_traffic(kernel: str, workload: str):
     """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) that an
-    ncu capture recorded in profiles/traffic.md for this kernel and workload, or
-    None if there is none or the kernel's sources changed since."""
-    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "traffic.md")
+    ncu capture recorded in profiles/traffic.json for this kernel and workload,
+    or None if there is none or the kernel's sources changed since."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
+    with open(path) as f:
+        entries = json.load(f).get("entries", [])
     want = kernel_source_hash(kernel)
-    for line in open(path):
-        cells = [c.strip() for c in line.strip().strip("|").split("|")]
-        if len(cells) >= 4 and cells[0] == kernel and cells[1] == workload and cells[3] == want:
-            try:
-                return int(cells[2])
-            except ValueError:
-                return None
+    for e in entries:
+        if e.get("kernel") == kernel and e.get("workload") == workload and \
+                e.get("sources_sha16") == want:
+            return int(e["bytes_per_launch"])
     return None
 
 
@@ -255,6 +259,115 @@ def host_inputs(w):
             "v_cache": wl.kv_cache(w, 1), "k_tree": wl.kv_tree(w, 0), "v_tree": wl.kv_tree(w, 1)}
 
 
+STAGE_METHOD = ("each call alone: a captured graph of M back-to-back launches over rotating "
+                "copies of its own inputs (together > 3x the L2), CUDA events around the whole "
+                "replay on the launching stream, per launch = total / M; no event between "
+                "launches, so no per-launch event latency")
+
+
+def stage_times(ops, w, base, copies, rounds, ws, dev, stream, steps):
+    """Per-launch time (ms) of each call of the round and of the two calls after
+    it, each timed alone (see STAGE_METHOD)."""
+    import torch
+
+    r0 = rounds[0]
+    t_budget_ms = 60.0  # device time per replay
+
+    def n_copies(nbytes):
+        return int(max(2, min(64, np.ceil(3 * L2_BYTES / max(1, nbytes)))))
+
+    def grow(key, n):  # n device copies of one per-step input (list-valued keys: layer 0)
+        have = [c[key][0] if isinstance(c[key], list) else c[key] for c in copies]
+        while len(have) < n:
+            have.append(have[len(have) % len(copies)].clone())
+        return have[:n]
+
+    def time_graph(make, n, est_ms):
+        M = n * max(1, int(min(64, max(4, t_budget_ms / max(est_ms, 1e-3))) // n))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(M):
+                make(i % n)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                g.replay()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            reps = []
+            for _ in range(3):
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                reps.append(e0.elapsed_time(e1) / M)
+        ops.ddtree_device_check()
+        del g
+        return {"ms": float(np.median(reps)), "launches": M, "input_copies": n}
+
+    def nb(t):
+        return t.numel() * t.element_size()
+
+    out = {}
+    # step 1: top-K over copies of the draft logits
+    drafts = grow("draft", n_copies(nb(base["draft"])))
+    out["topk"] = time_graph(lambda i: ops.ddtree_topk(drafts[i], w.K, r0.topk_idx, r0.topk_lp,
+                                                       r0.lse, ws["topk"]), len(drafts), 0.02)
+    # restore the round's top-K outputs (same draft logits: identical)
+    ops.ddtree_topk(base["draft"], w.K, r0.topk_idx, r0.topk_lp, r0.lse, ws["topk"])
+    # step 2: the build reads the (small) top-K outputs, as in the round
+    out["build"] = time_graph(lambda i: ops.ddtree_build(
+        r0.topk_lp.view(w.B, w.L, w.K), r0.topk_idx.view(w.B, w.L, w.K), base["bonus"],
+        base["prefix_len"], w.N, r0.tree), 1, 0.02)
+    # step 3: tree attention over copies of q, the KV cache and the tree K/V
+    kv_keys = ("q", "k_cache", "v_cache", "k_tree", "v_tree")
+    n_a = n_copies(sum(nb(base[k][0]) for k in kv_keys))
+    kv = {k: grow(k, n_a) for k in kv_keys}
+    est = 1e-3 * sum(nb(base[k][0]) for k in kv_keys) / 2e3  # ~2 TB/s guess
+    out["tree_attn"] = time_graph(lambda i: ops.ddtree_tree_attn(
+        kv["q"][i], kv["k_cache"][i], kv["v_cache"][i], kv["k_tree"][i], kv["v_tree"][i],
+        base["prefix_len"], r0.tree["n_nodes"], r0.tree["anc_mask"], r0.out[0], None, None,
+        ws["attn"]), n_a, est)
+    del kv
+    # step 4, both walks, over copies of the target logits
+    targets = grow("target", n_copies(nb(base["target"])))
+    accs = {"path": ops.accept_buffers(w.B, w.L, w.N, dev),
+            "full": ops.accept_buffers(w.B, w.L, w.N, dev)}
+    seed = wl.philox_seed(w)
+    est = 1e-3 * nb(base["target"]) / 3e3
+    out["accept_path"] = time_graph(lambda i: ops.ddtree_accept_path(
+        targets[i], r0.tree["parent"], r0.tree["token"], r0.tree["n_nodes"], w.L, accs["path"],
+        w.T, seed, 0), len(targets), 0.02)
+    out["accept_full"] = time_graph(lambda i: ops.ddtree_accept(
+        targets[i], r0.tree["parent"], r0.tree["token"], r0.tree["n_nodes"], w.L, accs["full"],
+        w.T, seed, 0, ws["accept"]), len(targets), est)
+    out["same_tokens"] = bool(torch.equal(accs["path"]["out_tokens"], accs["full"]["out_tokens"]))
+    out["path_rows"] = int(accs["path"]["accept_len"].sum().item()) + w.B
+    out["accept"] = dict(out["accept_" + walk_for(w)])
+    del targets, drafts
+    # after the round: commit the accepted path (prefix lengths restored before each)
+    try:
+        cap2 = w.P_cap + w.L + 1
+        kc2 = torch.empty((w.B, w.Hkv, cap2, w.D), dtype=torch.bfloat16, device=dev)
+        vc2 = torch.empty_like(kc2)
+        plen0 = base["prefix_len"]
+        plen = plen0.clone()
+
+        def commit(i):
+            plen.copy_(plen0)
+            ops.ddtree_commit(kc2, vc2, base["k_tree"][0], base["v_tree"][0],
+                              accs["path"]["accept_len"], accs["path"]["accepted_nodes"], plen)
+
+        out["commit"] = time_graph(commit, 1, 0.01)
+        out["commit"]["note"] = ("includes a 4-byte-per-sequence copy restoring the prefix "
+                                 "lengths before each launch")
+        out["commit_rows"] = out["path_rows"]
+        del kc2, vc2
+    except Exception as e:  # noqa: BLE001
+        out["commit"] = {"unavailable": repr(e)}
+    return out
+
+
 def gpu_arm(args, rank, world, dev):
     import torch
     from diffusion_draft_tree_gb300 import ops
@@ -289,7 +402,7 @@ def gpu_arm(args, rank, world, dev):
                    if k in ("draft", "target")) + sum(
         t[0].numel() * t[0].element_size() for k, t in base.items()
         if k in ("q", "k_cache", "v_cache", "k_tree", "v_tree"))
-    R = max(2, min(64, int(np.ceil(3 * L2_BYTES / per_copy))))
+    R = max(2, min(64, int(np.ceil(3 * L2_BYTES / per_copy))))  # > 3x the L2 together
 
     def clone(src):
         return {k: ([t.clone() for t in v] if isinstance(v, list) else v.clone())
@@ -351,123 +464,17 @@ def gpu_arm(args, rank, world, dev):
     ms_total = e0.elapsed_time(e1)
     clocks = sampler.summary()
 
-    # per-kernel durations: external event nodes inside a captured graph
-    kern = {}
+    # Every call of the round, and the calls outside it, timed alone: a captured
+    # graph of M back-to-back launches of that call over rotating copies of its
+    # own inputs (together > 3x the L2), CUDA events around the whole replay,
+    # per launch = total / M.  As in the round, programmatic dependent launch
+    # lets a launch's set-up overlap the previous launch's tail, and no event
+    # sits between launches to add its latency.
+    stage = {}
     try:
-        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
-               for _ in range(R)]
-        g_ev = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_ev, stream=stream):
-            for r, ev in zip(rounds, evs):
-                st = r.stages()
-                for i in range(4):
-                    ev[i].record()
-                    st[i]()
-                ev[4].record()
-        acc = np.zeros(4)
-        reps = max(4, min(200, args.steps // R))
-        for _ in range(reps):
-            g_ev.replay()
-            torch.cuda.synchronize()
-            for ev in evs:
-                acc += [ev[i].elapsed_time(ev[i + 1]) for i in range(4)]
-        kern_ms = acc / (reps * R)
-        kern_method = "external CUDA events between the four kernels inside the graph"
+        stage = stage_times(ops, w, base, copies, rounds, ws, dev, stream, args.steps)
     except Exception as e:  # noqa: BLE001
-        kern_ms = np.full(4, np.nan)
-        kern_method = f"unavailable: {e!r}"
-
-    # the step after the round: commit the accepted path to the KV cache (not
-    # part of the round's metric; timed alone, prefix lengths restored first)
-    commit = None
-    try:
-        r0 = rounds[0]
-        cap2 = w.P_cap + w.L + 1
-        kc2 = torch.empty((w.B, w.Hkv, cap2, w.D), dtype=torch.bfloat16, device=dev)
-        vc2 = torch.empty_like(kc2)
-        plen0 = base["prefix_len"]
-        plen = plen0.clone()
-        n_c = 20
-        c_ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
-                for _ in range(n_c)]
-
-        def commit_once(ev):
-            plen.copy_(plen0)
-            ev[0].record()
-            ops.ddtree_commit(kc2, vc2, base["k_tree"][0], base["v_tree"][0],
-                              r0.acc["accept_len"], r0.acc["accepted_nodes"], plen)
-            ev[1].record()
-
-        commit_once(c_ev[0])
-        torch.cuda.synchronize()
-        g_c = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_c, stream=stream):
-            for ev in c_ev:
-                commit_once(ev)
-        t_c = 0.0
-        for _ in range(5):
-            g_c.replay()
-            torch.cuda.synchronize()
-            t_c += sum(ev[0].elapsed_time(ev[1]) for ev in c_ev)
-        n_c *= 5
-        ops.ddtree_device_check()
-        rows = int(r0.acc["accept_len"].sum().item()) + w.B
-        commit = {"ms": t_c / n_c, "bytes": 8 * rows * w.Hkv * w.D}
-        del kc2, vc2
-    except Exception as e:  # noqa: BLE001
-        commit = {"unavailable": repr(e)}
-
-    # the path-only walk on the same round's tree and target rows (an alternative
-    # to the full-tree accept; timed alone, not in the round's metric)
-    # both step-4 walks timed alone on the same round's tree and target rows
-    # (whichever the round uses), and their emitted tokens compared
-    walks = {}
-    try:
-        r0 = rounds[0]
-        outs = {"path": ops.accept_buffers(w.B, w.L, w.N, dev),
-                "full": ops.accept_buffers(w.B, w.L, w.N, dev)}
-
-        def run_walk(kind):
-            if kind == "path":
-                ops.ddtree_accept_path(r0.inp["target"], r0.tree["parent"], r0.tree["token"],
-                                       r0.tree["n_nodes"], w.L, outs[kind], w.T,
-                                       wl.philox_seed(w), 0)
-            else:
-                ops.ddtree_accept(r0.inp["target"], r0.tree["parent"], r0.tree["token"],
-                                  r0.tree["n_nodes"], w.L, outs[kind], w.T, wl.philox_seed(w), 0,
-                                  ws["accept"])
-
-        for kind in ("path", "full"):
-            n_p = 20
-            p_ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
-                    for _ in range(n_p)]
-
-            def once(ev):
-                ev[0].record()
-                run_walk(kind)
-                ev[1].record()
-
-            once(p_ev[0])
-            torch.cuda.synchronize()
-            g_p = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g_p, stream=stream):
-                for ev in p_ev:
-                    once(ev)
-            t_p = 0.0
-            for _ in range(5):
-                g_p.replay()
-                torch.cuda.synchronize()
-                t_p += sum(ev[0].elapsed_time(ev[1]) for ev in p_ev)
-            ops.ddtree_device_check()
-            walks[kind] = {"ms": t_p / (5 * n_p)}
-        same = bool(torch.equal(outs["path"]["out_tokens"], outs["full"]["out_tokens"]))
-        rows = int(outs["path"]["accept_len"].sum().item()) + w.B
-        walks["path"]["bytes"] = rows * w.V * w.esize
-        walks["full"]["bytes"] = w.B * (w.N + 1) * w.V * w.esize
-        walks["same_tokens"] = same
-        del outs
-    except Exception as e:  # noqa: BLE001
-        walks = {"unavailable": repr(e)}
+        stage = {"unavailable": repr(e)}
 
     # 36-layer round: 36 tree-attention launches, each on its own KV cache
     x36 = None
@@ -594,28 +601,24 @@ def gpu_arm(args, rank, world, dev):
     tree_anc = int(np.sum([bin(int(x)).count("1") for x in
                            rounds[0].tree["anc_mask"].cpu().numpy().view(np.uint32).ravel()]))
     return {"w": w, "ms_total": ms_total, "R": R, "per_copy": per_copy, "clocks": clocks,
-            "kern_ms": kern_ms, "kern_method": kern_method, "x36": x36, "e2e": e2e,
-            "commit": commit, "walks": walks,
-            "tree_anc": tree_anc}
+            "stage": stage, "x36": x36, "e2e": e2e, "tree_anc": tree_anc}
 
 
 # ---------------------------------------------------------------------------
 # the CPU oracle (reported baseline; also the `--impl reference` arm)
 # ---------------------------------------------------------------------------
 
-def oracle_step(o, w, h, attn_units):
-    t0 = time.perf_counter()
-    idx, _, lp32, _ = o.topk(h["draft"].reshape(w.B, w.L, w.V), w.dtype, w.K)
-    t1 = time.perf_counter()
-    tree = o.build_tree(lp32, idx, h["bonus"], h["prefix_len"], w.N)
-    t2 = time.perf_counter()
-    o.tree_attn(h["q"], h["k_cache"], h["v_cache"], h["k_tree"], h["v_tree"], h["prefix_len"],
-                tree["n_nodes"], tree["anc_mask"], units=attn_units)
-    t3 = time.perf_counter()
-    o.accept(h["target"], w.dtype, tree, w.L, temperature=w.T, seed=wl.philox_seed(w))
-    t4 = time.perf_counter()
-    scale_attn = (w.B * w.Hkv) / len(attn_units)
-    return (t1 - t0) + (t2 - t1) + (t3 - t2) * scale_attn + (t4 - t3)
+# Key-head rows of fp64 tree attention one host core is given per oracle step
+# (one key row against one query head: ~0.2-0.3 us on the hosts measured), so
+# a step's attention takes about a second on every core.
+ORACLE_ROWS_PER_CORE = 1 << 22
+
+
+def host_cores() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
 
 
 def oracle_setup(w):
@@ -625,47 +628,117 @@ def oracle_setup(w):
     idx, _, lp32, _ = oracle.topk(draft, w.dtype, w.K)
     tree = oracle.build_tree(lp32, idx, h["bonus"], h["prefix_len"], w.N)
     h["target"] = wl.target_logits(w, draft, tree["depth"])
-    return oracle, h
+    return oracle, h, tree
+
+
+def oracle_attn_tasks(w, n_nodes, cores):
+    """The tree-attention work of one oracle step, as (b, kv_head, u_lo, u_hi)
+    tasks, with its size and the full layer's size in key-head rows (one key
+    against one query head).  The whole layer when it fits the per-core budget,
+    else a seeded uniform sample of single node rows (b, g, u) that does."""
+    G = w.Hq // w.Hkv
+    row_cost = [G * (w.P[b] + int(n_nodes[b]) + 1) for b in range(w.B)]
+    total = sum(w.Hkv * (int(n_nodes[b]) + 1) * row_cost[b] for b in range(w.B))
+    budget = cores * ORACLE_ROWS_PER_CORE
+    if total <= budget:
+        return [(b, g, 0, w.N + 1) for b in range(w.B) for g in range(w.Hkv)], total, total
+    rows = [(b, g, u) for b in range(w.B) for g in range(w.Hkv) for u in range(int(n_nodes[b]) + 1)]
+    order = np.random.default_rng(0x0AC1E).permutation(len(rows))
+    tasks, done = [], 0
+    for i in order:
+        b, g, u = rows[i]
+        if done + row_cost[b] > budget and len(tasks) >= cores:
+            break
+        tasks.append((b, g, u, u + 1))
+        done += row_cost[b]
+    return tasks, done, total
+
+
+def oracle_step(o, w, h, tasks, cores):
+    """One round of the oracle: top-K, heap and walk over the whole batch, tree
+    attention on `tasks` spread over `cores` host threads.  Returns the four
+    stage times (s)."""
+    t0 = time.perf_counter()
+    idx, _, lp32, _ = o.topk(h["draft"].reshape(w.B, w.L, w.V), w.dtype, w.K)
+    t1 = time.perf_counter()
+    tree = o.build_tree(lp32, idx, h["bonus"], h["prefix_len"], w.N)
+    t2 = time.perf_counter()
+    o.tree_attn_tasks(h["q"], h["k_cache"], h["v_cache"], h["k_tree"], h["v_tree"],
+                      h["prefix_len"], tree["n_nodes"], tree["anc_mask"], tasks, threads=cores)
+    t3 = time.perf_counter()
+    o.accept(h["target"], w.dtype, tree, w.L, temperature=w.T, seed=wl.philox_seed(w))
+    t4 = time.perf_counter()
+    return np.array([t1 - t0, t2 - t1, t3 - t2, t4 - t3])
+
+
+def oracle_summary(w, stage_s, done_rows, total_rows, cores, steps):
+    """The measured oracle step and, separately, a full round extrapolated from
+    it (attention time scaled by the unsampled share of its key-head rows)."""
+    per = stage_s.mean(axis=0)
+    step_s = float(per.sum())
+    full_s = float(per[0] + per[1] + per[2] * total_rows / done_rows + per[3])
+    frac = done_rows / total_rows
+    if done_rows == total_rows:
+        sample = (f"{steps} full rounds of '{w.name}' (all B = {w.B} sequences): top-K, heap and "
+                  f"walk on 1 core, tree attention over (sequence, KV head) units on {cores} "
+                  f"host threads")
+    else:
+        sample = (f"{steps} rounds of '{w.name}' (all B = {w.B} sequences): top-K, heap and walk "
+                  f"in full on 1 core; tree attention on a seeded sample of node rows "
+                  f"({100 * frac:.3g} % of the layer's key-head rows) on {cores} host threads; "
+                  f"value counts these sampled rounds")
+    return {"value": w.B / step_s, "unit": "rounds/s", "cores": cores, "kind": "oracle",
+            "sample": sample, "seconds_per_step": step_s,
+            "stage_seconds": {k: float(v) for k, v in zip(("topk", "build", "tree_attn", "accept"),
+                                                          per)},
+            "attn_fraction_of_layer": frac,
+            "full_round_extrapolated": {"seconds": full_s, "rounds_per_s": w.B / full_s,
+                                        "method": "attention time x (layer's key-head rows / "
+                                                  "sampled ones); other stages as measured"}}
 
 
 def cpu_baseline(w, seconds, steps=None):
-    o, h = oracle_setup(w)
-    units = [(0, 0)]  # one (sequence, KV head) unit of tree attention per step, scaled up
+    o, h, tree = oracle_setup(w)
+    cores = host_cores()
+    tasks, done, total = oracle_attn_tasks(w, tree["n_nodes"], cores)
     times = []
     t_start = time.perf_counter()
     while True:
-        times.append(oracle_step(o, w, h, units))
+        times.append(oracle_step(o, w, h, tasks, cores))
         if steps is not None and len(times) >= steps:
             break
         if steps is None and (time.perf_counter() - t_start > seconds or len(times) >= 50):
             break
-    per_step = float(np.mean(times))
-    sample = (f"{len(times)} rounds of '{w.name}': top-K, heap and walk in full; tree attention "
-              f"on 1 of {w.B * w.Hkv} (sequence, KV head) units, time scaled x{w.B * w.Hkv}")
-    return {"value": w.B / per_step, "unit": "rounds/s", "cores": 1, "kind": "oracle",
-            "sample": sample, "seconds_per_round": per_step}
+    return oracle_summary(w, np.array(times), done, total, cores, len(times))
 
 
 def reference_arm(args, rank, world):
+    """`--impl reference`: the oracle, as it stands, timed on the host cores on
+    the GPU arm's workload, metric, unit and direction.  Each step is one
+    oracle round (sampled attention on the large shapes); `ms_per_step` and
+    `value` are those measured steps; a full round's extrapolated time is in
+    its own field."""
     w = wl.CONFIGS[args.workload]
     if rank != 0:
         return
-    o, h = oracle_setup(w)
-    units = [(0, 0)]
+    o, h, tree = oracle_setup(w)
+    cores = host_cores()
+    tasks, done, total = oracle_attn_tasks(w, tree["n_nodes"], cores)
     for _ in range(args.warmup):
-        oracle_step(o, w, h, units)
-    t = [oracle_step(o, w, h, units) for _ in range(args.steps)]
-    per_step = float(np.mean(t))
-    value = w.B / per_step
-    sample = (f"each step: one round of '{w.name}' with tree attention on 1 of "
-              f"{w.B * w.Hkv} (sequence, KV head) units, time scaled x{w.B * w.Hkv}")
+        oracle_step(o, w, h, tasks, cores)
+    t0 = time.perf_counter()
+    st = np.array([oracle_step(o, w, h, tasks, cores) for _ in range(args.steps)])
+    wall = time.perf_counter() - t0
+    summ = oracle_summary(w, st, done, total, cores, args.steps)
+    ms_step = wall * 1e3 / args.steps
+    value = w.B * args.steps / wall
+    summ["value"] = value
     line = {"impl": "reference", "metric": METRIC,
             "value": value, "unit": "rounds/s", "n_gpus": args.gpus, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_of(w, None),
-            "cpu_baseline": {"value": value, "unit": "rounds/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "config": config_of(w), "cpu_baseline": summ,
+            "full_round_extrapolated": summ["full_round_extrapolated"],
             "e2e": {"value": value, "unit": "rounds/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -685,13 +758,16 @@ def aggregate_replicas(ms_local: float, world: int, B: int, steps: int, device):
     return ms, world * B * steps / (ms / 1e3)
 
 
-def config_of(w, R):
-    c = {"workload": w.name, "B": w.B, "L": w.L, "V": w.V, "K": w.K, "N": w.N,
-         "P": list(w.P) if len(set(w.P)) > 1 else w.P[0], "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
-         "temperature": w.T, "layers": 1, "walk": walk_for(w)}
-    if R is not None:
-        c["l2"] = f"inputs rotated over {R} copies per step (> 2x the 129 MB L2)"
-    return c
+# How the timed steps keep the L2 from serving their inputs (both arms print
+# the same config; the GPU arm's number of input copies is in `input_copies`).
+L2_POLICY = ("per-step inputs rotated over copies that together exceed 3x the 129 MB L2, "
+             "so no step reads its inputs from L2")
+
+
+def config_of(w):
+    return {"workload": w.name, "B": w.B, "L": w.L, "V": w.V, "K": w.K, "N": w.N,
+            "P": list(w.P) if len(set(w.P)) > 1 else w.P[0], "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+            "temperature": w.T, "layers": 1, "walk": walk_for(w), "l2": L2_POLICY}
 
 
 def acceptance_stats(rounds: int) -> dict:
@@ -760,6 +836,66 @@ def walk_for(w) -> str:
     return "path" if w.B * (w.N + 1) >= 128 else "full"
 
 
+def kernel_report(w, model, stage, peaks):
+    """Per-call achieved rates from the stage times, and the roofline object of
+    the dominant call (tree attention), its bound chosen from its arithmetic
+    intensity against the measured peaks."""
+    kernels = {}
+    if "unavailable" in stage:
+        return {"unavailable": stage["unavailable"]}, None
+    path_bytes = stage["path_rows"] * w.V * w.esize
+    full_bytes = w.B * (w.N + 1) * w.V * w.esize
+    if walk_for(w) == "path":  # the round's step 4 reads the path's rows only
+        model = dict(model, accept={"bytes": path_bytes})
+    model = dict(model, accept_path={"bytes": path_bytes}, accept_full={"bytes": full_bytes},
+                 commit={"bytes": 8 * stage.get("commit_rows", 0) * w.Hkv * w.D})
+    notes = {"accept": f"step 4 of the round: the {walk_for(w)} walk",
+             "accept_path": "step 4 reading only the accepted path's rows (bytes = "
+                            "(accept_len + 1) x V x elem per sequence); outside the round",
+             "accept_full": "step 4 resolving every tree row (bytes = (N + 1) x V x elem per "
+                            "sequence); outside the round",
+             "commit": "after the round, not in its metric: the accepted path's K/V rows "
+                       "into the cache"}
+    for n in ("topk", "build", "tree_attn", "accept", "accept_path", "accept_full", "commit"):
+        st = stage.get(n) or {}
+        if "ms" not in st:
+            kernels[n] = st
+            continue
+        ms = st["ms"]
+        k = {"ms": ms, "launches_timed": st["launches"], "input_copies": st["input_copies"]}
+        if "bytes" in model[n]:
+            k["bytes"] = model[n]["bytes"]
+            k["GBps"] = model[n]["bytes"] / (ms * 1e-3) / 1e9
+            k["hbm_frac"] = k["GBps"] / peaks["hbm_gbs"]
+        if "flops" in model[n]:
+            k["flops"] = model[n]["flops"]
+            k["TFLOPps"] = model[n]["flops"] / (ms * 1e-3) / 1e12
+            k["tensor_frac"] = k["TFLOPps"] / peaks["bf16_tflops"]
+        if n in notes:
+            k["note"] = notes[n]
+        if n.startswith("accept_"):
+            k["same_tokens_as_other_walk"] = stage.get("same_tokens")
+        kernels[n] = k
+    a = model["tree_attn"]
+    ams = kernels["tree_attn"]["ms"]
+    t_hbm = a["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = a["flops"] / (peaks["bf16_tflops"] * 1e12)
+    if t_tc >= t_hbm:
+        roof = {"kernel": "tree_attn", "bound": "tensor",
+                "achieved": a["flops"] / (ams * 1e-3) / 1e12, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"kernel": "tree_attn", "bound": "hbm", "achieved": a["bytes"] / (ams * 1e-3) / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = measured_traffic("tree_attn", w.name)
+    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json burst figure), of measured"
+    roof["algorithmic_bytes"] = a["bytes"]
+    roof["algorithmic_flops"] = a["flops"]
+    roof["duration_ms"] = ams
+    return kernels, roof
+
+
 def main():
     global WALK
     args = parse()
@@ -794,59 +930,16 @@ def main():
     ms_step = ms_total / args.steps
     peaks = load_peaks()
     model = work_model(w, res["tree_anc"])
-    wk = res.get("walks") or {}
-    if walk_for(w) == "path" and "path" in wk:  # the round's step 4 reads the path's rows only
-        model["accept"] = {"bytes": wk["path"]["bytes"]}
-    names = ["topk", "build", "tree_attn", "accept"]
-    kernels = {}
-    for n, ms in zip(names, res["kern_ms"]):
-        k = {"ms": float(ms)}
-        if "bytes" in model[n]:
-            k["GBps"] = model[n]["bytes"] / (ms * 1e-3) / 1e9
-            k["hbm_frac"] = k["GBps"] / peaks["hbm_gbs"]
-        if "flops" in model[n]:
-            k["TFLOPps"] = model[n]["flops"] / (ms * 1e-3) / 1e12
-            k["tensor_frac"] = k["TFLOPps"] / peaks["bf16_tflops"]
-        kernels[n] = k
-    c = res.get("commit")
-    if c and "ms" in c:
-        kernels["commit"] = {"ms": c["ms"], "GBps": c["bytes"] / (c["ms"] * 1e-3) / 1e9,
-                             "hbm_frac": c["bytes"] / (c["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                             "note": "after the round, not in its metric: the accepted "
-                                     "path's K/V rows into the cache"}
-    wk = res.get("walks") or {}
-    for kind in ("path", "full"):
-        c = wk.get(kind)
-        if c and "ms" in c:
-            kernels["accept_" + kind] = {
-                "ms": c["ms"], "GBps": c["bytes"] / (c["ms"] * 1e-3) / 1e9,
-                "hbm_frac": c["bytes"] / (c["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                "same_tokens_as_other_walk": wk.get("same_tokens"),
-                "note": ("step 4 reading only the accepted path's rows (bytes = (accept_len + 1)"
-                         " x V x elem per sequence)" if kind == "path" else
-                         "step 4 resolving every tree row (bytes = (N + 1) x V x elem per "
-                         "sequence)") + "; timed alone, outside the round"}
-    a = model["tree_attn"]
-    t_hbm = a["bytes"] / (peaks["hbm_gbs"] * 1e9)
-    t_tc = a["flops"] / (peaks["bf16_tflops"] * 1e12)
-    ams = float(res["kern_ms"][2])
-    if t_tc >= t_hbm:
-        roof = {"kernel": "tree_attn", "bound": "tensor", "achieved": a["flops"] / (ams * 1e-3) / 1e12,
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
-    else:
-        roof = {"kernel": "tree_attn", "bound": "hbm", "achieved": a["bytes"] / (ams * 1e-3) / 1e9,
-                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = measured_traffic("tree_attn", w.name)
-    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json burst figure)"
-    roof["algorithmic_bytes"] = a["bytes"]
-    roof["algorithmic_flops"] = a["flops"]
+    kernels, roof = kernel_report(w, model, res["stage"], peaks)
+    ms_sum = sum(kernels[n]["ms"] for n in ("topk", "build", "tree_attn", "accept")
+                 if "ms" in kernels.get(n, {}))
     line = {"metric": METRIC,
             "value": value, "unit": "rounds/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": config_of(w, res["R"]), "roofline": roof, "kernels": kernels,
-            "kernel_timing": res["kern_method"], "gpu_launches": LAUNCHES_PER_ROUND * args.steps,
+            "config": config_of(w), "roofline": roof, "kernels": kernels,
+            "kernel_timing": STAGE_METHOD, "round_calls_ms_sum": ms_sum,
+            "input_copies": res["R"], "gpu_launches": LAUNCHES_PER_ROUND * args.steps,
             "clocks": res["clocks"], "e2e": res["e2e"]}
     if res["x36"]:
         line["rounds_per_s_x36_layers"] = res["x36"]["rounds_per_s"] * world

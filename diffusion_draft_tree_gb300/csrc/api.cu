@@ -19,7 +19,7 @@ std::mutex g_err_mu;
 // One error word per device; kernels record the first inconsistency they meet.
 static __device__ uint32_t g_ddtree_error_word;
 
-namespace {
+namespace ddt {
 
 // Device address of this device's error word (looked up once per device).
 uint32_t* error_word() {
@@ -33,6 +33,12 @@ uint32_t* error_word() {
     }
     return g_err_ptr[dev];
 }
+
+}  // namespace ddt
+
+namespace {
+
+using ddt::error_word;
 
 inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 // Every pointer of 4-byte elements (int32, uint32, float) on its grid; null
@@ -52,6 +58,10 @@ ddtree_status launched(cudaError_t e) {
 }
 
 }  // namespace
+
+namespace ddt {
+int launch_status(cudaError_t e) { return (int)launched(e); }
+}  // namespace ddt
 
 extern "C" {
 

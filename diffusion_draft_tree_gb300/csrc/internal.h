@@ -95,4 +95,12 @@ cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// ---- shared by the entry points (api.cu) --------------------------------------
+// Device address of the current device's error word (nullptr if the lookup
+// fails); kernels record the first inconsistency or timeout they meet there.
+uint32_t* error_word();
+// The ddtree_status for a CUDA result; a failure is remembered for
+// ddtree_last_cuda_error().
+int launch_status(cudaError_t e);
+
 }  // namespace ddt

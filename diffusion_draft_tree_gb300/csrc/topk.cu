@@ -163,7 +163,12 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, i
         if (tid == 0) s_cnt = 0;
         if (!Chunk::wait_ring(&s_bar[j % kStages], (uint32_t)((j / kStages) & 1))) {
             if (tid == 0) record_error(err, ERR_TOPK | ERR_WAIT_TIMEOUT);
-            return;  // a copy never landed
+            // A copy never landed.  Give every copy still in flight into this
+            // CTA's ring (chunks j .. j+kStages-1) one more bounded wait before
+            // the shared memory is released; then leave.
+            for (int jj = j; jj < min(nmine, j + kStages); ++jj)
+                Chunk::wait_ring(&s_bar[jj % kStages], (uint32_t)((jj / kStages) & 1));
+            return;
         }
         const uint4* vec = reinterpret_cast<const uint4*>(s_ring + (j % kStages) * Chunk::BYTES);
         const uint4* vw = vec + warp * VPW;
@@ -585,8 +590,11 @@ extern "C" ddtree_status ddtree_topk_noalloc(const void* draft_logits, int dtype
     if (need > DDTREE_NOALLOC_SCRATCH_BYTES) return DDTREE_ERR_UNSUPPORTED;
     void* scratch = nullptr;
     // (every partial the merge reads is written by the same call: no clearing)
-    if (need && noalloc_scratch(&scratch) != cudaSuccess) return DDTREE_ERR_CUDA;
+    if (need) {
+        const cudaError_t e = noalloc_scratch(&scratch);
+        if (e != cudaSuccess) return (ddtree_status)ddt::launch_status(e);
+    }
     ddt::TopkArgs a{draft_logits, dtype, rows, V, row_stride, K, topk_idx, topk_logp, lse,
-                    scratch, nullptr};
-    return ddt::launch_topk(a, (cudaStream_t)stream) == cudaSuccess ? DDTREE_OK : DDTREE_ERR_CUDA;
+                    scratch, ddt::error_word()};
+    return (ddtree_status)ddt::launch_status(ddt::launch_topk(a, (cudaStream_t)stream));
 }

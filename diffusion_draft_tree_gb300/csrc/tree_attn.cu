@@ -562,9 +562,13 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 __threadfence();
             }
             softmax_bar();
-            if (tid == 64)
-                s_last = all_ok && ticket_is_last(&p.tickets[(b * p.Hkv + g) * p.mpairs + mpair],
-                                                  (unsigned)splits);
+            if (tid == 64) {
+                // every split takes its ticket, also after a timeout, so that the
+                // counter returns to zero for the next call
+                const bool last = ticket_is_last(&p.tickets[(b * p.Hkv + g) * p.mpairs + mpair],
+                                                 (unsigned)splits);
+                s_last = all_ok && last;
+            }
             softmax_bar();
             if (s_last && mine) {
                 // out = sum_s w_s o_s / sum_s w_s, w_s = l_s 2^(m_s - M)

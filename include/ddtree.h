@@ -111,9 +111,11 @@ ddtree_status ddtree_topk(const void* draft_logits, int dtype, int rows, int V,
  * V = 151936 bf16 that is about 390 rows).
  * The first call made on a device looks up the array's device address on that
  * device (make it with the device current, before any stream capture).  Every
- * partial a call reads is written by that call, so nothing is cleared.  All
- * calls share the one array: calls whose kernels can overlap on the GPU (other
- * streams, other threads) race and give wrong results; serialise them. */
+ * partial a call reads is written by that call, so nothing is cleared; a
+ * kernel that could not write its partials (a bounded wait that timed out)
+ * records that in the device error word, which ddtree_device_check() reports.
+ * All calls share the one array: calls whose kernels can overlap on the GPU
+ * (other streams, other threads) race and give wrong results; serialise them. */
 ddtree_status ddtree_topk_noalloc(const void* draft_logits, int dtype, int rows, int V,
                                   int64_t row_stride, int K, int32_t* topk_idx,
                                   float* topk_logp, float* lse, void* stream);

@@ -155,6 +155,42 @@ def tree_attn(q, k_cache, v_cache, k_tree, v_tree, prefix_len, n_nodes, anc_mask
     return out, lse
 
 
+def tree_attn_tasks(q, k_cache, v_cache, k_tree, v_tree, prefix_len, n_nodes, anc_mask, tasks,
+                    threads: int = 1, scale=None):
+    """The same fp64 tree attention on a list of (b, kv_head, u_lo, u_hi) tasks
+    -- node rows [u_lo, u_hi) of one (sequence, KV head) unit -- run on
+    `threads` host threads at once (each call of the C routine releases the
+    interpreter lock; tasks write disjoint rows of one output).  Rows not in a
+    task stay NaN.  Returns (out, lse) as tree_attn does."""
+    import concurrent.futures
+    B, R, Hq, D = q.shape
+    Hkv, cap = k_cache.shape[1], k_cache.shape[2]
+    N = R - 1
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    out = np.full((B, R, Hq, D), np.nan, np.float64)
+    lse = np.full((B, R, Hq), np.nan, np.float64)
+    arrs = [np.ascontiguousarray(a) for a in (q, k_cache, v_cache, k_tree, v_tree)]
+    pl = np.ascontiguousarray(prefix_len, np.int32)
+    nn = np.ascontiguousarray(n_nodes, np.int32)
+    am = np.ascontiguousarray(anc_mask, np.uint32)
+    lib = _load()
+
+    def run(t):
+        b, g, lo, hi = t
+        return lib.ddo_tree_attn_unit(b, g, lo, hi, _p(arrs[0]), _p(arrs[1]), _p(arrs[2]), cap,
+                                      _p(arrs[3]), _p(arrs[4]), _p(pl), _p(nn), _p(am), B, N,
+                                      Hq, Hkv, D, scale, _p(out), _p(lse))
+
+    if threads <= 1:
+        rcs = [run(t) for t in tasks]
+    else:
+        with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as ex:
+            rcs = list(ex.map(run, tasks))
+    for rc in rcs:
+        _check(rc, "tree_attn")
+    return out, lse
+
+
 def philox4x64_10(counter, key) -> np.ndarray:
     """Philox4x64-10 block function (Salmon et al., SC'11)."""
     c = np.ascontiguousarray(counter, np.uint64)

@@ -25,8 +25,28 @@ def test_walk_policy():
 
 def test_config_names_the_walk():
     bench.WALK = "auto"
-    c = bench.config_of(wl.CONFIGS["ragged_serving"], None)
+    c = bench.config_of(wl.CONFIGS["ragged_serving"])
     assert c["workload"] == "ragged_serving" and c["walk"] == "path"
+    # both arms print this same dict: nothing in it depends on the arm
+    assert c == bench.config_of(wl.CONFIGS["ragged_serving"]) and "l2" in c
+
+
+def test_oracle_attention_sample():
+    """Small layers run in full as (sequence, KV head) units; large ones as a
+    seeded sample of node rows within the per-core budget, at least one row per
+    core, never past a sequence's tree."""
+    w = wl.CONFIGS["8b_single"]
+    tasks, done, total = bench.oracle_attn_tasks(w, [w.N], 8)
+    assert done == total and len(tasks) == w.Hkv and all(t[2:] == (0, w.N + 1) for t in tasks)
+    w = wl.CONFIGS["long_context_70b"]
+    n = [200, 256, 10, 0]
+    tasks, done, total = bench.oracle_attn_tasks(w, n, 4)
+    assert 4 <= len(tasks) and done <= 4 * bench.ORACLE_ROWS_PER_CORE + 8 * (131072 + 257)
+    assert total == sum(8 * (n[b] + 1) * 8 * (131072 + n[b] + 1) for b in range(4))
+    assert len(set(tasks)) == len(tasks)
+    for b, g, lo, hi in tasks:
+        assert 0 <= g < 8 and hi == lo + 1 and 0 <= lo <= n[b]
+    assert tasks == bench.oracle_attn_tasks(w, n, 4)[0]  # seeded
 
 
 def test_work_model_8b():
@@ -70,9 +90,13 @@ def test_reference_arm_line():
     assert line["metric"] == bench.METRIC
     assert line["unit"] == "rounds/s" and line["higher_is_better"] is True
     assert line["value"] > 0 and line["steps"] == 2 and line["warmup"] == 1
-    assert line["config"]["workload"] == "tiny"
+    assert line["config"] == bench.config_of(wl.CONFIGS["tiny"])
+    # value and ms_per_step are the measured steps
+    assert abs(line["value"] * line["ms_per_step"] / 1e3 - 1) < 1e-9  # B = 1
     cb = line["cpu_baseline"]
-    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["sample"] and cb["value"] == line["value"]
+    assert cb["kind"] == "oracle" and cb["cores"] == bench.host_cores() and cb["sample"]
+    assert cb["value"] == line["value"]
+    assert line["full_round_extrapolated"]["rounds_per_s"] > 0
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0

@@ -4,16 +4,18 @@ where cudaMalloc's implicit synchronisation is not allowed), so cannot hand
 the library a workspace.  The entry point uses a fixed scratch array built into
 the library instead.
 
-It must give the same answer as ddtree_topk (indices bit-exact, log-probs and
-logsumexp within the 1e-5 the other top-K tests use) on two calls in a row --
-the second with a different shape, so stale counters or partials left in the
-shared array by the first call would show.  This file is collected last."""
+It must give the oracle's answer (indices bit-exact, log-probs and logsumexp
+within the 1e-5 of fp64 that the other top-K tests use) and the same answer as
+ddtree_topk, on two calls in a row -- the second with a different shape, so
+stale partials left in the shared array by the first call would show -- and
+leave the device error word clear after each.  This file is collected last."""
 import ctypes
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from diffusion_draft_tree_gb300 import ops
 from diffusion_draft_tree_gb300 import workloads as wl
 from tests.gpu_util import dev_logits, host
@@ -51,17 +53,21 @@ def test_noalloc_topk_matches_workspace_topk_twice(cuda_device):
     cases = [(wl.draft_logits(first).reshape(first.B * first.L, first.V), first.dtype, first.K),
              (wl.draft_logits(second).reshape(second.B * second.L, second.V), second.dtype, 16)]
     for raw, dtype, K in cases:
+        o_idx, o_lp64, _, o_lse = oracle.topk(raw, dtype, K)
         x = dev_logits(raw, dtype, cuda_device)
         need = ops.workspace_size(ops.OP_TOPK, B=x.shape[0], L=1, V=x.shape[1], K=K,
                                   dtype=dtype)
         assert 0 < need <= SCRATCH_BYTES
-        ref_idx, ref_lp, ref_lse = ops.topk(x, K)
         idx, lp, lse = _call_noalloc(x, K)
-        torch.cuda.synchronize()
+        ops.ddtree_device_check()  # raises if a kernel recorded an error
+        np.testing.assert_array_equal(host(idx), o_idx)
+        assert np.abs(host(lp) - o_lp64).max() <= TOL
+        assert np.abs(host(lse) - o_lse).max() <= TOL
+        ref_idx, ref_lp, ref_lse = ops.topk(x, K)
+        ops.ddtree_device_check()
         np.testing.assert_array_equal(host(idx), host(ref_idx))
         assert np.abs(host(lp) - host(ref_lp)).max() <= TOL
         assert np.abs(host(lse) - host(ref_lse)).max() <= TOL
-    ops.ddtree_device_check()
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
