@@ -60,6 +60,12 @@ def parse():
     ap.add_argument("--profile-rounds", type=int, default=0,
                     help="only run this many eager rounds (rotating input copies) and exit; "
                          "for kernel profilers")
+    ap.add_argument("--profile-call", default=None,
+                    choices=["topk", "build", "tree_attn", "accept", "accept_path"],
+                    help="only run this one call of the round 3 times on the workload's inputs "
+                         "and exit; for kernel profilers (capture the second launch)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="with --profile-call: use the first BATCH sequences of the workload")
     return ap.parse_args()
 
 
@@ -822,6 +828,55 @@ def acceptance_stats(rounds: int) -> dict:
     return out
 
 
+def profile_call(call: str, workload: str, batch=None) -> dict:
+    """Runs one call of the round three times on the workload's inputs (the
+    tree from the library's own top-K and build), for a kernel profiler."""
+    import torch
+    from diffusion_draft_tree_gb300 import ops
+
+    w = wl.CONFIGS[workload]
+    if batch is not None:
+        w = w.with_(B=batch, P=tuple(w.P[:batch]))
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(
+        torch.bfloat16)
+    draft = wl.draft_logits(w)
+    d = to_dev_logits(draft.reshape(w.B * w.L, w.V), w.dtype, dev)
+    idx, lp, _ = ops.topk(d, w.K)
+    bonus, plen = i32(wl.bonus_tokens(w)), i32(wl.prefix_lengths(w))
+    tree = ops.build(lp.view(w.B, w.L, w.K), idx.view(w.B, w.L, w.K), bonus, plen, w.N)
+    torch.cuda.synchronize()
+    if call == "topk":
+        ws = ops.alloc_workspace(ops.workspace_size(ops.OP_TOPK, B=w.B, L=w.L, V=w.V, K=w.K,
+                                                    dtype=w.dtype), dev)
+        run = lambda: ops.topk(d, w.K, workspace=ws)
+    elif call == "build":
+        run = lambda: ops.build(lp.view(w.B, w.L, w.K), idx.view(w.B, w.L, w.K), bonus, plen, w.N)
+    elif call == "tree_attn":
+        q, kc, vc = bf(wl.queries(w)), bf(wl.kv_cache(w, 0)), bf(wl.kv_cache(w, 1))
+        kt, vt = bf(wl.kv_tree(w, 0)), bf(wl.kv_tree(w, 1))
+        ws = ops.alloc_workspace(ops.workspace_size(ops.OP_TREE_ATTN, B=w.B, N=w.N, Hq=w.Hq,
+                                                    Hkv=w.Hkv, D=w.D, cache_cap=w.P_cap), dev)
+        run = lambda: ops.tree_attn(q, kc, vc, kt, vt, plen, tree["n_nodes"], tree["anc_mask"],
+                                    workspace=ws)
+    else:
+        tgt = to_dev_logits(wl.target_logits(w, draft, tree["depth"].cpu().numpy()), w.dtype, dev)
+        ws = ops.alloc_workspace(ops.workspace_size(ops.OP_ACCEPT, B=w.B, N=w.N, V=w.V,
+                                                    dtype=w.dtype), dev)
+        if call == "accept":
+            run = lambda: ops.accept(tgt, tree, w.L, temperature=w.T, seed=wl.philox_seed(w),
+                                     workspace=ws)
+        else:
+            run = lambda: ops.accept_path(tgt, tree, w.L, temperature=w.T, seed=wl.philox_seed(w))
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    ops.ddtree_device_check()
+    return {"profile_call": call, "workload": w.name, "B": w.B}
+
+
 WALK = "auto"  # step 4 of the timed round (--walk)
 
 
@@ -910,6 +965,9 @@ def main():
     if args.acceptance_stats:
         if rank == 0:
             print(json.dumps(acceptance_stats(args.acceptance_stats)), flush=True)
+        return
+    if args.profile_call:
+        print(json.dumps(profile_call(args.profile_call, args.workload, args.batch)), flush=True)
         return
     import torch
     if world > 1:
