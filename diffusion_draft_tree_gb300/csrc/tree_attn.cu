@@ -44,6 +44,11 @@ constexpr int BN = 128;  // keys per KV tile
 constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
 constexpr int kHalfBytes = 128 * 128;  // [128 rows][64 bf16], one 128B-swizzled slab
 constexpr float kRescaleLog2 = 8.f;
+// Column of S_k's TMEM region that holds the bf16 P pairs of keys
+// [16 kk, 16 kk + 16): keys 0-95 over the first 48 columns in order, keys
+// 96-127 over columns 96-111 (the softmax writes that quarter first, from the
+// registers its maximum pass left it in, over its own scores).
+DDT_DEV uint32_t p_col(int kk) { return kk < 6 ? (uint32_t)(kk * 8) : (uint32_t)(96 + (kk - 6) * 8); }
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxSplits = 16;  // KV splits of one unit = CTAs of one cluster
 // How the KV splits of a unit combine: a single split stores directly; few
@@ -281,7 +286,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const uint32_t v_addr = smem_u32(sv + (j % NS) * C::KV_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_bf16_ts(tmem + 256 + k * D, tmem + k * BN + kk * 8,
+                    mma_bf16_ts(tmem + 256 + k * D, tmem + k * BN + p_col(kk),
                                 smem_desc_sw128(v_addr + kk * 2048, kHalfBytes, 1024), idesc_pv,
                                 (j > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&bar_odone[k]);
@@ -335,6 +340,20 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
         };
         if (nprefix < nt) fetch_mask(tree_first);
+        // O_k *= factor (the running maximum grew by more than 2^8)
+        auto rescale_o = [&](float factor) {
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t t[32];
+                tmem_ld32(tm_o + c * 32, t);
+                tmem_ld_wait();
+                tmem_ld_fence(t);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    t[i] = __float_as_uint(__uint_as_float(t[i]) * factor);
+                tmem_st32(tm_o + c * 32, t);
+            }
+        };
         float m_run = -INFINITY, l = 0.f;          // running max (scaled, log2), sum
         bool ok = true;
         for (int j = 0; mine && j < nt; ++j) {
@@ -360,6 +379,76 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 for (int c = 0; c < 4; ++c) vm[c] &= am[c];
                 if (j + 1 < nt) fetch_mask(tree_first + j + 1 - nprefix);
             }
+            float sum = 0.f;
+            if (full) {
+                // ---- a whole prefix tile: both passes read S_k in 32-column
+                // quarters, the next quarter's TMEM load in flight while the
+                // current one is used ----
+                uint32_t qa[32], qb[32];
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                auto qmax = [&](const uint32_t (&q)[32]) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(q[i]));
+                };
+                tmem_ld32(tm_s, qa);
+                tmem_ld_wait();
+                tmem_ld_fence(qa);
+                tmem_ld32(tm_s + 32, qb);
+                qmax(qa);
+                tmem_ld_wait();
+                tmem_ld_fence(qb);
+                tmem_ld32(tm_s + 64, qa);
+                qmax(qb);
+                tmem_ld_wait();
+                tmem_ld_fence(qa);
+                tmem_ld32(tm_s + 96, qb);
+                qmax(qa);
+                tmem_ld_wait();
+                tmem_ld_fence(qb);
+                qmax(qb);
+                const float mt_raw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                const float m_new = fmaxf(m_run, mt_raw * sl2);
+                const bool resc = m_new > m_run + kRescaleLog2;
+                const float m_use = resc ? m_new : m_run;
+                const float factor = resc ? fast_exp2(m_run - m_new) : 1.f;
+                // O_k is stable here: the commit that signalled S_k covers the
+                // previous tile's P_k V product.
+                if (j >= 1 && __any_sync(0xffffffffu, factor != 1.f)) rescale_o(factor);
+                l *= factor;
+                m_run = m_use;
+                // P = 2^(s*scale*log2e - m) as bf16 pairs: quarter c's 32 weights
+                // go to columns p_col(2c) .. +16 of S_k, whose scores are read
+                // before (the row sum takes the fp32 weights: their bf16 rounding
+                // averages out over a whole tile)
+                const float neg = (m_use == -INFINITY) ? 0.f : -m_use;
+                float2 acc = make_float2(0.f, 0.f);
+                auto qexp = [&](const uint32_t (&q)[32], int c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 y = ffma2(make_float2(__uint_as_float(q[2 * i]), __uint_as_float(q[2 * i + 1])), sl2, neg);
+                        const float2 e = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+                        pk[i] = pack_bf16x2(e.x, e.y);
+                        acc = fadd2(acc, e);
+                    }
+                    tmem_st16(tm_s + p_col(2 * c), pk);
+                };
+                // the last quarter is still in qb: first, while quarter 0 loads
+                tmem_ld32(tm_s, qa);
+                qexp(qb, 3);
+                tmem_ld_wait();
+                tmem_ld_fence(qa);
+                tmem_ld32(tm_s + 32, qb);
+                qexp(qa, 0);
+                tmem_ld_wait();
+                tmem_ld_fence(qb);
+                tmem_ld32(tm_s + 64, qa);
+                qexp(qb, 1);
+                tmem_ld_wait();
+                tmem_ld_fence(qa);
+                qexp(qa, 2);
+                sum = acc.x + acc.y;
+            } else {
             // ---- pass 1: row max, 64 columns per TMEM wait, four independent chains ----
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -368,13 +457,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tmem_ld32(tm_s + 32 * c0, t);
                 tmem_ld32(tm_s + 32 * c0 + 32, t2);
                 tmem_ld_wait();
-                if (full) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(t[i]));
-                        mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(t2[i]));
-                    }
-                } else {
+                {
                     const uint32_t m = vm[c0], m2 = vm[c0 + 1];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
@@ -390,65 +473,47 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const float factor = resc ? fast_exp2(m_run - m_new) : 1.f;
             // O_k is stable here: the commit that signalled S_k covers the
             // previous tile's P_k V product.
-            if (j >= 1 && __any_sync(0xffffffffu, factor != 1.f)) {
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t t[32];
-                    tmem_ld32(tm_o + c * 32, t);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        t[i] = __float_as_uint(__uint_as_float(t[i]) * factor);
-                    tmem_st32(tm_o + c * 32, t);
-                }
-            }
+            if (j >= 1 && __any_sync(0xffffffffu, factor != 1.f)) rescale_o(factor);
             l *= factor;
             m_run = m_use;
 
             // ---- pass 2: P = 2^(s*scale*log2e - m) as bf16 pairs, 64 columns at a
-            // time, written over the first half of those columns of S_k (the P
-            // columns of half h are [32h, 32h+32), all read before they are written)
+            // time, written at the P columns of those keys (p_col), whose scores
+            // are all read before they are written
             const float neg = (m_use == -INFINITY) ? 0.f : -m_use;
-            float sum = 0.f;
 #pragma unroll 1
             for (int half = 0; half < 2; ++half) {
                 uint32_t t0[32], t1[32], pk[32];
                 tmem_ld32(tm_s + half * 64, t0);
                 tmem_ld32(tm_s + half * 64 + 32, t1);
                 tmem_ld_wait();
-                if (full) {
-                    // Many keys: the row sum takes the fp32 weights (their bf16
-                    // rounding averages out over a whole tile).
-                    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+                // few keys (partial or tree tile): the row sum takes exactly the
+                // bf16 weights the P V product sees
+                const uint32_t m0 = half ? vm[2] : vm[0], m1 = half ? vm[3] : vm[1];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float2 y0 = ffma2(make_float2(__uint_as_float(t0[2 * i]), __uint_as_float(t0[2 * i + 1])), sl2, neg);
-                        const float2 y1 = ffma2(make_float2(__uint_as_float(t1[2 * i]), __uint_as_float(t1[2 * i + 1])), sl2, neg);
-                        const float2 e0 = make_float2(fast_exp2(y0.x), fast_exp2(y0.y));
-                        const float2 e1 = make_float2(fast_exp2(y1.x), fast_exp2(y1.y));
-                        pk[i] = pack_bf16x2(e0.x, e0.y);
-                        pk[16 + i] = pack_bf16x2(e1.x, e1.y);
-                        acc0 = fadd2(acc0, e0);
-                        acc1 = fadd2(acc1, e1);
-                    }
-                    sum += (acc0.x + acc0.y) + (acc1.x + acc1.y);
-                } else {
-                    // Few keys (partial or tree tile): the row sum takes exactly
-                    // the bf16 weights the P V product sees.
-                    const uint32_t m0 = half ? vm[2] : vm[0], m1 = half ? vm[3] : vm[1];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float a = ((m0 >> (2 * i)) & 1u) ? fast_exp2(fmaf(__uint_as_float(t0[2 * i]), sl2, neg)) : 0.f;
-                        const float bq = ((m0 >> (2 * i + 1)) & 1u) ? fast_exp2(fmaf(__uint_as_float(t0[2 * i + 1]), sl2, neg)) : 0.f;
-                        const float c = ((m1 >> (2 * i)) & 1u) ? fast_exp2(fmaf(__uint_as_float(t1[2 * i]), sl2, neg)) : 0.f;
-                        const float d = ((m1 >> (2 * i + 1)) & 1u) ? fast_exp2(fmaf(__uint_as_float(t1[2 * i + 1]), sl2, neg)) : 0.f;
-                        pk[i] = pack_bf16x2(a, bq);
-                        pk[16 + i] = pack_bf16x2(c, d);
-                        sum += (__uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u)) +
-                               (__uint_as_float(pk[16 + i] << 16) + __uint_as_float(pk[16 + i] & 0xffff0000u));
-                    }
+                for (int i = 0; i < 16; ++i) {
+                    const float a = ((m0 >> (2 * i)) & 1u) ? fast_exp2(fmaf(__uint_as_float(t0[2 * i]), sl2, neg)) : 0.f;
+                    const float bq = ((m0 >> (2 * i + 1)) & 1u) ? fast_exp2(fmaf(__uint_as_float(t0[2 * i + 1]), sl2, neg)) : 0.f;
+                    const float c = ((m1 >> (2 * i)) & 1u) ? fast_exp2(fmaf(__uint_as_float(t1[2 * i]), sl2, neg)) : 0.f;
+                    const float d = ((m1 >> (2 * i + 1)) & 1u) ? fast_exp2(fmaf(__uint_as_float(t1[2 * i + 1]), sl2, neg)) : 0.f;
+                    pk[i] = pack_bf16x2(a, bq);
+                    pk[16 + i] = pack_bf16x2(c, d);
+                    sum += (__uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u)) +
+                           (__uint_as_float(pk[16 + i] << 16) + __uint_as_float(pk[16 + i] & 0xffff0000u));
                 }
-                tmem_st32(tm_s + half * 32, pk);
+                if (half == 0) {
+                    tmem_st32(tm_s, pk);
+                } else {  // keys 64-95 and 96-127 at their P columns
+                    uint32_t lo[16], hi[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        lo[i] = pk[i];
+                        hi[i] = pk[16 + i];
+                    }
+                    tmem_st16(tm_s + p_col(4), lo);
+                    tmem_st16(tm_s + p_col(6), hi);
+                }
+            }
             }
             tmem_st_wait();
             l += sum;
