@@ -134,6 +134,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
     __shared__ bool s_last;
+    __shared__ float2 s_ml1[BM];  // lone tile: (m, l) of the second group's key halves
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -194,6 +195,11 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int u00 = mt0 * nodes_per_tile, u01 = mt1 * nodes_per_tile;
     const bool tile1 = mt1 < p.mtiles;          // the second tile exists
     const bool has1 = tile1 && (u01 <= n);      // ... and holds a live node
+    // The last query tile of an odd count (R G = 128 m + G r, e.g. N + 1 nodes with
+    // N a power of two) is alone: both softmax groups then work on it, each on
+    // one 64-key half of every key tile, and merge their (m, l, O) at the end.
+    const bool dual = !tile1;
+    const bool two = has1 || dual;              // two S / P / O groups in flight
     if (u00 > n) {  // every query row of both tiles is padding: zeros, once
         if (split == 0) {
             for (int r = tid; r < 2 * BM; r += kThreads) {
@@ -269,26 +275,32 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // =========================== MMA issuer =============================
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0, 0);
+            constexpr uint32_t idesc_qk_half = idesc_bf16_f32(BM, BN / 2, 0, 0);
+            constexpr uint32_t kHalfRows = (BN / 2) * 128;  // bytes of 64 key rows in a slab
             constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, 0, 1);
             const uint32_t q_addr = smem_u32(sq);
             auto qk = [&](int j, int k) {
-                const uint32_t k_addr = smem_u32(sk + (j % NS) * C::KV_BYTES);
-                const uint32_t qa = q_addr + k * C::QT_BYTES;
+                // dual: query tile 0 against keys [64k, 64k + 64) of the tile
+                const uint32_t k_addr = smem_u32(sk + (j % NS) * C::KV_BYTES) + (dual ? k * kHalfRows : 0u);
+                const uint32_t qa = q_addr + (dual ? 0u : k * C::QT_BYTES);
+                const uint32_t idesc = dual ? idesc_qk_half : idesc_qk;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
                     mma_bf16_ss(tmem + k * BN, smem_desc_sw128(qa + off, 16, 1024),
-                                smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0);
+                                smem_desc_sw128(k_addr + off, 16, 1024), idesc, kk > 0);
                 }
                 mma_commit(&bar_sfull[k]);
             };
             auto pv = [&](int j, int k) {
-                const uint32_t v_addr = smem_u32(sv + (j % NS) * C::KV_BYTES);
+                const uint32_t v_addr = smem_u32(sv + (j % NS) * C::KV_BYTES) + (dual ? k * kHalfRows : 0u);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    if (dual && kk >= BN / 32) break;  // 64 keys: P columns [0, 32)
                     mma_bf16_ts(tmem + 256 + k * D, tmem + k * BN + p_col(kk),
                                 smem_desc_sw128(v_addr + kk * 2048, kHalfBytes, 1024), idesc_pv,
                                 (j > 0 || kk > 0) ? 1u : 0u);
+                }
                 mma_commit(&bar_odone[k]);
             };
             bool ok = mbar_wait(&bar_q, 0, &s_abort) && mbar_wait(&bar_full[0], 0, &s_abort);
@@ -296,7 +308,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (ok) {
                 tc_fence_after();
                 qk(0, 0);
-                if (has1) qk(0, 1);
+                if (two) qk(0, 1);
             }
             for (int j = 0; ok && j < nt; ++j) {
                 if (!mbar_wait(&bar_pfull[0], j & 1, &s_abort)) { fail(); break; }
@@ -307,13 +319,13 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     tc_fence_after();
                     qk(j + 1, 0);  // issued after pv(j, 0): reuses S_0/P_0 in order
                 }
-                if (has1) {
+                if (two) {
                     if (!mbar_wait(&bar_pfull[1], j & 1, &s_abort)) { fail(); break; }
                     tc_fence_after();
                     pv(j, 1);
                 }
                 mma_commit(&bar_empty[j % NS]);
-                if (has1 && j + 1 < nt) qk(j + 1, 1);
+                if (two && j + 1 < nt) qk(j + 1, 1);
             }
         }
     } else {
@@ -324,10 +336,13 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tm_s = tmem + lane_off + k * BN;
         const uint32_t tm_o = tmem + lane_off + 256 + k * D;
-        const bool mine = (k == 0) || has1;        // this group has work
-        const int u = (k == 0 ? u00 : u01) + r / G;
+        const bool mine = (k == 0) || has1;        // this group owns a query tile
+        const bool work = mine || dual;            // ... or half of tile 0's keys
+        const int key0 = dual ? k * (BN / 2) : 0;  // first key of the group's columns
+        const int ncol = dual ? BN / 2 : BN;       // keys per tile of the group
+        const int u = (k == 0 || dual ? u00 : u01) + r / G;
         const int hh = g * G + r % G;
-        const bool row_valid = mine && (u <= n);
+        const bool row_valid = work && (u <= n);
         const float sl2 = p.scale_log2;
         // ancestor words of this row for the next tree tile, fetched one tile ahead
         uint32_t am[4] = {0u, 0u, 0u, 0u};
@@ -356,7 +371,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         };
         float m_run = -INFINITY, l = 0.f;          // running max (scaled, log2), sum
         bool ok = true;
-        for (int j = 0; mine && j < nt; ++j) {
+        for (int j = 0; work && j < nt; ++j) {
             const int s = j % NS;
             if (!mbar_wait(&bar_sfull[k], j & 1, &s_abort)) { fail(); ok = false; break; }
             tc_fence_after();
@@ -365,9 +380,10 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // below the prefix length; a tree tile the row's ancestor bits)
             const bool is_tree = (j >= nprefix);
             const int a0 = (tree_first + j - nprefix) * BN;
-            const int lim = is_tree ? (n + 1 - a0) : (P - (t_begin + j) * BN);
-            const bool key_r_valid = r < lim;
-            const bool full = !is_tree && lim >= BN;
+            const int lim_t = is_tree ? (n + 1 - a0) : (P - (t_begin + j) * BN);
+            const bool key_r_valid = r < lim_t;
+            const int lim = lim_t - key0;  // valid keys among the group's columns
+            const bool full = !is_tree && lim >= ncol;
             uint32_t vm[4];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -375,8 +391,9 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 vm[c] = rem >= 32 ? ~0u : (rem <= 0 ? 0u : ((1u << rem) - 1u));
             }
             if (is_tree) {
+                const bool hi = dual && k == 1;  // keys 64-127: ancestor words 2, 3
 #pragma unroll
-                for (int c = 0; c < 4; ++c) vm[c] &= am[c];
+                for (int c = 0; c < 4; ++c) vm[c] &= (c < 2 && hi) ? am[c + 2] : am[c];
                 if (j + 1 < nt) fetch_mask(tree_first + j + 1 - nprefix);
             }
             float sum = 0.f;
@@ -397,14 +414,16 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 qmax(qa);
                 tmem_ld_wait();
                 tmem_ld_fence(qb);
-                tmem_ld32(tm_s + 64, qa);
-                qmax(qb);
-                tmem_ld_wait();
-                tmem_ld_fence(qa);
-                tmem_ld32(tm_s + 96, qb);
-                qmax(qa);
-                tmem_ld_wait();
-                tmem_ld_fence(qb);
+                if (!dual) {
+                    tmem_ld32(tm_s + 64, qa);
+                    qmax(qb);
+                    tmem_ld_wait();
+                    tmem_ld_fence(qa);
+                    tmem_ld32(tm_s + 96, qb);
+                    qmax(qa);
+                    tmem_ld_wait();
+                    tmem_ld_fence(qb);
+                }
                 qmax(qb);
                 const float mt_raw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
                 const float m_new = fmaxf(m_run, mt_raw * sl2);
@@ -433,6 +452,10 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                     tmem_st16(tm_s + p_col(2 * c), pk);
                 };
+                if (dual) {  // both quarters are still in registers
+                    qexp(qb, 1);
+                    qexp(qa, 0);
+                } else {
                 // the last quarter is still in qb: first, while quarter 0 loads
                 tmem_ld32(tm_s, qa);
                 qexp(qb, 3);
@@ -447,6 +470,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tmem_ld_wait();
                 tmem_ld_fence(qa);
                 qexp(qa, 2);
+                }
                 sum = acc.x + acc.y;
             } else {
             // ---- pass 1: row max, 64 columns per TMEM wait, four independent chains ----
@@ -482,7 +506,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // are all read before they are written
             const float neg = (m_use == -INFINITY) ? 0.f : -m_use;
 #pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
+            for (int half = 0; half < (dual ? 1 : 2); ++half) {
                 uint32_t t0[32], t1[32], pk[32];
                 tmem_ld32(tm_s + half * 64, t0);
                 tmem_ld32(tm_s + half * 64 + 32, t1);
@@ -534,10 +558,35 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
 
         // ---- epilogue (every softmax thread runs the same barrier sequence) ----
-        if (mine && ok && !mbar_wait(&bar_odone[k], (nt - 1) & 1, &s_abort)) { fail(); ok = false; }
+        if (work && ok && !mbar_wait(&bar_odone[k], (nt - 1) & 1, &s_abort)) { fail(); ok = false; }
+        if (dual && k == 1) s_ml1[r] = make_float2(m_run, l);
         const bool all_ok = softmax_bar_and(ok);
         const bool have = all_ok && mine;          // warp-uniform
         tc_fence_after();
+        if (dual && have) {
+            // fold the second group's keys into O_0: O = w0 O_0 + w1 O_1,
+            // l = w0 l_0 + w1 l_1, w_k = 2^(m_k - M), 0 for a group without keys
+            // (both 0 for a row without keys).  No per-row branch: the TMEM loads
+            // and stores are warp-collective.
+            const float2 ml1 = s_ml1[r];
+            const float M = fmaxf(m_run, ml1.x);
+            const float w0 = m_run == -INFINITY ? 0.f : fast_exp2(m_run - M);
+            const float w1 = ml1.x == -INFINITY ? 0.f : fast_exp2(ml1.x - M);
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t t0[32], t1[32];
+                tmem_ld32(tm_o + c * 32, t0);
+                tmem_ld32(tm_o + D + c * 32, t1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    t0[i] = __float_as_uint(w0 * __uint_as_float(t0[i]) + w1 * __uint_as_float(t1[i]));
+                tmem_st32(tm_o + c * 32, t0);
+            }
+            tmem_st_wait();
+            l = w0 * l + w1 * ml1.y;
+            m_run = M;
+        }
         const bool row_out = (k == 0 || tile1) && u < R;
         uint4* dst = (uint4*)(p.out + (((size_t)b * R + u) * p.Hq + hh) * D);
         // writes 32 output columns of this row, scaled by inv
