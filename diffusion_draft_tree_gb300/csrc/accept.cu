@@ -59,22 +59,6 @@ struct AcceptWs {
 };
 
 
-DDT_DEV unsigned int ld_acquire_u32(const unsigned int* p) {
-    unsigned int v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-DDT_DEV unsigned int atom_add_acq_rel_u32(unsigned int* p, unsigned int v) {
-    unsigned int old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-DDT_DEV unsigned int atom_or_acq_rel_u32(unsigned int* p, unsigned int v) {
-    unsigned int old;
-    asm volatile("atom.acq_rel.gpu.global.or.b32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-
 DDT_DEV double shfl_up_f64(double v, int o) {
     return __longlong_as_double(
         (long long)__shfl_up_sync(0xffffffffu, (unsigned long long)__double_as_longlong(v), o));

@@ -129,6 +129,24 @@ DDT_DEV bool ticket_is_last(unsigned int* counter, unsigned int expected) {
     return last;
 }
 
+// Acquire / release accesses at GPU scope, for counters that hand partial
+// results from one CTA to another.
+DDT_DEV unsigned int ld_acquire_u32(const unsigned int* p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+DDT_DEV unsigned int atom_add_acq_rel_u32(unsigned int* p, unsigned int v) {
+    unsigned int old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+DDT_DEV unsigned int atom_or_acq_rel_u32(unsigned int* p, unsigned int v) {
+    unsigned int old;
+    asm volatile("atom.acq_rel.gpu.global.or.b32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // Two floats rounded to a bf16 pair (lo in the low half).
 DDT_DEV uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;

@@ -21,7 +21,6 @@ struct TopkArgs {
     void* ws;
     uint32_t* err;
 };
-int topk_chunks(int V, int dtype);
 bool topk_supported(int V, int dtype, int K);
 size_t topk_workspace_bytes(int rows, int V, int dtype, int K);  // K <= 0: any K
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);

@@ -33,6 +33,31 @@ struct Seg {
         return fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
                      fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
     }
+    // element k of a vector, k known only at run time
+    DDT_DEV static float elem_dyn(const uint4& w, int k) {
+        if (BF16) {
+            const uint32_t h = (k < 4) ? ((k < 2) ? w.x : w.y) : ((k < 6) ? w.z : w.w);
+            return (k & 1) ? bf16hi(h) : bf16lo(h);
+        }
+        return __uint_as_float((k < 2) ? ((k == 0) ? w.x : w.y) : ((k == 2) ? w.z : w.w));
+    }
+    // bit k set where element k >= t (t a value of the element type, so that the
+    // bf16 comparison is exact; NaN compares false)
+    DDT_DEV static unsigned ge_mask(const uint4& w, float t) {
+        if (BF16) {
+            const __nv_bfloat162 t2 = __bfloat162bfloat162(__float2bfloat16_rn(t));
+            const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+            unsigned m = 0u;
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const unsigned h = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&a[p]), t2);
+                m |= ((h & 1u) | ((h >> 15) & 2u)) << (2 * p);
+            }
+            return m;
+        }
+        return (__uint_as_float(w.x) >= t ? 1u : 0u) | (__uint_as_float(w.y) >= t ? 2u : 0u) |
+               (__uint_as_float(w.z) >= t ? 4u : 0u) | (__uint_as_float(w.w) >= t ? 8u : 0u);
+    }
     // acc += 2^(x c + off) over the vector's elements, two lanes per fp32x2
     // instruction (acc.x and acc.y are two independent partial sums)
     DDT_DEV static void exp_sum2(const uint4& w, float c, float off, float2& acc) {

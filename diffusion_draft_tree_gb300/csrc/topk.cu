@@ -3,28 +3,33 @@
 // Draft Trees", §3 marginals q_i; §4.3 log-probabilities; App. A restricted
 // prefix set).
 //
-// One row = one (sequence, draft position), V logits, split into chunks (32 KB
-// = 16384 bf16 or 8192 fp32 logits; 16 KB when that many chunks still fit in
-// one wave).  A persistent wave of CTAs streams the (row, chunk) list, each
-// CTA a contiguous run of chunks through a ring of shared-memory stages
-// filled by bulk copies a few chunks ahead, so HBM is read once and stays
-// busy.  Per chunk, each warp makes one pass over its eighth in shared memory:
-// every vector's maximum, and each lane's online (max, sum of exponentials).
-// The chunk's K best keys need no sort here: every warp sorts the few vector
-// maxima of its slice above its K-th largest lane maximum and publishes its K
-// largest; tau, the K-th largest of those lists, is the K-th largest vector
-// maximum of the chunk -- K distinct elements are >= it -- so the chunk keeps
-// only its (value, index) keys >= tau (usually K to 1.5K), together with its
-// (m, s) and tau.  Any chunk's tau bounds its row's K-th largest from below,
-// so a CTA's later chunks of a row it has already met skip the sorts: they
-// keep their keys >= the bound found so far and report it as their tau.  A
-// second, PDL-chained kernel (one CTA per row) bounds the row's K-th largest
-// by the largest chunk tau, ranks the kept keys above it by counting, and
-// forms the logsumexp.
+// One row = one (sequence, draft position), V logits, cut into 4 KB segments.
+// The flattened (row, segment) list is split into equal chunks, one per warp
+// of a single wave (at least (nseg - 1)/31 segments each, so that a row has at
+// most 32 pieces).  A warp streams its chunk through a private ring of shared-memory
+// stages filled by bulk copies two segments ahead (no CTA barrier anywhere), and
+// keeps, for the piece of a row it is in:
+//   - each lane's online (max, sum of exponentials);
+//   - the piece's K best (value, index) keys, as a sorted list in shared memory
+//     followed by new candidates.  A candidate must beat the list's K-th key;
+//     vectors whose maximum is below it are skipped whole.  Before the list is
+//     full, the K-th largest lane maximum bounds the segment's K-th value from
+//     below (K distinct elements reach it).  Ranking by counting merges
+//     candidates into the list when the buffer fills, after the piece's first
+//     segment and at the piece's end.
+// A piece whose list fills raises a bound shared by the row's pieces (a key
+// that K elements of the row reach), which every piece then filters against.
+// At the end of a piece the warp publishes (max, sum) and its K keys, and takes
+// the row's ticket; the warp that completes the row merges its pieces: the
+// logsumexp from the (max, sum) pairs, the K best by a K-round tournament over
+// the pieces' sorted lists (one lane per piece), and leaves the row's counter,
+// bound and slots at zero (the workspace is all zero again after a call).
+#include <algorithm>
 #include <mutex>
 
-#include "chunk.cuh"
 #include "internal.h"
+#include "segment.cuh"
+#include "warp_ring.cuh"
 
 #include "../../include/ddtree.h"
 
@@ -32,30 +37,17 @@ namespace ddt {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-// Chunks are 32 KB when there are enough to keep every CTA streaming, else
-// 16 KB (twice the CTAs, half the work per warp: lower latency).
-constexpr int kChunkBig = 32768, kChunkSmall = 16384;
-constexpr int kMaxChunks = 128;  // per row, at the small size
-constexpr int kStages = 3;       // chunks in flight per CTA
-constexpr int kCtasPerSm = 2;
-constexpr int kMergeCand = 1024; // candidates the merge gathers before its slow path
-
-// Warp-wide bitonic sort of one uint32 per lane, descending (lane 0 largest).
-DDT_DEV uint32_t warp_sort_desc_u32(uint32_t v) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            const uint32_t o = __shfl_xor_sync(0xffffffffu, v, j);
-            const bool keep_max = (((lane & k) == 0) == ((lane & j) == 0));
-            v = keep_max ? max(v, o) : min(v, o);
-        }
-    }
-    return v;
-}
+constexpr int kSegBytes = 4096;
+constexpr int kStages = 3;
+constexpr int kRingBytes = kWarps * kStages * kSegBytes;  // 192 KB
+constexpr int kSmemBytes = kRingBytes + 128;              // + alignment slack
+constexpr int kCap = 96;            // a warp's sorted list (first n) + candidates
+constexpr int kMaxPieces = 32;      // pieces of one row (one per merging lane)
+constexpr int kMaxGridWarps = 2560; // warps of the wave (160 SMs), for the workspace bound
+constexpr int kMaxV = 1 << 24;      // logits per row (element ids and segment counts fit)
+constexpr int kMergeHeads = 8;      // a merging lane's keys held in registers
 
 // Merges (m, s) pairs: s2 rescaled to the larger maximum (exp base 2^(x c)).
 DDT_DEV void ms_combine(float& m, float& s, float m2, float s2, float c) {
@@ -65,395 +57,404 @@ DDT_DEV void ms_combine(float& m, float& s, float m2, float s2, float c) {
     m = mx;
 }
 
-// Per chunk, the streaming kernel leaves its (m, s), a bound tau on its K-th
-// largest value (as an order key) and every key >= tau -- usually K to 2K of
-// them, at most kChunkCand; a chunk with more (degenerate ties) keeps exactly
-// its K best, sorted, and sets tau to the K-th.
-constexpr int kChunkCand = 64;
-struct ChunkOut {
-    float m, s;       // max, sum exp(x - m)
-    uint32_t tau;     // ord key: the chunk has >= K elements >= it
-    int count;        // keys below
-    uint64_t keys[kChunkCand];
+// A warp's K best keys of the current piece: buf[0, n) sorted descending (the
+// list), buf[n, n + cc) unsorted candidates; tkey = the list's K-th key once it
+// is full (0 before: every key is larger); rb = a bound on the row's K-th key
+// found by any piece of the row.  Keys <= bound() are out.  Every member is
+// warp-uniform.
+struct KBest {
+    uint64_t* buf;  // kCap keys, 16-byte aligned, this warp's alone
+    int K, n, cc;
+    uint64_t tkey, rb;
+
+    DDT_DEV uint64_t bound() const { return tkey > rb ? tkey : rb; }
+    DDT_DEV void reset() {
+        n = 0;
+        cc = 0;
+        tkey = 0ull;
+        rb = 0ull;
+    }
+    // The K largest of list + candidates, sorted, into the list (rank by
+    // counting: the keys are distinct, so the ranks are).
+    DDT_DEV void reduce() {
+        const int lane = threadIdx.x & 31;
+        const int t = n + cc;
+        __syncwarp();
+        const uint64_t k0 = lane < t ? buf[lane] : 0ull;
+        const uint64_t k1 = lane + 32 < t ? buf[lane + 32] : 0ull;
+        const uint64_t k2 = lane + 64 < t ? buf[lane + 64] : 0ull;
+        const int r0 = lane < t ? count_larger(buf, t, k0) : kCap;
+        const int r1 = lane + 32 < t ? count_larger(buf, t, k1) : kCap;
+        const int r2 = lane + 64 < t ? count_larger(buf, t, k2) : kCap;
+        __syncwarp();
+        if (r0 < K) buf[r0] = k0;
+        if (r1 < K) buf[r1] = k1;
+        if (r2 < K) buf[r2] = k2;
+        __syncwarp();
+        n = min(K, t);
+        cc = 0;
+        tkey = n == K ? buf[K - 1] : 0ull;
+    }
+    // Appends `key` of every lane where c holds (warp-collective); makes room
+    // first if the buffer could overflow, and then re-tests c against the
+    // raised K-th key.
+    DDT_DEV void push(bool c, uint64_t key) {
+        const int lane = threadIdx.x & 31;
+        unsigned b = __ballot_sync(0xffffffffu, c);
+        if (!b) return;
+        if (n + cc + __popc(b) > kCap) {
+            reduce();
+            c = c && key > bound();
+            b = __ballot_sync(0xffffffffu, c);
+        }
+        if (c) buf[n + cc + __popc(b & ((1u << lane) - 1u))] = key;
+        cc += __popc(b);
+    }
 };
 
-// Exact K best keys of a chunk by K rounds of a CTA-wide maximum below the
-// previous one (all threads call it; correctness only, kept out of line).
-// Thread 0 writes them to out->keys.
-template <typename Chunk>
-__device__ __noinline__ void cta_exact_top_k(const uint4* vec, int c0, int V, int K,
-                                             uint64_t* s_red, ChunkOut* out) {
-    constexpr int VEC = Chunk::VEC;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint64_t prev = ~0ull;
-    for (int r = 0; r < K; ++r) {
-        uint64_t tb = 0ull;
-#pragma unroll 1
-        for (int v = tid; v < Chunk::NVEC; v += kThreads) {
-            float x[VEC];
-            Chunk::unpack(vec[v], x);
-            for (int k = 0; k < VEC; ++k) {
-                const int e = c0 + v * VEC + k;
-                if (e < V) {
-                    const uint64_t key = value_index_key(x[k], (uint32_t)e);
-                    if (key < prev && key > tb) tb = key;
-                }
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) tb = umax64(tb, shfl_xor_u64(tb, o));
-        if (lane == 0) s_red[warp] = tb;
-        __syncthreads();
-        tb = s_red[0];
-        for (int i = 1; i < kWarps; ++i) tb = umax64(tb, s_red[i]);
-        if (tid == 0) out->keys[r] = tb;
-        prev = tb;
-        __syncthreads();
-    }
-    if (tid == 0) {
-        out->count = K;
-        out->tau = (uint32_t)(prev >> 32);
-    }
-}
+// Workspace: per row a completion counter and a shared bound; per piece slot (chunk c's piece of
+// row r sits at slot c + r) the piece's (max, sum) as a float2 followed by its
+// K keys (0 past the piece's element count).
+struct TopkWs {
+    unsigned int* row_cnt;         // [rows]
+    unsigned long long* row_tau;   // [rows] largest piece K-th key so far (0: none)
+    uint64_t* slots;               // [nslots][1 + K]
+};
 
-// Persistent: CTA i handles chunks [i per, (i+1) per) of the flattened
-// (row, chunk) list, streaming them through a ring of kStages shared-memory
-// stages (bulk copies issued kStages-1 chunks ahead), and writes one ChunkOut
-// per chunk.  Warps own eighths of the chunk until the chunk's tau is known.
-template <bool BF16, int CHUNK_BYTES>
-__global__ void __launch_bounds__(kThreads)
-topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int K, int nchunks,
-            bool aligned, int total, int per, ChunkOut* __restrict__ outs, uint32_t* err) {
-    using Chunk = SmemChunk<BF16, CHUNK_BYTES / (BF16 ? 2 : 4)>;
-    constexpr int VEC = Chunk::VEC;
-    constexpr int VPW = Chunk::NVEC / kWarps;  // vectors per warp
-    constexpr int PL = VPW / 32;               // vectors per lane
-    extern __shared__ __align__(128) uint8_t s_ring[];  // kStages x Chunk::BYTES
-    __shared__ __align__(8) uint64_t s_bar[kStages];
-    __shared__ float2 s_wms[kWarps];
-    __shared__ uint64_t s_red[kWarps];
-    __shared__ int16_t s_vlist[kWarps][Chunk::NVEC / kWarps];  // passing vector ids per warp
-    __shared__ uint32_t s_vm[kWarps][32];                      // a warp's top vector maxima
-    __shared__ int s_cnt;
+struct Cur {  // a warp's position: chunk c, flattened segment i of [., iend)
+    long c, i, iend;
+    int row, seg;
+};
+
+// One wave: warp w of CTA b streams chunks w grid + b + k nw, k = 0, 1, ...
+// (spc segments each; the plan makes at most one per warp).
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int rows, int nseg,
+            long spc, bool aligned, int K, TopkWs ws, int32_t* __restrict__ topk_idx,
+            float* __restrict__ topk_logp, float* __restrict__ lse, uint32_t* err) {
+    using S = Seg<BF16, kSegBytes>;
+    using Ring = WarpRing<BF16, kSegBytes, kStages>;
+    constexpr int VEC = S::VEC;
+    constexpr int VPL = Ring::VPL;  // vectors per lane per segment
+    extern __shared__ __align__(128) uint8_t smem_raw[];  // the warps' rings
+    __shared__ __align__(8) uint64_t s_bar[kWarps][kStages];
+    __shared__ __align__(16) uint64_t s_buf[kWarps][kCap];
+    __shared__ int s_cc[kWarps];  // a warp's next free buffer place (fast path)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int w0 = blockIdx.x * per;
-    const int nmine = min(total, w0 + per) - w0;
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) sm100::mbar_init(&s_bar[s], 1);
-        sm100::mbar_init_fence();
-    }
-    __syncthreads();
+    const long total = (long)rows * nseg;
+    const long nchunks = (total + spc - 1) / spc;
+    const long nw = (long)gridDim.x * kWarps;
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
+    Ring ring{smem + warp * kStages * kSegBytes, s_bar[warp]};
+    ring.init();
+    KBest kb{s_buf[warp], K, 0, 0, 0ull, 0ull};
     pdl_wait();
-    auto issue = [&](int j) {  // chunk j of this CTA into stage j % kStages
-        const int w = w0 + j, row = w / nchunks, chunk = w - row * nchunks;
-        Chunk::issue_ring(s_ring + (j % kStages) * Chunk::BYTES, &s_bar[j % kStages],
-                          (const char*)logits + (size_t)row * (size_t)row_stride * Chunk::ES,
-                          chunk * Chunk::SIZE, V, aligned);
-    };
-    for (int j = 0; j < kStages - 1 && j < nmine; ++j) issue(j);
-    uint32_t tau_run = 0u;  // a bound <= the current row's K-th largest (0: none yet)
-    for (int j = 0; j < nmine; ++j) {
-        if (j + kStages - 1 < nmine) issue(j + kStages - 1);  // into the stage freed last step
-        if (j == nmine - 1) pdl_trigger();
-        const int w = w0 + j;
-        const int c0 = (w % nchunks) * Chunk::SIZE;
-        if (c0 == 0) tau_run = 0u;  // a new row
-        ChunkOut* out = outs + w;
-        if (tid == 0) s_cnt = 0;
-        if (!Chunk::wait_ring(&s_bar[j % kStages], (uint32_t)((j / kStages) & 1))) {
-            if (tid == 0) record_error(err, ERR_TOPK | ERR_WAIT_TIMEOUT);
-            // A copy never landed.  Give every copy still in flight into this
-            // CTA's ring (chunks j .. j+kStages-1) one more bounded wait before
-            // the shared memory is released; then leave.
-            for (int jj = j; jj < min(nmine, j + kStages); ++jj)
-                Chunk::wait_ring(&s_bar[jj % kStages], (uint32_t)((jj / kStages) & 1));
-            return;
-        }
-        const uint4* vec = reinterpret_cast<const uint4*>(s_ring + (j % kStages) * Chunk::BYTES);
-        const uint4* vw = vec + warp * VPW;
-        const int e_lane = c0 + (warp * VPW + lane) * VEC;  // first element of the lane
 
-        // ---- one pass: vector maxima, and the lane's online (max, sum of exps) ----
-        float vmx[PL];
-        float mt = -INFINITY, a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int i = 0; i < PL; ++i) {
-            const uint4 v = vw[lane + 32 * i];
-            const float vm = Chunk::vmax(v);
-            vmx[i] = vm;
-            if (vm > mt) {
-                const float f = fast_exp2((mt - vm) * kLog2e);  // 0 while mt = -inf
-                a0 *= f;
-                a1 *= f;
-                mt = vm;
+    auto place = [&](Cur& x) -> bool {  // x.c set: its first segment
+        if (x.c >= nchunks) return false;
+        x.i = x.c * spc;
+        x.iend = min(total, x.i + spc);
+        x.row = (int)(x.i / nseg);
+        x.seg = (int)(x.i - (long)x.row * nseg);
+        return true;
+    };
+    auto next = [&](Cur& x) -> bool {
+        if (++x.i < x.iend) {
+            if (++x.seg == nseg) {
+                ++x.row;
+                x.seg = 0;
             }
-            if (mt != -INFINITY) Chunk::exp_sum(v, kLog2e, -mt * kLog2e, a0, a1);
+            return true;
         }
-        float m_w = mt, s_w = a0 + a1;
+        x.c += nw;
+        return place(x);
+    };
+    // chunks that hold a piece of the row (at most kMaxPieces by the plan)
+    auto pieces = [&](int row) -> int {
+        return (int)(((long)(row + 1) * nseg - 1) / spc - ((long)row * nseg) / spc + 1);
+    };
+    auto rowp_of = [&](int row) {
+        return (const char*)logits + (size_t)row * (size_t)row_stride * S::ES;
+    };
+    // The row's result, by the warp that completed it (its count was acquired,
+    // so every piece's slot is visible).  Lane p holds piece p's (max, sum) and
+    // its sorted keys, kMergeHeads at a time in registers; K rounds of a
+    // tournament take the largest head (the value word, then the index word,
+    // each by one warp reduction), and the winning lane moves to its next key.
+    // Every key of the row's K best is in its piece's list, so the K winners are
+    // the row's K best, in order.
+    auto merge = [&](int row) {
+        const long c_lo = ((long)row * nseg) / spc;
+        const int np = pieces(row);
+        uint64_t* base = ws.slots + (size_t)(c_lo + row) * (size_t)(1 + K);
+        const uint64_t* mine = base + (size_t)lane * (1 + K);
+        float pm = -INFINITY, ps = 0.f;
+        uint64_t hk[kMergeHeads];
+#pragma unroll
+        for (int i = 0; i < kMergeHeads; ++i)
+            hk[i] = (lane < np && i < K) ? __ldcg((const unsigned long long*)mine + 1 + i) : 0ull;
+        if (lane < np) {
+            const float2 h = __ldcg(reinterpret_cast<const float2*>(mine));
+            pm = h.x;
+            ps = h.y;
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            const float mo = __shfl_xor_sync(0xffffffffu, m_w, o);
-            const float so = __shfl_xor_sync(0xffffffffu, s_w, o);
-            ms_combine(m_w, s_w, mo, so, kLog2e);
+            const float mo = __shfl_xor_sync(0xffffffffu, pm, o);
+            const float so = __shfl_xor_sync(0xffffffffu, ps, o);
+            ms_combine(pm, ps, mo, so, kLog2e);
         }
-        if (lane == 0) s_wms[warp] = make_float2(m_w, s_w);
-
-        // The chunk's keys >= tv, from the vectors whose maximum reaches it: their
-        // ids are compacted per warp first (a ballot per vector row), so each
-        // passing vector is unpacked by one lane instead of the whole warp
-        // stepping through every row in which any lane passes.  Counts them in
-        // s_cnt; stores the first kChunkCand.
-        auto gather = [&](float tv) {
-            int nv = 0;
+        const float M = (pm == -INFINITY) ? 0.f : pm;
+        const float logS = logf(ps);
+        int used = 0;  // keys of this lane's piece taken so far
+        for (int r = 0; r < K; ++r) {
+            const uint32_t vw = (uint32_t)(hk[0] >> 32);
+            const uint32_t vmax = __reduce_max_sync(0xffffffffu, vw);
+            const uint32_t iw = (vw == vmax) ? (uint32_t)hk[0] : 0u;
+            const uint32_t imax = __reduce_max_sync(0xffffffffu, iw);
+            const uint64_t key = ((uint64_t)vmax << 32) | imax;
+            if (lane == 0) {
+                topk_idx[(size_t)row * K + r] = (int32_t)key_index(key);
+                topk_logp[(size_t)row * K + r] = (key_value(key) - M) - logS;
+            }
+            if (vw == vmax && (uint32_t)hk[0] == imax) {  // the winner (keys are distinct)
 #pragma unroll
-            for (int i = 0; i < PL; ++i) {
-                const unsigned bal = __ballot_sync(0xffffffffu, vmx[i] >= tv);
-                if (vmx[i] >= tv) s_vlist[warp][nv + __popc(bal & ((1u << lane) - 1u))] = (int16_t)(lane + 32 * i);
-                nv += __popc(bal);
+                for (int i = 0; i + 1 < kMergeHeads; ++i) hk[i] = hk[i + 1];
+                hk[kMergeHeads - 1] = 0ull;
+                if (++used % kMergeHeads == 0 && used < K) {  // its next keys (K > 8 only)
+#pragma unroll
+                    for (int i = 0; i < kMergeHeads; ++i)
+                        hk[i] = used + i < K ? __ldcg((const unsigned long long*)mine + 1 + used + i) : 0ull;
+                }
+            }
+        }
+        __syncwarp();
+        // the row's slots back to zero, like its counter and bound: a later call
+        // of other sizes may place its counters here
+        for (int wd = lane; wd < np * (1 + K); wd += 32) base[wd] = 0ull;
+        if (lane == 0) {
+            if (lse) lse[row] = M + logS;
+            ws.row_cnt[row] = 0u;  // ready for the next call
+            ws.row_tau[row] = 0ull;
+        }
+        __syncwarp();
+    };
+
+    // Segment by segment through the warp's ring, kStages - 1 ahead.  After a
+    // fill that never lands (a bounded wait that timed out) the warp stops
+    // issuing, records the error and runs the rest of its protocol on zeros, so
+    // every row count still completes (and returns to zero) and the call ends.
+    // chunk c goes to CTA c mod grid: every SM streams even when there are
+    // fewer chunks than warps
+    Cur xi{(long)warp * gridDim.x + blockIdx.x, 0, 0, 0, 0};
+    bool hi = place(xi);
+    Cur xp = xi;
+    bool hp = hi;
+    int ni = 0, np = 0;
+    bool dead = false;
+    // The row's shared bound is fetched with each segment's copy and used when
+    // the segment is read: a queue of kStages values (q0 is the segment read
+    // next), in registers.
+    static_assert(kStages == 3, "the bound queue holds three segments");
+    uint64_t q0 = 0ull, q1 = 0ull, q2 = 0ull;
+    for (int k = 0; k < kStages - 1 && hi; ++k) {
+        ring.issue(ni % kStages, rowp_of(xi.row), xi.seg * S::SIZE, V, aligned);
+        (k == 0 ? q0 : q1) = __ldcg(&ws.row_tau[xi.row]);
+        ++ni;
+        hi = next(xi);
+    }
+    float m = -INFINITY;                      // the lane's running max of the piece
+    float2 acc = make_float2(0.f, 0.f);       // ... and sum of exp(x - m), in two
+    float2 acc2 = make_float2(0.f, 0.f);      // independent chains
+    while (hp) {
+        if (hi && !dead) {  // into the stage read last
+            ring.issue(ni % kStages, rowp_of(xi.row), xi.seg * S::SIZE, V, aligned);
+            q2 = __ldcg(&ws.row_tau[xi.row]);
+            ++ni;
+            hi = next(xi);
+        }
+        const uint64_t rbl = q0;  // this segment's row bound, fetched with its copy
+        q0 = q1;
+        q1 = q2;
+        const int st = np % kStages;
+        if (!dead && !ring.wait(st, (uint32_t)((np / kStages) & 1))) {
+            dead = true;
+            if (lane == 0) record_error(err, ERR_TOPK | ERR_WAIT_TIMEOUT);
+        }
+        uint4 cur[VPL];
+        if (!dead) {
+            ring.read(st, cur);
+        } else {
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) cur[k] = make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();  // every lane has read the stage: it may be refilled
+        ++np;
+        const int e0 = xp.seg * S::SIZE;
+
+        // ---- vector maxima; the lane's online (max, sum of exponentials) ----
+        float vm[VPL];
+        float ms = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            vm[k] = S::vmax(cur[k]);
+            ms = fmaxf(ms, vm[k]);
+        }
+        if (ms > m) {
+            const float f = fast_exp2((m - ms) * kLog2e);  // 0 while m = -inf
+            acc.x *= f;
+            acc.y *= f;
+            acc2.x *= f;
+            acc2.y *= f;
+            m = ms;
+        }
+        if (m != -INFINITY) {
+            const float off = -m * kLog2e;
+#pragma unroll
+            for (int k = 0; k < VPL; k += 2) {
+                S::exp_sum2(cur[k], kLog2e, off, acc);
+                S::exp_sum2(cur[k + 1], kLog2e, off, acc2);
+            }
+        }
+
+        // ---- candidates: keys above the bound (the list's K-th key or the
+        // row's shared bound; with neither, at or above the K-th largest lane
+        // maximum of the segment) ----
+        kb.rb = umax64(kb.rb, rbl);
+        const uint64_t bnd = kb.bound();
+        float tv = bnd != 0ull ? key_value(bnd) : -INFINITY;
+        if (bnd == 0ull) {
+            const bool real = e0 + lane * VEC < V;  // the lane holds an element
+            const uint32_t b = warp_kth_largest(real ? ord_from_float(ms) : 0u, K);
+            if (b != 0u) tv = fmaxf(tv, float_from_ord(b));
+        }
+        unsigned vpm = 0u;  // the lane's vectors that may hold a candidate
+#pragma unroll
+        for (int k = 0; k < VPL; ++k)
+            if (e0 + (lane + 32 * k) * VEC < V && vm[k] >= tv) vpm |= 1u << k;
+        if (__any_sync(0xffffffffu, vpm != 0u)) {
+            const uint4* stv = reinterpret_cast<const uint4*>(ring.buf + st * kSegBytes) + lane;
+            // Fast path: each lane walks its own passing vectors (re-read from the
+            // stage, intact until the next iteration refills it) and reserves
+            // buffer places with a shared-memory add -- no warp-wide step per
+            // candidate.  If the buffer would overflow, nothing of it is kept
+            // and the slow path below redoes the step from the same place.
+            const int base0 = kb.n + kb.cc;
+            if (lane == 0) s_cc[warp] = base0;
+            __syncwarp();
+            const uint64_t tk = kb.bound();
+            bool ovf = false;
+            for (unsigned pend = vpm; pend != 0u; pend &= pend - 1u) {
+                const int k = __ffs(pend) - 1;
+                const uint4 v = stv[32 * k];
+                const int ev = e0 + (lane + 32 * k) * VEC;
+                // the vector's elements >= tv (one packed comparison per pair),
+                // then the key test for those alone (usually one)
+                for (unsigned em = S::ge_mask(v, tv); em != 0u; em &= em - 1u) {
+                    const int j = __ffs(em) - 1;
+                    const uint64_t key = value_index_key(S::elem_dyn(v, j), (uint32_t)(ev + j));
+                    if (ev + j >= V || key <= tk) continue;
+                    const int pos = atomicAdd(&s_cc[warp], 1);
+                    if (pos < kCap) kb.buf[pos] = key;
+                    else ovf = true;
+                }
             }
             __syncwarp();
-            for (int b0 = 0; b0 < nv; b0 += 32) {
-                const int v = b0 + lane < nv ? s_vlist[warp][b0 + lane] : -1;
-                float x[VEC];
-                int mine = 0;
-                const int e = c0 + (warp * VPW + v) * VEC;
-                if (v >= 0) {
-                    Chunk::unpack(vw[v], x);
+            if (!__any_sync(0xffffffffu, ovf)) {
+                kb.cc = s_cc[warp] - kb.n;
+            } else {
+                // Slow path: the lanes take their passing vectors one round at a
+                // time; a scan places each round's candidates, and ties beyond the
+                // buffer go key by key, merging whenever it fills.
+                unsigned pend = vpm;
+                while (__any_sync(0xffffffffu, pend != 0u)) {
+                    const bool have = pend != 0u;
+                    const int k = have ? __ffs(pend) - 1 : 0;
+                    pend &= pend - 1u;
+                    const uint4 v = stv[32 * k];
+                    const int ev = e0 + (lane + 32 * k) * VEC;
+                    const uint64_t tb = kb.bound();
+                    unsigned em = 0u;  // bit j: element j of the vector qualifies
 #pragma unroll
-                    for (int k = 0; k < VEC; ++k) mine += (x[k] >= tv && e + k < V) ? 1 : 0;
-                }
-                int incl = mine;
+                    for (int j = 0; j < VEC; ++j) {
+                        const float x = S::elem(v, j);
+                        if (have && ev + j < V && x >= tv && value_index_key(x, (uint32_t)(ev + j)) > tb)
+                            em |= 1u << j;
+                    }
+                    const int cnt = __popc(em);
+                    int incl = cnt;
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int t = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += t;
-                }
-                int wbase = 0;
-                if (lane == 31 && incl > 0) wbase = atomicAdd(&s_cnt, incl);
-                wbase = __shfl_sync(0xffffffffu, wbase, 31);
-                if (mine) {
-                    int pos = wbase + incl - mine;
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += t;
+                    }
+                    const int tot = __shfl_sync(0xffffffffu, incl, 31);
+                    if (tot == 0) continue;
+                    if (kb.n + kb.cc + tot <= kCap) {
+                        int pos = kb.n + kb.cc + incl - cnt;
 #pragma unroll
-                    for (int k = 0; k < VEC; ++k) {
-                        if (x[k] >= tv && e + k < V) {
-                            if (pos < kChunkCand) out->keys[pos] = value_index_key(x[k], (uint32_t)(e + k));
-                            ++pos;
+                        for (int j = 0; j < VEC; ++j)
+                            if ((em >> j) & 1u) kb.buf[pos++] = value_index_key(S::elem(v, j), (uint32_t)(ev + j));
+                        kb.cc += tot;
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) {
+                            const uint64_t key = value_index_key(S::elem(v, j), (uint32_t)(ev + j));
+                            kb.push(((em >> j) & 1u) && key > kb.bound(), key);
                         }
                     }
                 }
             }
-        };
+        }
+        // merge the candidates once 32 have gathered (and while the list is not
+        // yet full): the list's K-th key, and with it the row's bound, rises
+        if (kb.cc >= 32 || (kb.n < K && kb.cc > 0)) kb.reduce();
+        if (kb.n == K && kb.tkey > kb.rb) {  // a tighter bound for the whole row
+            if (lane == 0) atomicMax(&ws.row_tau[xp.row], (unsigned long long)kb.tkey);
+            kb.rb = kb.tkey;
+        }
 
-        // A later chunk of the row this CTA already met: every key below tau_run
-        // (an earlier chunk's bound) is out of the row's K best, so the chunk
-        // keeps its keys >= tau_run and reports tau_run as its bound -- valid for
-        // the merge, which needs only a bound <= the row's K-th largest and every
-        // key >= it.  Too many such keys: the chunk takes the full path below.
-        bool cheap = false;
-        int cnt = 0;
-        if (tau_run != 0u) {
-            gather(float_from_ord(tau_run));
-            __syncthreads();
-            cnt = s_cnt;
-            cheap = cnt <= kChunkCand;
-            if (!cheap) {
-                __syncthreads();  // every thread has read the count
-                if (tid == 0) s_cnt = 0;
+        // ---- the row's piece ends: publish, take the row's ticket, and merge
+        // the row if this piece completes it ----
+        if (xp.seg + 1 == nseg || xp.i + 1 == xp.iend) {
+            if (kb.cc > 0) kb.reduce();
+            float mw = m, sw = (acc.x + acc.y) + (acc2.x + acc2.y);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float mo = __shfl_xor_sync(0xffffffffu, mw, o);
+                const float so = __shfl_xor_sync(0xffffffffu, sw, o);
+                ms_combine(mw, sw, mo, so, kLog2e);
             }
+            uint64_t* sl = ws.slots + (size_t)(xp.c + xp.row) * (size_t)(1 + K);
+            if (lane == 0) *reinterpret_cast<float2*>(sl) = make_float2(mw, sw);
+            if (lane < K) sl[1 + lane] = lane < kb.n ? kb.buf[lane] : 0ull;
+            __syncwarp();
+            // the piece before its count; the other pieces visible to the warp
+            // whose count completes the row
+            unsigned now = 0u;
+            if (lane == 0) now = atom_add_acq_rel_u32(&ws.row_cnt[xp.row], 1u) + 1u;
+            now = __shfl_sync(0xffffffffu, now, 0);
+            __syncwarp();
+            if (now == (unsigned)pieces(xp.row)) merge(xp.row);
+            kb.reset();
+            m = -INFINITY;
+            acc = make_float2(0.f, 0.f);
+            acc2 = make_float2(0.f, 0.f);
         }
-        uint32_t tau = tau_run;
-        if (!cheap) {
-            // The warp's K largest vector maxima (K distinct elements), descending,
-            // into s_vm[warp]: the vector maxima at or above the K-th largest lane
-            // maximum (usually K to 3K) sorted by the warp; if there are too many,
-            // K copies of that lane bound (still K elements >= each).
-            {
-                const uint32_t tau_l = warp_kth_largest(e_lane < V ? ord_from_float(mt) : 0u, K);
-                const float tl = (tau_l == 0u) ? -INFINITY : float_from_ord(tau_l);
-                int nm = 0;
-#pragma unroll
-                for (int i = 0; i < PL; ++i) {
-                    const bool in = vmx[i] >= tl && e_lane + 32 * i * VEC < V;
-                    const unsigned bal = __ballot_sync(0xffffffffu, in);
-                    const int at = nm + __popc(bal & ((1u << lane) - 1u));
-                    if (in && at < 32) s_vm[warp][at] = ord_from_float(vmx[i]);
-                    nm += __popc(bal);
-                }
-                __syncwarp();
-                uint32_t top = tau_l;
-                if (nm <= 32) top = warp_sort_desc_u32(lane < nm ? s_vm[warp][lane] : 0u);
-                __syncwarp();
-                if (lane < K) s_vm[warp][lane] = top;
-            }
-            __syncthreads();
-            // tau: the K-th largest of the warps' lists (each warp, redundantly),
-            // a bound on the chunk's K-th largest value
-            {
-                int ptr = 0;
-                uint32_t head = lane < kWarps ? s_vm[lane][0] : 0u;
-                for (int r = 0; r < K; ++r) {
-                    tau = __reduce_max_sync(0xffffffffu, head);
-                    const unsigned holders = __ballot_sync(0xffffffffu, head == tau);
-                    if (lane == __ffs(holders) - 1) {
-                        ++ptr;
-                        head = ptr < K ? s_vm[lane][ptr] : 0u;
-                    }
-                }
-            }
-            gather((tau == 0u) ? -INFINITY : float_from_ord(tau));
-            __syncthreads();
-            cnt = s_cnt;
-            if (cnt > kChunkCand) {
-                cta_exact_top_k<Chunk>(vec, c0, V, K, s_red, out);  // degenerate ties
-            } else {
-                tau_run = max(tau_run, tau);  // (uniform: every warp computed tau)
-            }
-        }
-        if (tid == 0) {
-            if (cnt <= kChunkCand) {
-                out->count = cnt;
-                out->tau = tau;
-            }
-            float m = s_wms[0].x, sm = s_wms[0].y;
-#pragma unroll
-            for (int i = 1; i < kWarps; ++i) ms_combine(m, sm, s_wms[i].x, s_wms[i].y, kLog2e);
-            out->m = m;
-            out->s = sm;
-        }
-        __syncthreads();  // the stage and the shared counters are free again
+        hp = next(xp);
     }
-}
-
-// One CTA per row merges the row's chunk outputs.  Every chunk holds >= K
-// elements >= its tau, so the row's K best keys are >= tau2 = max over chunks
-// of tau; the kept keys >= tau2 are gathered and each is ranked by counting
-// the larger ones (the K of rank < K are the answer, in order).  The
-// logsumexp combines the chunks' (max, sum) pairs.  Each thread issues a batch
-// of kMergeLoads key loads before using any.
-constexpr int kMergeThreads = 256;
-constexpr int kMergeLoads = 8;
-__global__ void __launch_bounds__(kMergeThreads)
-topk_merge_kernel(const ChunkOut* __restrict__ outs, int nchunks, int K,
-                  int32_t* __restrict__ topk_idx, float* __restrict__ topk_logp,
-                  float* __restrict__ lse) {
-    __shared__ __align__(16) uint64_t s_c[kMergeCand];
-    __shared__ uint64_t s_sel[DDTREE_MAX_K];
-    __shared__ int s_n[kMaxChunks];
-    __shared__ uint32_t s_tau[kMergeThreads / 32];
-    __shared__ float2 s_ms[kMergeThreads / 32];
-    __shared__ int s_cnt;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int row = blockIdx.x;
-    if (tid == 0) s_cnt = 0;
-    if (tid < K) s_sel[tid] = 0ull;
-    pdl_wait();
-    const ChunkOut* ro = outs + (size_t)row * nchunks;
-    // the first batch of key slots is loaded with the chunk headers (one round
-    // trip); slots past a chunk's count are dropped once the counts are known
-    const int nslots = nchunks * kChunkCand;
-    uint64_t kv0[kMergeLoads];
-#pragma unroll
-    for (int u = 0; u < kMergeLoads; ++u) {
-        const int i = u * kMergeThreads + tid;
-        kv0[u] = i < nslots ? __ldcg((const unsigned long long*)&ro[i / kChunkCand].keys[i % kChunkCand])
-                            : 0ull;
-    }
-    uint32_t tau2 = 0u;
-    float mt = -INFINITY, st = 0.f;
-    for (int c = tid; c < nchunks; c += kMergeThreads) {
-        tau2 = max(tau2, __ldcg(&ro[c].tau));
-        ms_combine(mt, st, __ldcg(&ro[c].m), __ldcg(&ro[c].s), kLog2e);
-        s_n[c] = min(__ldcg(&ro[c].count), kChunkCand);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        tau2 = max(tau2, __shfl_xor_sync(0xffffffffu, tau2, o));
-        const float mo = __shfl_xor_sync(0xffffffffu, mt, o);
-        const float so = __shfl_xor_sync(0xffffffffu, st, o);
-        ms_combine(mt, st, mo, so, kLog2e);
-    }
-    if (lane == 0) {
-        s_tau[warp] = tau2;
-        s_ms[warp] = make_float2(mt, st);
-    }
-    __syncthreads();
-    tau2 = s_tau[0];
-    mt = s_ms[0].x;
-    st = s_ms[0].y;
-#pragma unroll
-    for (int i = 1; i < kMergeThreads / 32; ++i) {
-        tau2 = max(tau2, s_tau[i]);
-        ms_combine(mt, st, s_ms[i].x, s_ms[i].y, kLog2e);
-    }
+    if (dead)  // copies still in flight into the ring: one more bounded wait each
+        for (int k = np; k < ni; ++k) ring.wait(k % kStages, (uint32_t)((k / kStages) & 1));
     pdl_trigger();
-    // gather the kept keys >= tau2 (slot k of chunk c is index c * kChunkCand + k)
-    for (int b0 = 0; b0 < nslots; b0 += kMergeLoads * kMergeThreads) {
-        uint64_t kv[kMergeLoads];
-#pragma unroll
-        for (int u = 0; u < kMergeLoads; ++u) {
-            const int i = b0 + u * kMergeThreads + tid;
-            const int c = i / kChunkCand, k = i - c * kChunkCand;
-            if (b0 == 0) kv[u] = (i < nslots && k < s_n[c]) ? kv0[u] : 0ull;
-            else kv[u] = (i < nslots && k < s_n[c])
-                             ? __ldcg((const unsigned long long*)&ro[c].keys[k]) : 0ull;
-        }
-#pragma unroll
-        for (int u = 0; u < kMergeLoads; ++u) {
-            if (kv[u] != 0ull && (uint32_t)(kv[u] >> 32) >= tau2) {
-                const int at = atomicAdd(&s_cnt, 1);
-                if (at < kMergeCand) s_c[at] = kv[u];
-            }
-        }
-    }
-    __syncthreads();
-    const int cnt = s_cnt;
-    if (cnt <= kMergeCand) {
-        for (int i = tid; i < cnt; i += kMergeThreads) {
-            const uint64_t key = s_c[i];
-            const int rank = count_larger(s_c, cnt, key);
-            if (rank < K) s_sel[rank] = key;
-        }
-    } else {
-        // Degenerate ties: K rounds of a CTA maximum below the previous one over
-        // every kept key (correctness only).
-        uint64_t prev = ~0ull;
-        for (int r = 0; r < K; ++r) {
-            uint64_t tb = 0ull;
-            for (int i = tid; i < nslots; i += kMergeThreads) {
-                const int c = i / kChunkCand, k = i - c * kChunkCand;
-                if (k < s_n[c]) {
-                    const uint64_t key = __ldcg((const unsigned long long*)&ro[c].keys[k]);
-                    if (key < prev && key > tb) tb = key;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) tb = umax64(tb, shfl_xor_u64(tb, o));
-            __syncthreads();
-            if (lane == 0) s_c[warp] = tb;
-            __syncthreads();
-            tb = s_c[0];
-            for (int i = 1; i < kMergeThreads / 32; ++i) tb = umax64(tb, s_c[i]);
-            if (tid == 0) s_sel[r] = tb;
-            prev = tb;
-        }
-    }
-    __syncthreads();
-    if (warp != 0) return;
-    const float M = (mt == -INFINITY) ? 0.f : mt;
-    const float logS = logf(st);
-    if (lane < K) {
-        const uint64_t key = s_sel[lane];
-        topk_idx[(size_t)row * K + lane] = (int32_t)key_index(key);
-        topk_logp[(size_t)row * K + lane] = (key_value(key) - M) - logS;
-    }
-    if (lane == 0 && lse) lse[row] = M + logS;
 }
 
-int chunks_at(int V, int dtype, int bytes) {
-    const int size = bytes / (dtype == DDTREE_BF16 ? 2 : 4);
-    return (V + size - 1) / size;
-}
+struct Plan {
+    int nseg;
+    long spc, nchunks;
+    int grid;
+};
 
 // Streaming multiprocessors of the current device (148 if the query fails).
 int num_sms_topk() {
@@ -469,73 +470,81 @@ int num_sms_topk() {
     return cached[dev];
 }
 
-// Chunks per row: small ones when even those fit in one wave of CTAs.
-struct ChunkPlan {
-    bool small;
-    int nch;
-};
-ChunkPlan chunk_plan(int rows, int V, int dtype) {
-    const long slots = (long)num_sms_topk() * kCtasPerSm;
-    const bool small = (long)chunks_at(V, dtype, kChunkSmall) * rows <= slots;
-    return {small, chunks_at(V, dtype, small ? kChunkSmall : kChunkBig)};
+int seg_count(int V, int dtype) {
+    const int size = kSegBytes / (dtype == DDTREE_BF16 ? 2 : 4);
+    return (V + size - 1) / size;
 }
 
-// Workspace: one ChunkOut per (row, chunk).
-size_t topk_layout_bytes(int rows, int V, int dtype) {
-    return (size_t)rows * chunk_plan(rows, V, dtype).nch * sizeof(ChunkOut);
+// Equal chunks, one per warp of a one-CTA-per-SM wave, each at least
+// (nseg - 1) / 31 segments long so that no row has more than kMaxPieces pieces.
+Plan topk_plan(int rows, int V, int dtype, int sms) {
+    Plan p;
+    p.nseg = seg_count(V, dtype);
+    const long total = (long)rows * p.nseg;
+    const long w = (long)std::min(sms, kMaxGridWarps / kWarps) * kWarps;
+    // a row meets at most ceil((nseg - 1) / spc) + 1 chunks
+    p.spc = std::max({1L, (total + w - 1) / w, (long)(p.nseg - 1 + kMaxPieces - 2) / (kMaxPieces - 1)});
+    p.nchunks = (total + p.spc - 1) / p.spc;
+    p.grid = (int)std::min((long)sms, p.nchunks);
+    return p;
+}
+
+// Workspace: the row counters and bounds, then one slot per (chunk, row) piece.  Chunk c's
+// piece of row r sits at slot c + r < chunks + rows; the plan never makes more
+// chunks than segments or than kMaxGridWarps, whatever the device.
+struct WsLayout {
+    size_t row_cnt, row_tau, slots, total;
+};
+WsLayout topk_layout(int rows, int V, int dtype, int K) {
+    const long total = (long)rows * seg_count(V, dtype);
+    const size_t nslots = (size_t)std::min(total, (long)kMaxGridWarps) + (size_t)rows;
+    WsLayout l;
+    l.row_cnt = 0;
+    l.row_tau = align_up((size_t)rows * 4, 256);
+    l.slots = align_up(l.row_tau + (size_t)rows * 8, 256);
+    l.total = align_up(l.slots + nslots * 8 * (size_t)(1 + K), 256);
+    return l;
 }
 
 }  // namespace
 
 bool topk_supported(int V, int dtype, int K) {
-    return topk_chunks(V, dtype) <= kMaxChunks && K >= 1 && K <= DDTREE_MAX_K;
+    (void)dtype;
+    return V >= 1 && V <= kMaxV && K >= 1 && K <= DDTREE_MAX_K;
 }
-
-int topk_chunks(int V, int dtype) { return chunks_at(V, dtype, kChunkSmall); }
 
 size_t topk_workspace_bytes(int rows, int V, int dtype, int K) {
-    (void)K;
-    return topk_layout_bytes(rows, V, dtype);
+    if (rows <= 0 || V <= 0) return 0;
+    return topk_layout(rows, V, dtype, K >= 1 ? K : DDTREE_MAX_K).total;
 }
 
-template <bool BF16, int BYTES>
-cudaError_t launch_partials(const TopkArgs& a, int nch, bool aligned, int total, int per,
-                            ChunkOut* outs, cudaStream_t s) {
+template <bool BF16>
+cudaError_t launch_stream(const TopkArgs& a, const Plan& p, bool aligned, TopkWs ws,
+                          cudaStream_t s) {
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
     int dev = 0;
     cudaGetDevice(&dev);
-    const size_t ring = (size_t)kStages * BYTES;
     std::call_once(once[dev & 63], [&] {
         attr_err[dev & 63] = cudaFuncSetAttribute(
-            topk_kernel<BF16, BYTES>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring);
+            topk_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     });
     if (attr_err[dev & 63] != cudaSuccess) return attr_err[dev & 63];
-    const int grid = (total + per - 1) / per;
-    return launch_pdl(topk_kernel<BF16, BYTES>, dim3(grid), dim3(kThreads), ring, s, a.logits,
-                      a.V, a.row_stride, a.K, nch, aligned, total, per, outs, a.err);
+    return launch_pdl(topk_kernel<BF16>, dim3(p.grid), dim3(kThreads), (size_t)kSmemBytes, s,
+                      a.logits, a.V, a.row_stride, a.rows, p.nseg, p.spc, aligned, a.K, ws,
+                      a.topk_idx, a.topk_logp, a.lse, a.err);
 }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
     const int es = a.dtype == DDTREE_BF16 ? 2 : 4;
     const bool aligned = ((uintptr_t)a.logits % 16 == 0) && ((a.row_stride * es) % 16 == 0);
-    ChunkOut* outs = (ChunkOut*)a.ws;
-    // one wave of persistent CTAs, each streaming a contiguous run of chunks
-    const long slots = (long)num_sms_topk() * kCtasPerSm;
-    const ChunkPlan cp = chunk_plan(a.rows, a.V, a.dtype);
-    const int nch = cp.nch;
-    const long total = (long)nch * a.rows;
-    const int per = (int)((total + slots - 1) / slots);
-    cudaError_t e;
-    if (a.dtype == DDTREE_BF16)
-        e = cp.small ? launch_partials<true, kChunkSmall>(a, nch, aligned, (int)total, per, outs, s)
-                     : launch_partials<true, kChunkBig>(a, nch, aligned, (int)total, per, outs, s);
-    else
-        e = cp.small ? launch_partials<false, kChunkSmall>(a, nch, aligned, (int)total, per, outs, s)
-                     : launch_partials<false, kChunkBig>(a, nch, aligned, (int)total, per, outs, s);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(topk_merge_kernel, dim3(a.rows), dim3(kMergeThreads), 0, s,
-                      (const ChunkOut*)outs, nch, a.K, a.topk_idx, a.topk_logp, a.lse);
+    const Plan p = topk_plan(a.rows, a.V, a.dtype, num_sms_topk());
+    const WsLayout l = topk_layout(a.rows, a.V, a.dtype, a.K);
+    char* base = (char*)a.ws;
+    const TopkWs ws{(unsigned int*)(base + l.row_cnt), (unsigned long long*)(base + l.row_tau),
+                    (uint64_t*)(base + l.slots)};
+    return a.dtype == DDTREE_BF16 ? launch_stream<true>(a, p, aligned, ws, s)
+                                  : launch_stream<false>(a, p, aligned, ws, s);
 }
 
 }  // namespace ddt
@@ -589,7 +598,7 @@ extern "C" ddtree_status ddtree_topk_noalloc(const void* draft_logits, int dtype
     const size_t need = ddt::topk_workspace_bytes(rows, V, dtype, K);
     if (need > DDTREE_NOALLOC_SCRATCH_BYTES) return DDTREE_ERR_UNSUPPORTED;
     void* scratch = nullptr;
-    // (every partial the merge reads is written by the same call: no clearing)
+    // (the array starts zeroed and every call leaves its row counters at zero)
     if (need) {
         const cudaError_t e = noalloc_scratch(&scratch);
         if (e != cudaSuccess) return (ddtree_status)ddt::launch_status(e);

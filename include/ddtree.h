@@ -33,7 +33,9 @@
  *     must be 256-byte aligned and zero-filled before its first use (e.g. one
  *     cudaMemsetAsync when it is allocated).  Each call leaves its counters at
  *     zero again, so a workspace can be reused call after call by the SAME
- *     operation; two calls that may run concurrently need separate workspaces.
+ *     operation with the same sizes (a top-K call leaves all of the workspace
+ *     it used at zero, so top-K may also change sizes); two calls that may run
+ *     concurrently need separate workspaces.
  *
  * Symbols used below: B sequences, L draft positions per block, V vocabulary,
  * K tokens kept per position, N node budget (drafted nodes; the root is extra,
@@ -108,12 +110,14 @@ ddtree_status ddtree_topk(const void* draft_logits, int dtype, int rows, int V,
  * process exits); the call allocates nothing.  It needs
  * ddtree_workspace_size(DDTREE_OP_TOPK, ...) bytes of it; a larger problem is
  * rejected with DDTREE_ERR_UNSUPPORTED before anything is enqueued (for
- * V = 151936 bf16 that is about 390 rows).
+ * V = 151936 bf16 that is 10286 rows at K = 8, 1348 rows at K = 32).
  * The first call made on a device looks up the array's device address on that
- * device (make it with the device current, before any stream capture).  Every
- * partial a call reads is written by that call, so nothing is cleared; a
- * kernel that could not write its partials (a bounded wait that timed out)
- * records that in the device error word, which ddtree_device_check() reports.
+ * device (make it with the device current, before any stream capture).  The
+ * array starts zeroed and every call leaves all of it that it used at zero
+ * again, so calls of any sizes follow one another with nothing cleared in
+ * between; a kernel whose copy
+ * never landed (a bounded wait that timed out) records that in the device
+ * error word, which ddtree_device_check() reports.
  * All calls share the one array: calls whose kernels can overlap on the GPU
  * (other streams, other threads) race and give wrong results; serialise them. */
 ddtree_status ddtree_topk_noalloc(const void* draft_logits, int dtype, int rows, int V,

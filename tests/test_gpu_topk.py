@@ -1,9 +1,10 @@
 """GPU parity of step 1 (log-softmax + top-K) against the oracle.
 Criteria: indices bit-exact; log-probs and logsumexp within 1e-5 absolute of
-the oracle's fp64 values.  Both chunk sizes are covered: 16 KB chunks when
-every chunk of every row fits one wave of CTAs, 32 KB otherwise; the edge
-shapes run once as they are (six rows: 16 KB) and once with their rows
-repeated 64 times (32 KB)."""
+the oracle's fp64 values.  Rows are streamed in 4 KB segments by warps that
+each take an equal run of them, so a row is cut into one or many pieces and a
+warp's run may cross many rows; the edge shapes run once as they are (six
+rows: a row spans many warps) and once with their rows repeated 64 times
+(longer runs, crossing row ends)."""
 import numpy as np
 import pytest
 import torch
@@ -49,7 +50,7 @@ def test_topk_workloads(cuda_device, name):
 @pytest.mark.parametrize("reps", [1, 64])
 def test_topk_edge_shapes_and_ties(cuda_device, V, K, dtype, unaligned, reps):
     if reps > 1 and V > 100000:
-        pytest.skip("the long-row workloads above already take 32 KB chunks")
+        pytest.skip("the long-row workloads above already stream many rows per warp")
     rng = np.random.default_rng(V + K)
     x = (rng.standard_normal((6, V)) * 3).astype(np.float32)
     x[1, :] = 0.0                                     # a constant row: ties everywhere

@@ -74,7 +74,7 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     """Sizes are checked on the host before anything is enqueued: no GPU needed."""
     f = _noalloc()
     fake = ctypes.c_void_p(0x1000)
-    rows = 2000  # 2000 rows of a 151936-token bf16 vocabulary need ~11 MB of partials
+    rows = 20000  # 20000 rows of a 151936-token bf16 vocabulary need ~1.9 MB at K = 8
     assert ops.workspace_size(ops.OP_TOPK, B=rows, L=1, V=151936, K=8,
                               dtype=ops.BF16) > SCRATCH_BYTES
     assert f(fake, ops.BF16, rows, 151936, 151936, 8, fake, fake, None, None) == 2
