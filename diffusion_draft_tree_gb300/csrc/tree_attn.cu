@@ -169,12 +169,23 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (warp == 1) tmem_dealloc(tmem, kTmemCols);
     };
 
-    // ---- decode the unit (its KV splits are consecutive CTAs: one cluster) -------
+    // ---- decode the unit.  Cluster plans: a unit's KV splits are consecutive
+    // CTAs (one cluster; split == rank in it).  Otherwise the tile pairs that
+    // read the same KV range are consecutive CTAs, so they run at the same time
+    // and the range comes from DRAM once for all of them.
     int idx = blockIdx.x;
-    const int split = idx % p.smax;  // == rank in the cluster
-    idx /= p.smax;
-    const int mpair = idx % p.mpairs;
-    idx /= p.mpairs;
+    int split, mpair;
+    if (p.merge == kMergeCluster) {
+        split = idx % p.smax;
+        idx /= p.smax;
+        mpair = idx % p.mpairs;
+        idx /= p.mpairs;
+    } else {
+        mpair = idx % p.mpairs;
+        idx /= p.mpairs;
+        split = idx % p.smax;
+        idx /= p.smax;
+    }
     const int g = idx % p.Hkv;
     const int b = idx / p.Hkv;
     const int R = p.N + 1, G = p.G;
