@@ -365,45 +365,18 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int rows
             if (!__any_sync(0xffffffffu, ovf)) {
                 kb.cc = s_cc[warp] - kb.n;
             } else {
-                // Slow path: the lanes take their passing vectors one round at a
-                // time; a scan places each round's candidates, and ties beyond the
-                // buffer go key by key, merging whenever it fills.
-                unsigned pend = vpm;
-                while (__any_sync(0xffffffffu, pend != 0u)) {
-                    const bool have = pend != 0u;
-                    const int k = have ? __ffs(pend) - 1 : 0;
-                    pend &= pend - 1u;
+                // Slow path (the buffer would overflow: many ties): key by key,
+                // merging whenever the buffer fills; rare, so kept compact.
+#pragma unroll 1
+                for (int k = 0; k < VPL; ++k) {
                     const uint4 v = stv[32 * k];
                     const int ev = e0 + (lane + 32 * k) * VEC;
-                    const uint64_t tb = kb.bound();
-                    unsigned em = 0u;  // bit j: element j of the vector qualifies
-#pragma unroll
+                    const bool vp = (vpm >> k) & 1u;
+#pragma unroll 1
                     for (int j = 0; j < VEC; ++j) {
-                        const float x = S::elem(v, j);
-                        if (have && ev + j < V && x >= tv && value_index_key(x, (uint32_t)(ev + j)) > tb)
-                            em |= 1u << j;
-                    }
-                    const int cnt = __popc(em);
-                    int incl = cnt;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-                        if (lane >= o) incl += t;
-                    }
-                    const int tot = __shfl_sync(0xffffffffu, incl, 31);
-                    if (tot == 0) continue;
-                    if (kb.n + kb.cc + tot <= kCap) {
-                        int pos = kb.n + kb.cc + incl - cnt;
-#pragma unroll
-                        for (int j = 0; j < VEC; ++j)
-                            if ((em >> j) & 1u) kb.buf[pos++] = value_index_key(S::elem(v, j), (uint32_t)(ev + j));
-                        kb.cc += tot;
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < VEC; ++j) {
-                            const uint64_t key = value_index_key(S::elem(v, j), (uint32_t)(ev + j));
-                            kb.push(((em >> j) & 1u) && key > kb.bound(), key);
-                        }
+                        const float x = S::elem_dyn(v, j);
+                        const uint64_t key = value_index_key(x, (uint32_t)(ev + j));
+                        kb.push(vp && ev + j < V && x >= tv && key > kb.bound(), key);
                     }
                 }
             }
