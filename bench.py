@@ -53,7 +53,7 @@ def parse():
     ap.add_argument("--walk", default="auto", choices=["auto", "full", "path"],
                     help="step 4: the full-tree walk (ddtree_accept), the path-only walk "
                          "(ddtree_accept_path), or auto: the path-only walk once the batch "
-                         "has >= 128 tree rows, B (N + 1)")
+                         "has >= 32 tree rows, B (N + 1)")
     ap.add_argument("--acceptance-stats", type=int, default=0, metavar="ROUNDS",
                     help="instead of timing: run ROUNDS independent synthetic rounds per node "
                          "budget (and the K = 1 chain) and report acceptance lengths")
@@ -881,14 +881,15 @@ WALK = "auto"  # step 4 of the timed round (--walk)
 
 
 def walk_for(w) -> str:
-    """The walk the round uses: measured on the five workloads, the path-only
-    walk (a dependent chain of rows) is faster once the batch's trees hold
-    128 rows or more (N = 128: 73 -> 66 us a round, ragged_serving 976 -> 736
-    us), the full-tree walk (every row at once) below (8b_single: 40.1 vs
-    40.5 us)."""
+    """The walk the round uses: measured on the workloads, the path-only walk
+    (a dependent chain of rows) gives the faster round once the batch's trees
+    hold 32 rows or more (8b_single 44.2 -> 40.4 us a round, N = 32 55.5 ->
+    50.5 us, N = 64 65.7 -> 59.2 us; larger trees gain more); the full-tree
+    walk (every row at once) only for the tiniest trees, where it is also the
+    faster call alone."""
     if WALK != "auto":
         return WALK
-    return "path" if w.B * (w.N + 1) >= 128 else "full"
+    return "path" if w.B * (w.N + 1) >= 32 else "full"
 
 
 def kernel_report(w, model, stage, peaks):

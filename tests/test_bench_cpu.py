@@ -12,8 +12,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 def test_walk_policy():
     bench.WALK = "auto"
-    want = {"tiny": "full", "8b_single": "full", "budget_sweep_n32": "full",
-            "budget_sweep_n64": "full", "budget_sweep_n128": "path",
+    want = {"tiny": "full", "8b_single": "path", "budget_sweep_n32": "path",
+            "budget_sweep_n64": "path", "budget_sweep_n128": "path",
             "budget_sweep_n512": "path", "ragged_serving": "path", "long_context_70b": "path"}
     for name, walk in want.items():
         assert bench.walk_for(wl.CONFIGS[name]) == walk, name
