@@ -45,7 +45,7 @@ constexpr int kVpl = kSegBytes / 16 / 32;       // 16-byte vectors per lane per 
 constexpr int kMaxSegs = 1024;                  // per row
 constexpr int kRingBytes = kWarps * kStages * kSegBytes;  // 192 KB: one CTA per SM
 constexpr int kSmemBytes = kRingBytes + 128;    // (the walks reuse the rings)
-constexpr int kChunksPerWarp = 8;
+constexpr int kChunksPerWarp = 4;  // (ragged_serving T = 1: 133 us at 8, 127 us at 4, 139 us at 2)
 constexpr int kRegRounds = 4;                   // rows of <= 128 segments resolve from registers
 constexpr unsigned kOrphan = 0x80000000u;       // row count flag: the owner has finished
 constexpr uint64_t kLingerNs = 20000;           // a sampler's wait for its last rows

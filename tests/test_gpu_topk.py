@@ -69,3 +69,24 @@ def test_topk_spike_is_top1(cuda_device):
     raw = wl.draft_logits(w).reshape(w.L, w.V)
     idx, _, _ = ops.topk(dev_logits(raw, w.dtype, cuda_device), w.K)
     np.testing.assert_array_equal(host(idx)[:, 0], np.argmax(wl.bf16_to_f32(raw), axis=1))
+
+
+def test_topk_leaves_its_workspace_zero_and_reuses_it_across_sizes(cuda_device):
+    """Every top-K call returns the workspace it used to zero (row counters,
+    row bounds and piece slots), so one workspace serves calls of different
+    sizes one after another; each result still matches the oracle."""
+    w1, w2 = wl.CONFIGS["8b_single"], wl.CONFIGS["long_context_70b"]
+    cases = [(wl.draft_logits(w2).reshape(w2.B * w2.L, w2.V), w2.dtype, 16),
+             (wl.draft_logits(w1).reshape(w1.B * w1.L, w1.V), w1.dtype, w1.K),
+             (wl.draft_logits(w2).reshape(w2.B * w2.L, w2.V)[:5], w2.dtype, 3)]
+    need = max(ops.workspace_size(ops.OP_TOPK, B=r.shape[0], L=1, V=r.shape[1], K=K, dtype=d)
+               for r, d, K in cases)
+    ws = ops.alloc_workspace(need, cuda_device)
+    for raw, dtype, K in cases:
+        o_idx, o_lp64, _, o_lse = oracle.topk(raw, dtype, K)
+        idx, lp, lse = ops.topk(dev_logits(raw, dtype, cuda_device), K, workspace=ws)
+        ops.ddtree_device_check()
+        np.testing.assert_array_equal(host(idx), o_idx)
+        assert np.abs(host(lp) - o_lp64).max() <= TOL
+        assert np.abs(host(lse) - o_lse).max() <= TOL
+        assert int(torch.count_nonzero(ws)) == 0
