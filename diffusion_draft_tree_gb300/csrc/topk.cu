@@ -5,8 +5,8 @@
 //
 // One row = one (sequence, draft position), V logits, cut into 4 KB segments.
 // The flattened (row, segment) list is split into equal chunks, one per warp
-// of a single wave (at least (nseg - 1)/31 segments each, so that a row has at
-// most 32 pieces).  A warp streams its chunk through a private ring of shared-memory
+// of a single wave (at least (nseg - 1)/95 segments each, so that a row has at
+// most 96 pieces).  A warp streams its chunk through a private ring of shared-memory
 // stages filled by bulk copies two segments ahead (no CTA barrier anywhere), and
 // keeps, for the piece of a row it is in:
 //   - each lane's online (max, sum of exponentials);
@@ -22,7 +22,7 @@
 // At the end of a piece the warp publishes (max, sum) and its K keys, and takes
 // the row's ticket; the warp that completes the row merges its pieces: the
 // logsumexp from the (max, sum) pairs, the K best by a K-round tournament over
-// the pieces' sorted lists (one lane per piece), and leaves the row's counter,
+// the pieces' sorted lists (three pieces per lane), and leaves the row's counter,
 // bound and slots at zero (the workspace is all zero again after a call).
 #include <algorithm>
 #include <mutex>
@@ -44,10 +44,11 @@ constexpr int kStages = 3;
 constexpr int kRingBytes = kWarps * kStages * kSegBytes;  // 192 KB
 constexpr int kSmemBytes = kRingBytes + 128;              // + alignment slack
 constexpr int kCap = 96;            // a warp's sorted list (first n) + candidates
-constexpr int kMaxPieces = 32;      // pieces of one row (one per merging lane)
+// A merging lane holds LISTS pieces of a row (1, or 3 when rows are long
+// against the wave: more, shorter pieces), so a row has at most 32 LISTS.
 constexpr int kMaxGridWarps = 2560; // warps of the wave (160 SMs), for the workspace bound
 constexpr int kMaxV = 1 << 24;      // logits per row (element ids and segment counts fit)
-constexpr int kMergeHeads = 8;      // a merging lane's keys held in registers
+constexpr int kMergeHeads = 4;      // keys of each held piece in registers at a time
 
 // Merges (m, s) pairs: s2 rescaled to the larger maximum (exp base 2^(x c)).
 DDT_DEV void ms_combine(float& m, float& s, float m2, float s2, float c) {
@@ -128,7 +129,7 @@ struct Cur {  // a warp's position: chunk c, flattened segment i of [., iend)
 
 // One wave: warp w of CTA b streams chunks w grid + b + k nw, k = 0, 1, ...
 // (spc segments each; the plan makes at most one per warp).
-template <bool BF16>
+template <bool BF16, int LISTS>
 __global__ void __launch_bounds__(kThreads, 1)
 topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int rows, int nseg,
             long spc, bool aligned, int K, TopkWs ws, int32_t* __restrict__ topk_idx,
@@ -171,7 +172,7 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int rows
         x.c += nw;
         return place(x);
     };
-    // chunks that hold a piece of the row (at most kMaxPieces by the plan)
+    // chunks that hold a piece of the row (at most 32 LISTS by the plan)
     auto pieces = [&](int row) -> int {
         return (int)(((long)(row + 1) * nseg - 1) / spc - ((long)row * nseg) / spc + 1);
     };
@@ -179,26 +180,31 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int rows
         return (const char*)logits + (size_t)row * (size_t)row_stride * S::ES;
     };
     // The row's result, by the warp that completed it (its count was acquired,
-    // so every piece's slot is visible).  Lane p holds piece p's (max, sum) and
-    // its sorted keys, kMergeHeads at a time in registers; K rounds of a
-    // tournament take the largest head (the value word, then the index word,
-    // each by one warp reduction), and the winning lane moves to its next key.
-    // Every key of the row's K best is in its piece's list, so the K winners are
-    // the row's K best, in order.
+    // so every piece's slot is visible).  Lane p holds pieces p, p + 32, ...
+    // (LISTS of them): their (max, sum) and their sorted keys, kMergeHeads of
+    // each at a time in registers.  K rounds of a tournament take the largest head (the
+    // value word, then the index word, each by one warp reduction); the piece
+    // that held it moves to its next key.  Every key of the row's K best is in
+    // its piece's list, so the K winners are the row's K best, in order.
     auto merge = [&](int row) {
         const long c_lo = ((long)row * nseg) / spc;
         const int np = pieces(row);
         uint64_t* base = ws.slots + (size_t)(c_lo + row) * (size_t)(1 + K);
-        const uint64_t* mine = base + (size_t)lane * (1 + K);
         float pm = -INFINITY, ps = 0.f;
-        uint64_t hk[kMergeHeads];
+        uint64_t hk[LISTS][kMergeHeads];
+        int used[LISTS];  // keys of each held piece taken so far
 #pragma unroll
-        for (int i = 0; i < kMergeHeads; ++i)
-            hk[i] = (lane < np && i < K) ? __ldcg((const unsigned long long*)mine + 1 + i) : 0ull;
-        if (lane < np) {
-            const float2 h = __ldcg(reinterpret_cast<const float2*>(mine));
-            pm = h.x;
-            ps = h.y;
+        for (int q = 0; q < LISTS; ++q) {
+            const int pc = lane + 32 * q;
+            const uint64_t* sl = base + (size_t)pc * (1 + K);
+#pragma unroll
+            for (int i = 0; i < kMergeHeads; ++i)
+                hk[q][i] = (pc < np && i < K) ? __ldcg((const unsigned long long*)sl + 1 + i) : 0ull;
+            used[q] = 0;
+            if (pc < np) {
+                const float2 h = __ldcg(reinterpret_cast<const float2*>(sl));
+                ms_combine(pm, ps, h.x, h.y, kLog2e);
+            }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -208,25 +214,30 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int rows
         }
         const float M = (pm == -INFINITY) ? 0.f : pm;
         const float logS = logf(ps);
-        int used = 0;  // keys of this lane's piece taken so far
         for (int r = 0; r < K; ++r) {
-            const uint32_t vw = (uint32_t)(hk[0] >> 32);
+            uint64_t best = hk[0][0];
+#pragma unroll
+            for (int q = 1; q < LISTS; ++q) best = umax64(best, hk[q][0]);
+            const uint32_t vw = (uint32_t)(best >> 32);
             const uint32_t vmax = __reduce_max_sync(0xffffffffu, vw);
-            const uint32_t iw = (vw == vmax) ? (uint32_t)hk[0] : 0u;
+            const uint32_t iw = (vw == vmax) ? (uint32_t)best : 0u;
             const uint32_t imax = __reduce_max_sync(0xffffffffu, iw);
             const uint64_t key = ((uint64_t)vmax << 32) | imax;
             if (lane == 0) {
                 topk_idx[(size_t)row * K + r] = (int32_t)key_index(key);
                 topk_logp[(size_t)row * K + r] = (key_value(key) - M) - logS;
             }
-            if (vw == vmax && (uint32_t)hk[0] == imax) {  // the winner (keys are distinct)
 #pragma unroll
-                for (int i = 0; i + 1 < kMergeHeads; ++i) hk[i] = hk[i + 1];
-                hk[kMergeHeads - 1] = 0ull;
-                if (++used % kMergeHeads == 0 && used < K) {  // its next keys (K > 8 only)
+            for (int q = 0; q < LISTS; ++q) {
+                if (hk[q][0] != key) continue;  // (keys are distinct: one piece holds it)
+#pragma unroll
+                for (int i = 0; i + 1 < kMergeHeads; ++i) hk[q][i] = hk[q][i + 1];
+                hk[q][kMergeHeads - 1] = 0ull;
+                if (++used[q] % kMergeHeads == 0 && used[q] < K) {  // its next keys
+                    const uint64_t* sl = base + (size_t)(lane + 32 * q) * (1 + K) + 1 + used[q];
 #pragma unroll
                     for (int i = 0; i < kMergeHeads; ++i)
-                        hk[i] = used + i < K ? __ldcg((const unsigned long long*)mine + 1 + used + i) : 0ull;
+                        hk[q][i] = used[q] + i < K ? __ldcg((const unsigned long long*)sl + i) : 0ull;
                 }
             }
         }
@@ -424,7 +435,7 @@ topk_kernel(const void* __restrict__ logits, int V, int64_t row_stride, int rows
 }
 
 struct Plan {
-    int nseg;
+    int nseg, lists;
     long spc, nchunks;
     int grid;
 };
@@ -449,14 +460,21 @@ int seg_count(int V, int dtype) {
 }
 
 // Equal chunks, one per warp of a one-CTA-per-SM wave, each at least
-// (nseg - 1) / 31 segments long so that no row has more than kMaxPieces pieces.
+// (nseg - 1) / (32 LISTS - 1) segments long so that no row has more than
+// 32 LISTS pieces; LISTS = 3 only where the 32-piece bound is what limits the
+// chunk length (long rows against the wave), since the larger merge costs more.
 Plan topk_plan(int rows, int V, int dtype, int sms) {
     Plan p;
     p.nseg = seg_count(V, dtype);
     const long total = (long)rows * p.nseg;
     const long w = (long)std::min(sms, kMaxGridWarps / kWarps) * kWarps;
     // a row meets at most ceil((nseg - 1) / spc) + 1 chunks
-    p.spc = std::max({1L, (total + w - 1) / w, (long)(p.nseg - 1 + kMaxPieces - 2) / (kMaxPieces - 1)});
+    auto spc_for = [&](int lists) {
+        const long mp = 32L * lists;
+        return std::max({1L, (total + w - 1) / w, (long)(p.nseg - 1 + mp - 2) / (mp - 1)});
+    };
+    p.lists = spc_for(3) < spc_for(1) ? 3 : 1;
+    p.spc = spc_for(p.lists);
     p.nchunks = (total + p.spc - 1) / p.spc;
     p.grid = (int)std::min((long)sms, p.nchunks);
     return p;
@@ -491,7 +509,7 @@ size_t topk_workspace_bytes(int rows, int V, int dtype, int K) {
     return topk_layout(rows, V, dtype, K >= 1 ? K : DDTREE_MAX_K).total;
 }
 
-template <bool BF16>
+template <bool BF16, int LISTS>
 cudaError_t launch_stream(const TopkArgs& a, const Plan& p, bool aligned, TopkWs ws,
                           cudaStream_t s) {
     static std::once_flag once[64];
@@ -500,10 +518,10 @@ cudaError_t launch_stream(const TopkArgs& a, const Plan& p, bool aligned, TopkWs
     cudaGetDevice(&dev);
     std::call_once(once[dev & 63], [&] {
         attr_err[dev & 63] = cudaFuncSetAttribute(
-            topk_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            topk_kernel<BF16, LISTS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     });
     if (attr_err[dev & 63] != cudaSuccess) return attr_err[dev & 63];
-    return launch_pdl(topk_kernel<BF16>, dim3(p.grid), dim3(kThreads), (size_t)kSmemBytes, s,
+    return launch_pdl(topk_kernel<BF16, LISTS>, dim3(p.grid), dim3(kThreads), (size_t)kSmemBytes, s,
                       a.logits, a.V, a.row_stride, a.rows, p.nseg, p.spc, aligned, a.K, ws,
                       a.topk_idx, a.topk_logp, a.lse, a.err);
 }
@@ -516,8 +534,11 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
     char* base = (char*)a.ws;
     const TopkWs ws{(unsigned int*)(base + l.row_cnt), (unsigned long long*)(base + l.row_tau),
                     (uint64_t*)(base + l.slots)};
-    return a.dtype == DDTREE_BF16 ? launch_stream<true>(a, p, aligned, ws, s)
-                                  : launch_stream<false>(a, p, aligned, ws, s);
+    if (a.dtype == DDTREE_BF16)
+        return p.lists == 3 ? launch_stream<true, 3>(a, p, aligned, ws, s)
+                            : launch_stream<true, 1>(a, p, aligned, ws, s);
+    return p.lists == 3 ? launch_stream<false, 3>(a, p, aligned, ws, s)
+                        : launch_stream<false, 1>(a, p, aligned, ws, s);
 }
 
 }  // namespace ddt
