@@ -5,25 +5,29 @@
 //
 // One row = one (sequence, draft position), V logits, cut into 4 KB segments.
 // The flattened (row, segment) list is split into equal chunks, one per warp
-// of a single wave (at least (nseg - 1)/95 segments each, so that a row has at
-// most 96 pieces).  A warp streams its chunk through a private ring of shared-memory
-// stages filled by bulk copies two segments ahead (no CTA barrier anywhere), and
-// keeps, for the piece of a row it is in:
+// of a single wave, long enough that a row meets at most 32 (or, for long rows
+// in small batches, 96) chunks -- its "pieces".  A warp streams its chunk
+// through a private ring of shared-memory stages filled by bulk copies two
+// segments ahead (no CTA barrier anywhere), and keeps, for the piece of a row
+// it is in:
 //   - each lane's online (max, sum of exponentials);
 //   - the piece's K best (value, index) keys, as a sorted list in shared memory
-//     followed by new candidates.  A candidate must beat the list's K-th key;
-//     vectors whose maximum is below it are skipped whole.  Before the list is
-//     full, the K-th largest lane maximum bounds the segment's K-th value from
-//     below (K distinct elements reach it).  Ranking by counting merges
-//     candidates into the list when the buffer fills, after the piece's first
-//     segment and at the piece's end.
-// A piece whose list fills raises a bound shared by the row's pieces (a key
-// that K elements of the row reach), which every piece then filters against.
+//     followed by new candidates.  A candidate must beat the bound: the list's
+//     K-th key, or the row's shared bound if that is larger (before either
+//     exists, the K-th largest lane maximum of the segment, which K distinct
+//     elements reach).  Vectors whose maximum is below the bound are skipped
+//     whole; a passing vector is re-read from its stage and its qualifying
+//     elements placed with a shared-memory add.  Ranking by counting merges
+//     the candidates into the list once 32 have gathered, while the list is
+//     not yet full, and at the piece's end.
+// A piece whose list fills raises the row's shared bound (a key that K
+// elements of the row reach), which every piece then filters against.
 // At the end of a piece the warp publishes (max, sum) and its K keys, and takes
 // the row's ticket; the warp that completes the row merges its pieces: the
 // logsumexp from the (max, sum) pairs, the K best by a K-round tournament over
-// the pieces' sorted lists (three pieces per lane), and leaves the row's counter,
-// bound and slots at zero (the workspace is all zero again after a call).
+// the pieces' sorted lists (one or three pieces per lane), and leaves the
+// row's counter, bound and slots at zero (the workspace is all zero again
+// after a call).
 #include <algorithm>
 #include <mutex>
 
