@@ -4,7 +4,9 @@
 #include <initializer_list>
 #include <mutex>
 
+#include "common.cuh"
 #include "internal.h"
+#include "sm100.cuh"
 
 #include "../../include/ddtree.h"
 
@@ -248,6 +250,33 @@ ddtree_status ddtree_commit(void* k_cache, void* v_cache, int64_t cache_cap, con
     ddt::CommitArgs a{k_cache, v_cache, cache_cap, k_tree, v_tree, accept_len, accepted_nodes,
                       prefix_len, B, L, N, Hkv, D, error_word()};
     return launched(ddt::launch_commit(a, (cudaStream_t)stream));
+}
+
+namespace {
+
+// One warp waits, through the bounded wait every kernel of the library uses, on
+// an mbarrier that nothing arrives on; when the bound passes it records the
+// timeout in the error word and returns, as a kernel whose copy never landed
+// does.
+__global__ void selftest_wait_kernel(uint64_t limit_ns, uint32_t* err) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        ddt::sm100::mbar_init(&bar, 1);
+        ddt::sm100::mbar_init_fence();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0 && !ddt::sm100::mbar_wait(&bar, 0, nullptr, limit_ns))
+        ddt::record_error(err, ddt::ERR_SELFTEST | ddt::ERR_WAIT_TIMEOUT);
+}
+
+}  // namespace
+
+ddtree_status ddtree_selftest_wait(uint32_t limit_us, void* stream) {
+    if (limit_us < 1 || limit_us > 1000000) return DDTREE_ERR_INVALID_ARG;
+    uint32_t* err = error_word();
+    if (!err) return DDTREE_ERR_CUDA;
+    selftest_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((uint64_t)limit_us * 1000ull, err);
+    return launched(cudaGetLastError());
 }
 
 ddtree_status ddtree_device_check(void* stream, uint32_t* detail) {

@@ -21,6 +21,7 @@ enum : uint32_t {
     ERR_ATTN = 0x03000000u,
     ERR_ACCEPT = 0x04000000u,
     ERR_COMMIT = 0x05000000u,
+    ERR_SELFTEST = 0x0F000000u,  // ddtree_selftest_wait
     ERR_BAD_PREFIX_LEN = 0x1,
     ERR_BAD_N_NODES = 0x2,
     ERR_BAD_TREE = 0x3,

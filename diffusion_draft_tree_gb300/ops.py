@@ -63,13 +63,14 @@ def _load() -> ctypes.CDLL:
                                        P, P, P, P, P, P]
     lib.ddtree_topk_noalloc.argtypes = [P, i32, i32, i32, i64, i32, P, P, P, P]
     lib.ddtree_device_check.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.ddtree_selftest_wait.argtypes = [ctypes.c_uint32, P]
     lib.ddtree_last_cuda_error.argtypes = []
     lib.ddtree_last_cuda_error.restype = ctypes.c_char_p
     lib.ddtree_status_str.argtypes = [i32]
     lib.ddtree_status_str.restype = ctypes.c_char_p
     for f in ("ddtree_topk", "ddtree_build", "ddtree_build_heap", "ddtree_tree_attn",
               "ddtree_accept", "ddtree_accept_path", "ddtree_commit", "ddtree_topk_noalloc",
-              "ddtree_device_check"):
+              "ddtree_device_check", "ddtree_selftest_wait"):
         getattr(lib, f).restype = i32
     return lib
 
@@ -200,6 +201,11 @@ def ddtree_commit(k_cache, v_cache, k_tree, v_tree, accept_len, accepted_nodes, 
     _check("ddtree_commit", lib.ddtree_commit(
         _ptr(k_cache), _ptr(v_cache), cap, _ptr(k_tree), _ptr(v_tree), _ptr(accept_len),
         _ptr(accepted_nodes), _ptr(prefix_len), B, L, R - 1, Hkv, D, _stream(stream)))
+
+
+def ddtree_selftest_wait(limit_us: int, stream=None):
+    """Enqueues a bounded wait that runs out (see include/ddtree.h)."""
+    _check("ddtree_selftest_wait", lib.ddtree_selftest_wait(int(limit_us), _stream(stream)))
 
 
 def ddtree_device_check(stream=None) -> int:

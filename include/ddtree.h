@@ -261,9 +261,22 @@ ddtree_status ddtree_commit(void* k_cache, void* v_cache, int64_t cache_cap, con
  * word.  Returns DDTREE_OK, DDTREE_ERR_DEVICE (and the recorded code in
  * *detail when non-null: which kernel and what was wrong), or DDTREE_ERR_CUDA.
  * Code: high byte = kernel (1 top-K, 2 build, 3 tree attention, 4 accept,
- * 5 commit), low byte = reason (1 bad prefix length, 2 bad node count, 3 bad
- * tree or path, 4 a bounded wait timed out, 5 bad input, 6 internal plan). */
+ * 5 commit, 15 ddtree_selftest_wait), low byte = reason (1 bad prefix length,
+ * 2 bad node count, 3 bad tree or path, 4 a bounded wait timed out, 5 bad
+ * input, 6 internal plan). */
 ddtree_status ddtree_device_check(void* stream, uint32_t* detail);
+
+/* Failure-reporting self-test (diagnostics; the paper has no counterpart).
+ * Every wait inside the library's kernels (for a bulk copy to land, for the
+ * tensor core, for another warp's results) is bounded in wall time: when the
+ * bound passes, the kernel records "a bounded wait timed out" in the device
+ * error word and unwinds, leaving the CUDA context usable.  This call enqueues
+ * one warp that waits, through that same bounded wait, on a barrier that
+ * nothing ever signals, with the bound shortened to limit_us microseconds
+ * (1 .. 1000000).  A later ddtree_device_check() returns DDTREE_ERR_DEVICE
+ * with detail 0x0F000004; nothing faults and the wait always ends.
+ * Returns DDTREE_ERR_INVALID_ARG for a limit out of range. */
+ddtree_status ddtree_selftest_wait(uint32_t limit_us, void* stream);
 
 /* Name of the CUDA error behind the calling thread's most recent
  * DDTREE_ERR_CUDA (e.g. "cudaErrorInvalidValue"), or "no error". */

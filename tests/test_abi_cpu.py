@@ -128,3 +128,12 @@ def test_misaligned_element_arrays_rejected(lib):
         assert L.ddtree_accept_path(*common, None) == 1
     # the no-workspace top-K checks the same
     assert L.ddtree_topk_noalloc(ok, 0, 1, 1000, 1000, 4, odd, ok, None, None) == 1
+
+
+def test_selftest_rejects_limits_out_of_range_on_the_host(lib):
+    """Checked before anything is enqueued: no GPU needed."""
+    L = ctypes.CDLL(lib.LIB_PATH)
+    L.ddtree_selftest_wait.argtypes = [ctypes.c_uint32, ctypes.c_void_p]
+    L.ddtree_selftest_wait.restype = ctypes.c_int
+    assert L.ddtree_selftest_wait(0, None) == 1
+    assert L.ddtree_selftest_wait(1000001, None) == 1
