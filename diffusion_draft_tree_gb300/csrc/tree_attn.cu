@@ -51,6 +51,7 @@ constexpr float kRescaleLog2 = 8.f;
 DDT_DEV uint32_t p_col(int kk) { return kk < 6 ? (uint32_t)(kk * 8) : (uint32_t)(96 + (kk - 6) * 8); }
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxSplits = 16;  // KV splits of one unit = CTAs of one cluster
+constexpr int kLptMaxItems = 128;  // (sequence, split) items ranked in each CTA, at most
 // How the KV splits of a unit combine: a single split stores directly; few
 // units run each unit's splits as one cluster and merge on chip; many units
 // (clusters would fragment the schedule) merge through a global workspace.
@@ -92,6 +93,7 @@ struct Params {
     unsigned int* tickets;  // global merge: [B*Hkv*mpairs]
     int B, N, Hq, Hkv, G, W, mtiles, mpairs, tps, smax;
     int merge;              // how the KV splits of a unit combine: kMerge*
+    int lpt;                // non-cluster plans: CTAs ordered longest split first
     int64_t cache_cap;
     float scale_log2;
     uint32_t* err;
@@ -173,23 +175,64 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // CTAs (one cluster; split == rank in it).  Otherwise the tile pairs that
     // read the same KV range are consecutive CTAs, so they run at the same time
     // and the range comes from DRAM once for all of them.
+    // Longest first (p.lpt): the (sequence, split) items are ranked by their key
+    // tiles, descending (ties by item), and CTA r * Hkv * mpairs + ... takes the
+    // item of rank r, so a ragged batch's long splits start in the first wave
+    // and the short ones fill the tail.
     int idx = blockIdx.x;
-    int split, mpair;
+    int split = 0, mpair, g, b = 0;
     if (p.merge == kMergeCluster) {
         split = idx % p.smax;
         idx /= p.smax;
         mpair = idx % p.mpairs;
         idx /= p.mpairs;
+        g = idx % p.Hkv;
+        b = idx / p.Hkv;
+    } else if (p.lpt) {
+        mpair = idx % p.mpairs;
+        idx /= p.mpairs;
+        g = idx % p.Hkv;  // (idx / Hkv: the item's rank, resolved below)
     } else {
         mpair = idx % p.mpairs;
         idx /= p.mpairs;
         split = idx % p.smax;
         idx /= p.smax;
+        g = idx % p.Hkv;
+        b = idx / p.Hkv;
     }
-    const int g = idx % p.Hkv;
-    const int b = idx / p.Hkv;
     const int R = p.N + 1, G = p.G;
     pdl_wait();
+    if (p.merge != kMergeCluster && p.lpt) {
+        // (dynamic shared memory is free until the first copy below is issued)
+        int* s_w = reinterpret_cast<int*>(smem_raw);  // [kLptMaxItems] key tiles
+        int* s_perm = s_w + kLptMaxItems;              // [kLptMaxItems] item of rank r
+        const int items = p.B * p.smax;
+        for (int i = tid; i < items; i += kThreads) {
+            const int bb = i / p.smax, ss = i - bb * p.smax;
+            const int pb = p.prefix_len[bb], nb = p.n_nodes[bb];
+            int w = 0;
+            if (pb >= 0 && pb <= p.cache_cap && nb >= 0 && nb <= p.N) {
+                const int tot = (pb + BN - 1) / BN + (nb + 1 + BN - 1) / BN;
+                w = max(0, min(tot, (ss + 1) * p.tps) - ss * p.tps);
+            }
+            s_w[i] = w;
+        }
+        __syncthreads();
+        for (int i = tid; i < items; i += kThreads) {
+            const int wi = s_w[i];
+            int rk = 0;
+            for (int j = 0; j < items; ++j) {
+                const int wj = s_w[j];
+                rk += (wj > wi || (wj == wi && j < i)) ? 1 : 0;
+            }
+            s_perm[rk] = i;
+        }
+        __syncthreads();
+        const int item = s_perm[idx / p.Hkv];
+        b = item / p.smax;
+        split = item - b * p.smax;
+        __syncthreads();  // (the scratch is read before any copy lands there)
+    }
     const int P = p.prefix_len[b];
     const int n = p.n_nodes[b];
     if (P < 0 || P > p.cache_cap || n < 0 || n > p.N) {  // (the whole cluster exits here)
@@ -1046,6 +1089,7 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
     p.B = a.B; p.N = a.N; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.W = (a.N + 1 + 31) / 32;
     p.mtiles = pl.mtiles; p.mpairs = pl.mpairs; p.tps = pl.tps; p.smax = pl.smax;
     p.merge = pl.merge;
+    p.lpt = (pl.merge != kMergeCluster && (long)a.B * pl.smax <= kLptMaxItems) ? 1 : 0;
     p.cache_cap = a.cache_cap;
     p.scale_log2 = a.scale * kLog2e;
     p.err = a.err;
