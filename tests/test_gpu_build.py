@@ -53,7 +53,10 @@ def _table(rng, B, L, K, ties):
     (1, 5, 3, 0, False),       # root only
     (4, 1, 7, 7, True),        # one position
     (1, 16, 16, 543, True), (1, 16, 16, 544, True), (1, 9, 5, 95, False), (1, 9, 5, 96, False),
-    (5, 16, 8, 63, True), (5, 16, 8, 64, False)])
+    (5, 16, 8, 63, True), (5, 16, 8, 64, False),
+    # 128-thread build with more children than its register cache holds (level 3
+    # recomputes the keys every pass) and an N-th-key select with a tie group
+    (2, 16, 32, 64, False), (2, 16, 32, 64, True), (1, 8, 32, 60, False)])
 @pytest.mark.parametrize("heap", [False, True], ids=["level", "heap"])
 def test_build_edge_cases(cuda_device, B, L, K, N, ties, heap):
     rng = np.random.default_rng(B * 1000 + L * 100 + K * 10 + N)
