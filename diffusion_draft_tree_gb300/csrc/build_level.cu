@@ -17,8 +17,8 @@
 // the top-K step already returns in priority order, so it is written directly.
 //
 // A level never sorts more children than can enter T.  A child enters a full
-// T only by beating its last key; when the children that pass that test
-// (together with T) overflow the budget by many, the N-th largest key of
+// T only by beating its last key; when more children pass that test than the
+// CTA has threads and T cannot take them all, the N-th largest key of
 // T U children is found first by an exact MSB-first radix select over the
 // 64-bit keys (8-bit digits below the bits that all keys share, until at
 // most 32 keys are left in the digit that holds it, which one warp sorts), and
@@ -32,7 +32,9 @@
 // child's key from its parent's score and the position's log-prob).  Once no
 // parent takes part, or no child qualifies, the build stops.  The
 // result -- nodes, their order, fp32 scores formed as parent score +
-// log-prob -- is identical to the heap's.
+// log-prob -- is identical to the heap's.  The outputs are written from T at
+// the end; the ancestor bitmask is built row by row in dynamic shared memory
+// and leaves with coalesced stores.
 //
 // One CTA per sequence (128 threads for budgets up to 64, else 512).  T holds 64-bit keys:
 //   [63:32] orderable fp32 score, [31:27] 31 - depth,
@@ -52,7 +54,7 @@ namespace ddt {
 
 namespace {
 
-constexpr int kCandCap = 2048;  // survivors (<= DDTREE_MAX_N) + the rank sort's copy
+constexpr int kCandCap = 2048;  // survivors (<= DDTREE_MAX_N), then the sorts' second buffer
 constexpr int kRankSortMax = 64;  // batches up to this size are ranked by counting
 constexpr int kBins = 256;  // radix-select digit: 8 bits
 constexpr int kRegKeys = 8;  // child keys a thread keeps in registers over a level
