@@ -25,6 +25,12 @@
 // its peers' partials through distributed shared memory.  Every mbarrier wait
 // is bounded in wall time; a timeout records an error and the CTA unwinds.
 #include <mutex>
+#include <functional>
+#include <algorithm>
+#include <vector>
+#include <tuple>
+#include <queue>
+#include <map>
 
 #include <cudaTypedefs.h>
 
@@ -960,13 +966,56 @@ Plan plan_base(int N, int Hq, int Hkv) {
 
 long plan_units(const Plan& pl, int B, int Hkv) { return (long)B * Hkv * pl.mpairs; }
 
-// Many units fill the GPU without clusters: split only long tile lists, at a
-// quarter of the longest (so that long sequences of a ragged batch do not leave
-// a tail of lone CTAs), and merge through the workspace.
-Plan plan_many(const Plan& base, Tiles t) {
+// Predicted span of `units` units of T key tiles, each cut into splits of tps
+// tiles (the last one shorter), every split a CTA per query-tile pair, the CTAs
+// started longest first on `sms` SMs, each costing tiles + 2 (set-up, merge).
+long lpt_span(long units, int T, int tps, int sms) {
+    std::vector<long> sizes;
+    for (int s0 = 0; s0 < T; s0 += tps) sizes.push_back(std::min(T, s0 + tps) - s0 + 2);
+    std::sort(sizes.begin(), sizes.end(), std::greater<long>());
+    std::priority_queue<long, std::vector<long>, std::greater<long>> sm;
+    for (int i = 0; i < sms; ++i) sm.push(0);
+    long span = 0;
+    for (const long z : sizes)
+        for (long u = 0; u < units; ++u) {
+            const long e = sm.top() + z;
+            sm.pop();
+            sm.push(e);
+            span = std::max(span, e);
+        }
+    return span;
+}
+
+// Many units fill the GPU without clusters: split only long tile lists, into
+// four pieces merged through the workspace.  The pieces are a quarter of the
+// longest list each, unless a longer first three and a short last one pack the
+// SMs' waves better: with the CTAs ordered longest first the short ones fill
+// the last wave (1152 equal CTAs on 152 SMs leave it 40 % empty).  The choice
+// assumes every unit as long as the longest; it is cached per shape.
+Plan plan_many(const Plan& base, Tiles t, long units, int sms) {
     Plan pl = base;
     const int T = t.prefix + t.tree;
     pl.tps = T > 64 ? std::max(32, (T + 3) / 4) : T;
+    if (T > 64 && pl.tps > 32) {
+        static std::mutex mu;
+        static std::map<std::tuple<int, long, int>, int> cache;
+        std::lock_guard<std::mutex> lock(mu);
+        const auto key = std::make_tuple(T, units, sms);
+        const auto it = cache.find(key);
+        if (it != cache.end()) {
+            pl.tps = it->second;
+        } else {
+            long best = lpt_span(units, T, pl.tps, sms);
+            for (int tps = pl.tps + 1; (T + tps - 1) / tps == 4; ++tps) {
+                const long span = lpt_span(units, T, tps, sms);
+                if (span * 100 < best * 98) {  // a clear gain only
+                    best = span;
+                    pl.tps = tps;
+                }
+            }
+            cache[key] = pl.tps;
+        }
+    }
     pl.smax = (T + pl.tps - 1) / pl.tps;
     pl.merge = pl.smax > 1 ? kMergeGlobal : kMergeNone;
     return pl;
@@ -1058,7 +1107,7 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
     const Tiles t = max_tiles(a.N, a.cache_cap);
     const long units = plan_units(base, a.B, a.Hkv);
     const int sms = num_sms();
-    const Plan pl = units >= sms ? plan_many(base, t)
+    const Plan pl = units >= sms ? plan_many(base, t, units, sms)
                                  : plan_few(base, t, units, sms,
                                             [&](int S) {
                                                 return Cfg<D>::recv_fits_upto(S) ? active_clusters<D>(dev, S) : 0;
@@ -1106,7 +1155,8 @@ cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
 size_t attn_workspace_bytes(int B, int N, int Hq, int Hkv, int D, int64_t cache_cap) {
     const Plan base = plan_base(N, Hq, Hkv);
     if (plan_units(base, B, Hkv) < num_sms()) return 0;
-    return attn_layout(plan_many(base, max_tiles(N, cache_cap)), B, Hkv, D).total;
+    return attn_layout(plan_many(base, max_tiles(N, cache_cap), plan_units(base, B, Hkv), num_sms()),
+                       B, Hkv, D).total;
 }
 
 cudaError_t launch_tree_attn(const AttnArgs& a, cudaStream_t s) {
