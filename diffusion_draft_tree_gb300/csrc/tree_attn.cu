@@ -990,8 +990,10 @@ long lpt_span(long units, int T, int tps, int sms) {
 // four pieces merged through the workspace.  The pieces are a quarter of the
 // longest list each, unless a longer first three and a short last one pack the
 // SMs' waves better: with the CTAs ordered longest first the short ones fill
-// the last wave (1152 equal CTAs on 152 SMs leave it 40 % empty).  The choice
-// assumes every unit as long as the longest; it is cached per shape.
+// the last wave (1152 equal CTAs on 152 SMs leave it 40 % empty).  Every size
+// up to just under a third is scored by lpt_span, and the best is taken when
+// it beats the quarter by at least 2 %.  The choice assumes every unit as long
+// as the longest; it is cached per shape.
 Plan plan_many(const Plan& base, Tiles t, long units, int sms) {
     Plan pl = base;
     const int T = t.prefix + t.tree;
@@ -1005,14 +1007,17 @@ Plan plan_many(const Plan& base, Tiles t, long units, int sms) {
         if (it != cache.end()) {
             pl.tps = it->second;
         } else {
-            long best = lpt_span(units, T, pl.tps, sms);
+            const long quarter = lpt_span(units, T, pl.tps, sms);
+            long best = quarter;
+            int best_tps = pl.tps;
             for (int tps = pl.tps + 1; (T + tps - 1) / tps == 4; ++tps) {
                 const long span = lpt_span(units, T, tps, sms);
-                if (span * 100 < best * 98) {  // a clear gain only
+                if (span < best) {
                     best = span;
-                    pl.tps = tps;
+                    best_tps = tps;
                 }
             }
+            if (best * 100 < quarter * 98) pl.tps = best_tps;  // a clear gain only
             cache[key] = pl.tps;
         }
     }
